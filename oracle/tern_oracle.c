@@ -1,0 +1,270 @@
+/*
+ * Ternary-weight linear layer: CPU ORACLE.  TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the plain, slow, obviously-correct definition that the CUDA
+ * path is checked against.  Only tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load it.  It shares no code, header, table or constant
+ * with the CUDA library, and never calls it.
+ *
+ * What it computes (all citations name a web page and a section on it):
+ *
+ *  - Ternary weights w in {-1, 0, +1} with one fp16 scale per 128 consecutive
+ *    weights along K ("NInfer sm_89 fork" write-up, 2kiu.com/news/5424991,
+ *    section 9 "why NInfer is fast", item 2 "ternary weights": codes plus one
+ *    FP16 scale per 128 weights).
+ *
+ *  - 2-bit packing.  The pages pack base-3 trits five to a byte; this layer
+ *    stores one trit digit (w + 1, the digit a base-3 packing also stores) in a
+ *    2-bit field instead.  Word n*(K/16) + k/16 of the packed matrix holds
+ *    weight (n, k) in bits 2*(k%16) .. 2*(k%16)+1:
+ *        code 0 -> -1,  code 1 -> 0,  code 2 -> +1,  code 3 -> invalid.
+ *
+ *  - bf16 rungs (T <= 16):  y[t,n] = sum_g s[n,g] * sum_{k in g} w[n,k] x[t,k]
+ *    accumulated in fp64 here; m[t,n] = sum_k |s w x| is the tolerance scale.
+ *
+ *  - s8 rung (T >= 17): per token a = max_k |x|, xs = a / 127 (fp32),
+ *    q = clamp(rint(x / xs), -127, 127) with round-to-nearest-even, then
+ *    acc[t,n,g] = sum_{k in g} q w exactly in integers and
+ *    y = xs * sum_g s * acc (fp64 here).  Int8 activations x ternary-as-int8
+ *    weights with int32 accumulation is the "s8" prefill rung of the
+ *    "ninfer-perf-tuning" skill page (markdownregistry.com), section 2 rung map
+ *    and section 4 numeric gate; per-token absmax/127 with round-to-nearest-even
+ *    is the reading of "quantised per token to int8".
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - the 2-bit code is the offset digit w+1 (linear in w);
+ *  - the quantiser divides by xs = a/127 in IEEE fp32 and clamps to +-127;
+ *  - a token whose absmax is 0 gets xs = 0 and q = 0.
+ *
+ * Build: plain C11, no fast-math, optional OpenMP over output rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- scalar conversions (exact widenings) ------------------------------ */
+
+/* bf16 -> fp32 is the upper 16 bits of an fp32: exact. */
+static float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* IEEE binary16 -> double, written out from the format definition:
+ * sign(1) exponent(5, bias 15) fraction(10); subnormals when exponent == 0. */
+static double f16_to_f64(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -24); /* f * 2^-10 * 2^-14 */
+  else if (e == 31)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+  return sign ? -v : v;
+}
+
+/* ---- packing ------------------------------------------------------------ */
+
+/* Weight (n, k) from the packed matrix; returns 2 for the invalid code 3 so
+ * that callers can count it. */
+static int unpack_one(const uint32_t* wp, int K, int n, int k) {
+  uint32_t word = wp[(size_t)n * (size_t)(K / 16) + (size_t)(k / 16)];
+  int code = (int)((word >> (2 * (k % 16))) & 3u);
+  return code - 1; /* 0->-1, 1->0, 2->+1, 3->2 (invalid) */
+}
+
+/* W [N][K] int8 in {-1,0,1} -> packed [N][K/16] u32.  Values outside
+ * {-1,0,1} are stored as 0 and counted; the count is returned. */
+long tern_oracle_pack(const int8_t* W, int K, int N, uint32_t* wp) {
+  long bad = 0;
+  size_t words = (size_t)N * (size_t)(K / 16);
+  memset(wp, 0, words * sizeof(uint32_t));
+  for (int n = 0; n < N; ++n) {
+    for (int k = 0; k < K; ++k) {
+      int w = W[(size_t)n * K + k];
+      if (w < -1 || w > 1) {
+        ++bad;
+        w = 0;
+      }
+      uint32_t code = (uint32_t)(w + 1);
+      wp[(size_t)n * (K / 16) + k / 16] |= code << (2 * (k % 16));
+    }
+  }
+  return bad;
+}
+
+/* packed -> W [N][K] int8; invalid codes become 0 and are counted. */
+long tern_oracle_unpack(const uint32_t* wp, int K, int N, int8_t* W) {
+  long bad = 0;
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) {
+      int w = unpack_one(wp, K, n, k);
+      if (w == 2) {
+        ++bad;
+        w = 0;
+      }
+      W[(size_t)n * K + k] = (int8_t)w;
+    }
+  return bad;
+}
+
+/* ---- bf16 rungs: plain fp64 definition ----------------------------------- */
+
+/* y[t][n] = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k]   (fp64)
+ * m[t][n] = sum_g sum_{k in g} |s[n][g] * w[n][k] * x[t][k]|  (fp64)
+ * scales: fp16 bits [N][K/128]; x: bf16 bits [T][K].  m may be NULL.
+ * Rows n are independent, so they are split across threads; each output is a
+ * single sequential sum in k order. */
+void tern_oracle_linear_f64(const uint32_t* wp, const uint16_t* scales,
+                            const uint16_t* x, int T, int K, int N, double* y,
+                            double* m) {
+  int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int n = 0; n < N; ++n) {
+    for (int t = 0; t < T; ++t) {
+      double acc = 0.0, mag = 0.0;
+      for (int g = 0; g < G; ++g) {
+        double s = f16_to_f64(scales[(size_t)n * G + g]);
+        double part = 0.0, partm = 0.0;
+        for (int k = g * 128; k < (g + 1) * 128; ++k) {
+          int w = unpack_one(wp, K, n, k);
+          double xv = (double)bf16_to_f32(x[(size_t)t * K + k]);
+          part += (double)w * xv;
+          partm += fabs((double)w * xv);
+        }
+        acc += s * part;
+        mag += fabs(s) * partm;
+      }
+      y[(size_t)t * N + n] = acc;
+      if (m) m[(size_t)t * N + n] = mag;
+    }
+  }
+}
+
+/* Same definition for a list of sampled outputs (t_idx[i], n_idx[i]). */
+void tern_oracle_linear_f64_sampled(const uint32_t* wp, const uint16_t* scales,
+                                    const uint16_t* x, int K, int N,
+                                    const int* t_idx, const int* n_idx,
+                                    long count, double* y, double* m) {
+  int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 64)
+  for (long i = 0; i < count; ++i) {
+    int t = t_idx[i], n = n_idx[i];
+    double acc = 0.0, mag = 0.0;
+    for (int g = 0; g < G; ++g) {
+      double s = f16_to_f64(scales[(size_t)n * G + g]);
+      double part = 0.0, partm = 0.0;
+      for (int k = g * 128; k < (g + 1) * 128; ++k) {
+        int w = unpack_one(wp, K, n, k);
+        double xv = (double)bf16_to_f32(x[(size_t)t * K + k]);
+        part += (double)w * xv;
+        partm += fabs((double)w * xv);
+      }
+      acc += s * part;
+      mag += fabs(s) * partm;
+    }
+    y[i] = acc;
+    if (m) m[i] = mag;
+  }
+  (void)N;
+}
+
+/* ---- s8 rung ------------------------------------------------------------- */
+
+/* Per-token int8 quantisation, fp32 arithmetic:
+ *   a  = max_k |x[t][k]|
+ *   xs = a / 127.0f                       (IEEE single division)
+ *   q  = clamp(rintf(x / xs), -127, 127)  (rintf: round to nearest even)
+ * a == 0 gives xs = 0 and q = 0. */
+void tern_oracle_quant_s8(const uint16_t* x, int T, int K, int8_t* q,
+                          float* xs) {
+  for (int t = 0; t < T; ++t) {
+    float a = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float v = fabsf(bf16_to_f32(x[(size_t)t * K + k]));
+      if (v > a) a = v;
+    }
+    float scale = a / 127.0f;
+    xs[t] = scale;
+    for (int k = 0; k < K; ++k) {
+      float r = 0.0f;
+      if (a > 0.0f) {
+        r = rintf(bf16_to_f32(x[(size_t)t * K + k]) / scale);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+      }
+      q[(size_t)t * K + k] = (int8_t)r;
+    }
+  }
+}
+
+/* Exact per-group integer accumulators and the fp64 output:
+ *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]          (int64, exact)
+ *   y[t][n]      = xs[t] * sum_g s[n][g] * acc[t][n][g]    (fp64)
+ *   m[t][n]      = xs[t] * sum_g |s[n][g] * acc[t][n][g]|  (tolerance scale)
+ * acc and m may be NULL. */
+void tern_oracle_linear_s8(const uint32_t* wp, const uint16_t* scales,
+                           const int8_t* q, const float* xs, int T, int K,
+                           int N, int64_t* acc, double* y, double* m) {
+  int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int n = 0; n < N; ++n) {
+    for (int t = 0; t < T; ++t) {
+      double sum = 0.0, mag = 0.0;
+      for (int g = 0; g < G; ++g) {
+        int64_t a = 0;
+        for (int k = g * 128; k < (g + 1) * 128; ++k)
+          a += (int64_t)q[(size_t)t * K + k] * (int64_t)unpack_one(wp, K, n, k);
+        if (acc) acc[((size_t)t * N + n) * G + g] = a;
+        double s = f16_to_f64(scales[(size_t)n * G + g]);
+        sum += s * (double)a;
+        mag += fabs(s * (double)a);
+      }
+      y[(size_t)t * N + n] = (double)xs[t] * sum;
+      if (m) m[(size_t)t * N + n] = fabs((double)xs[t]) * mag;
+    }
+  }
+}
+
+/* Same for sampled outputs. */
+void tern_oracle_linear_s8_sampled(const uint32_t* wp, const uint16_t* scales,
+                                   const int8_t* q, const float* xs, int K,
+                                   int N, const int* t_idx, const int* n_idx,
+                                   long count, int64_t* acc, double* y,
+                                   double* m) {
+  int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 64)
+  for (long i = 0; i < count; ++i) {
+    int t = t_idx[i], n = n_idx[i];
+    double sum = 0.0, mag = 0.0;
+    for (int g = 0; g < G; ++g) {
+      int64_t a = 0;
+      for (int k = g * 128; k < (g + 1) * 128; ++k)
+        a += (int64_t)q[(size_t)t * K + k] * (int64_t)unpack_one(wp, K, n, k);
+      if (acc) acc[(size_t)i * G + g] = a;
+      double s = f16_to_f64(scales[(size_t)n * G + g]);
+      sum += s * (double)a;
+      mag += fabs(s * (double)a);
+    }
+    y[i] = (double)xs[t] * sum;
+    if (m) m[i] = fabs((double)xs[t]) * mag;
+  }
+  (void)N;
+}
+
+int tern_oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,300 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a hand-derived fixture, a brute-force
+loop written independently here (Python integers / fractions, numpy's own
+float16 and bfloat16 widening), a closed form, or an invariant.  A dropped
+term, a wrong sign or group index, a transposed operand or a wrong bit order
+in the oracle fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([p.strip() for p in line.split("|")])
+    return rows
+
+
+def _bf16_value(bits):
+    """bf16 bits -> exact Python float, independently of the oracle."""
+    return float(np.array([int(bits) << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def _bf16_bits_exact(values):
+    """Python floats that are exactly representable in bf16 -> bf16 bits."""
+    f = np.asarray(values, dtype=np.float32)
+    bits = f.view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0), "value not exactly representable in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def _brute_linear(W, s, xb):
+    """y[t][n] = sum_g s[n,g] * sum_{k in g} w[n,k] x[t,k], with exact rationals."""
+    N, K = W.shape
+    T = xb.shape[0]
+    G = K // 128
+    y = np.zeros((T, N))
+    for t in range(T):
+        xs = [Fraction(_bf16_value(b)) for b in xb[t]]
+        for n in range(N):
+            tot = Fraction(0)
+            for g in range(G):
+                part = Fraction(0)
+                for k in range(g * 128, (g + 1) * 128):
+                    w = int(W[n, k])
+                    if w:
+                        part += w * xs[k]
+                tot += Fraction(float(s[n, g])) * part
+            y[t, n] = float(tot)
+    return y
+
+
+# ---------------------------------------------------------------- packing
+
+def test_pack_layout_golden_words():
+    for name, ws, word in _read_fixture("pack_layout.txt"):
+        w = np.array([int(v) for v in ws.split(",")], dtype=np.int8).reshape(1, 16)
+        wp, bad = oracle.pack(w)
+        assert bad == 0
+        assert int(wp[0, 0]) == int(word, 16), name
+        back, bad2 = oracle.unpack(wp, 16)
+        assert bad2 == 0 and np.array_equal(back, w), name
+
+
+def test_pack_word_and_row_order():
+    # Two rows, K = 48: word index n*(K/16) + k/16.  One nonzero weight per row
+    # at a hand-chosen position; every other field is 0b01.
+    W = np.zeros((2, 48), dtype=np.int8)
+    W[0, 17] = -1   # word 1 of row 0, field 1 -> 0x55555551
+    W[1, 40] = 1    # word 2 of row 1, field 8 -> 0x55565555
+    wp, _ = oracle.pack(W)
+    expect = np.full((2, 3), 0x55555555, dtype=np.uint32)
+    expect[0, 1] = 0x55555551
+    expect[1, 2] = 0x55565555
+    assert np.array_equal(wp, expect)
+
+
+def test_pack_unpack_round_trip_random():
+    W = synth.ternary_weights(7, 256, 0.4, seed=11)
+    wp, bad = oracle.pack(W)
+    assert bad == 0
+    back, bad2 = oracle.unpack(wp, 256)
+    assert bad2 == 0 and np.array_equal(back, W)
+
+
+def test_pack_counts_invalid_values():
+    W = np.zeros((1, 16), dtype=np.int8)
+    W[0, 3] = 2
+    W[0, 9] = -5
+    wp, bad = oracle.pack(W)
+    assert bad == 2
+    assert int(wp[0, 0]) == 0x55555555  # invalid values stored as 0
+
+
+def test_unpack_counts_invalid_code():
+    wp = np.array([[0x55555555 | (3 << 6)]], dtype=np.uint32)  # field 3 = 0b11
+    W, bad = oracle.unpack(wp, 16)
+    assert bad == 1 and W[0, 3] == 0
+
+
+# ---------------------------------------------------------------- bf16 rungs
+
+@pytest.mark.parametrize("T,K,N", [(1, 128, 3), (3, 256, 5), (2, 384, 4)])
+def test_linear_f64_brute_force(T, K, N):
+    W = synth.ternary_weights(N, K, 0.4, seed=T * 100 + N)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=T + N)
+    x = synth.activations(T, K, seed=N, outlier_frac=0.02)
+    wp, _ = oracle.pack(W)
+    y, m = oracle.linear_f64(wp, s, x, T, K, N)
+    yb = _brute_linear(W, s, x)
+    np.testing.assert_allclose(y, yb, rtol=1e-12, atol=1e-15)
+    # m = sum |s w x|, brute-forced with numpy's own widenings
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    sf = np.repeat(s.astype(np.float64), 128, axis=1)
+    mb = np.abs(xf[:, None, :] * (W[None, :, :] * sf[None, :, :])).sum(-1)
+    np.testing.assert_allclose(m, mb, rtol=1e-12)
+
+
+def test_linear_f64_zero_weights_give_zero():
+    T, K, N = 2, 256, 6
+    W = np.zeros((N, K), dtype=np.int8)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=1)
+    x = synth.activations(T, K, seed=2)
+    wp, _ = oracle.pack(W)
+    y, m = oracle.linear_f64(wp, s, x, T, K, N)
+    assert np.all(y == 0.0) and np.all(m == 0.0)
+
+
+def test_linear_f64_all_plus_one_is_scaled_group_sums():
+    T, K, N = 2, 384, 3
+    W = np.ones((N, K), dtype=np.int8)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=3)
+    x = synth.activations(T, K, seed=4)
+    wp, _ = oracle.pack(W)
+    y, _ = oracle.linear_f64(wp, s, x, T, K, N)
+    xf = [[_bf16_value(b) for b in row] for row in x]
+    for t in range(T):
+        for n in range(N):
+            expect = math.fsum(float(s[n, g]) * math.fsum(xf[t][g * 128:(g + 1) * 128])
+                               for g in range(K // 128))
+            assert y[t, n] == pytest.approx(expect, rel=1e-13, abs=1e-15)
+
+
+def test_linear_f64_one_hot_selects_one_weight():
+    T, K, N = 1, 512, 8
+    W = synth.ternary_weights(N, K, 1.0 / 3.0, seed=5)
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=6)
+    wp, _ = oracle.pack(W)
+    for k0 in (0, 127, 128, 300, 511):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k0] = _bf16_bits_exact([1.0])[0]
+        y, _ = oracle.linear_f64(wp, s, x, T, K, N)
+        expect = s[:, k0 // 128].astype(np.float64) * W[:, k0]
+        assert np.array_equal(y[0], expect), k0
+
+
+def test_linear_f64_negation_and_additivity():
+    T, K, N = 2, 256, 5
+    W = synth.ternary_weights(N, K, 0.4, seed=7)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=8)
+    wp, _ = oracle.pack(W)
+    rng = np.random.default_rng(9)
+    a = rng.integers(-8, 9, size=(T, K)).astype(np.float32)
+    b = rng.integers(-8, 9, size=(T, K)).astype(np.float32)
+    ya, _ = oracle.linear_f64(wp, s, _bf16_bits_exact(a), T, K, N)
+    yb, _ = oracle.linear_f64(wp, s, _bf16_bits_exact(b), T, K, N)
+    yab, _ = oracle.linear_f64(wp, s, _bf16_bits_exact(a + b), T, K, N)
+    yneg, _ = oracle.linear_f64(wp, s, _bf16_bits_exact(-a), T, K, N)
+    np.testing.assert_allclose(yab, ya + yb, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(yneg, -ya)
+
+
+def test_linear_f64_sampled_matches_full():
+    T, K, N = 3, 256, 9
+    c = synth.case("x", T, K=K, N=N, seed=12)
+    wp, _ = oracle.pack(c.W)
+    y, m = oracle.linear_f64(wp, c.scales, c.x, T, K, N)
+    ti = np.array([0, 2, 1, 2], dtype=np.int32)
+    ni = np.array([8, 0, 4, 8], dtype=np.int32)
+    ys, ms = oracle.linear_f64_sampled(wp, c.scales, c.x, K, N, ti, ni)
+    assert np.array_equal(ys, y[ti, ni]) and np.array_equal(ms, m[ti, ni])
+
+
+# ---------------------------------------------------------------- s8 quantiser
+
+def test_quant_s8_golden_ties():
+    for name, xs_txt, q_txt, scale_txt in _read_fixture("quant_ties.txt"):
+        xv = [float(v) for v in xs_txt.split(",")]
+        qv = np.array([int(v) for v in q_txt.split(",")], dtype=np.int8)
+        q, xs = oracle.quant_s8(_bf16_bits_exact(xv).reshape(1, -1), 1, len(xv))
+        assert np.array_equal(q[0], qv), name
+        assert float(xs[0]) == float(scale_txt), name
+
+
+def test_quant_s8_properties_random():
+    T, K = 5, 1024
+    x = synth.activations(T, K, seed=21, outlier_frac=0.01)
+    q, xs = oracle.quant_s8(x, T, K)
+    xf = synth.bf16_bits_to_f32(x)
+    for t in range(T):
+        a = float(np.max(np.abs(xf[t])))
+        # x_scale is the fp32 quotient a/127 (numpy's IEEE float32 division)
+        assert xs[t] == np.float32(a) / np.float32(127.0)
+        # the absmax channel maps to +-127
+        k = int(np.argmax(np.abs(xf[t])))
+        assert abs(int(q[t, k])) == 127 and np.sign(q[t, k]) == np.sign(xf[t, k])
+        # every code is within half a step of x / x_scale
+        err = np.abs(q[t].astype(np.float64) - xf[t].astype(np.float64) / float(xs[t]))
+        assert np.all(err <= 0.5 + 1e-6)
+        assert np.all(np.abs(q[t]) <= 127)
+
+
+def test_quant_s8_integer_rows_are_identity():
+    # Integer rows holding +-127 quantise to themselves (x_scale = 1).
+    rng = np.random.default_rng(22)
+    x = rng.integers(-127, 128, size=(3, 256)).astype(np.float32)
+    x[:, 7] = 127.0
+    x[1, 7] = -127.0
+    q, xs = oracle.quant_s8(_bf16_bits_exact(x), 3, 256)
+    assert np.all(xs == 1.0)
+    assert np.array_equal(q.astype(np.float32), x)
+
+
+# ---------------------------------------------------------------- s8 linear
+
+@pytest.mark.parametrize("T,K,N", [(1, 128, 4), (3, 256, 5)])
+def test_linear_s8_brute_force(T, K, N):
+    W = synth.ternary_weights(N, K, 0.4, seed=31 + T)
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=32)
+    x = synth.activations(T, K, seed=33, outlier_frac=0.01)
+    wp, _ = oracle.pack(W)
+    q, xs = oracle.quant_s8(x, T, K)
+    y, m, acc = oracle.linear_s8(wp, s, q, xs, T, K, N, want_acc=True)
+    G = K // 128
+    for t in range(T):
+        for n in range(N):
+            tot = Fraction(0)
+            for g in range(G):
+                a = sum(int(q[t, k]) * int(W[n, k]) for k in range(g * 128, (g + 1) * 128))
+                assert acc[t, n, g] == a
+                tot += Fraction(float(s[n, g])) * a
+            expect = float(Fraction(float(xs[t])) * tot)
+            assert y[t, n] == pytest.approx(expect, rel=1e-12, abs=1e-300)
+
+
+def test_linear_s8_unit_scale_integer_trick():
+    # scales = 1 and integer activations containing +-127: q = x, x_scale = 1,
+    # so y must equal the exact integer dot product.
+    T, K, N = 2, 384, 6
+    W = synth.ternary_weights(N, K, 0.4, seed=41)
+    s = np.ones((N, K // 128), dtype=np.float16)
+    rng = np.random.default_rng(42)
+    x = rng.integers(-127, 128, size=(T, K)).astype(np.float32)
+    x[:, 0] = 127.0
+    wp, _ = oracle.pack(W)
+    q, xs = oracle.quant_s8(_bf16_bits_exact(x), T, K)
+    y, _, _ = oracle.linear_s8(wp, s, q, xs, T, K, N)
+    exact = x.astype(np.int64) @ W.astype(np.int64).T
+    assert np.array_equal(y, exact.astype(np.float64))
+
+
+def test_linear_s8_sampled_matches_full():
+    T, K, N = 2, 256, 7
+    c = synth.case("x", T, K=K, N=N, seed=43)
+    wp, _ = oracle.pack(c.W)
+    q, xs = oracle.quant_s8(c.x, T, K)
+    y, m, acc = oracle.linear_s8(wp, c.scales, q, xs, T, K, N, want_acc=True)
+    ti = np.array([1, 0, 1], dtype=np.int32)
+    ni = np.array([6, 3, 0], dtype=np.int32)
+    ys, ms, accs = oracle.linear_s8_sampled(wp, c.scales, q, xs, K, N, ti, ni, want_acc=True)
+    assert np.array_equal(ys, y[ti, ni]) and np.array_equal(ms, m[ti, ni])
+    assert np.array_equal(accs, acc[ti, ni])
+
+
+# ---------------------------------------------------------------- generators
+
+def test_synth_distributions():
+    W = synth.ternary_weights(64, 4096, 0.4, seed=0)
+    frac0 = float(np.mean(W == 0))
+    assert abs(frac0 - 0.4) < 0.01
+    assert abs(float(np.mean(W == 1)) - 0.3) < 0.01
+    s = synth.scales_lognormal(64, 4096, -3.5, 0.3, seed=0).astype(np.float64)
+    assert abs(np.mean(np.log(s)) + 3.5) < 0.05
+    x = synth.bf16_bits_to_f32(synth.activations(4, 5120, seed=0, outlier_frac=0.01))
+    big = np.abs(x).max(axis=0) > 10
+    assert 30 <= int(big.sum()) <= 51  # 51 outlier channels; a few may draw small values
