@@ -1,0 +1,149 @@
+/*
+ * tern.h — C ABI of the ternary-weight linear layer for one GB300 (sm_103a).
+ *
+ * The layer computes y = x W^T for ternary weights W in {-1, 0, +1} with one
+ * fp16 scale per 128 consecutive weights along K, for T tokens of bf16
+ * activations.  Three token bands, each served by its own kernel ("rung"):
+ *   T = 1        decode GEMV                           rung "gemv"
+ *   T = 2..8     speculative-verify small-T tile       rung "small_t"
+ *   T = 9..16    two small-T token tiles per weight    rung "small_t_tiled"
+ *   T >= 17      int8 per-token activations ("s8")     rung "s8"
+ * The band map, the env override and the per-rung probe follow the rung map
+ * and the probe discipline of the "ninfer-perf-tuning" skill page
+ * (markdownregistry.com), section 2 ("which rung ran" and its rung-map
+ * table); the format follows the "NInfer sm_89 fork" write-up
+ * (2kiu.com/news/5424991), section 9 item 2 (ternary codes plus one FP16
+ * scale per 128 weights; int8 activations with m16n8k32 int8 MMA for prefill).
+ *
+ * Conventions for every entry point
+ *  - All array arguments are DEVICE pointers of the current CUDA device, owned
+ *    by the caller.  The library never allocates or frees device memory.
+ *  - `stream` is a cudaStream_t (passed as void*; NULL = legacy default
+ *    stream).  Calls are asynchronous on that stream and never synchronise.
+ *  - Row-major, densely packed layouts; element types are given as bit
+ *    patterns so that this header needs no CUDA headers:
+ *      bf16 = uint16_t (upper half of an IEEE fp32), fp16 = uint16_t (IEEE
+ *      binary16), fp32 = float.
+ *  - Every pointer must be 16-byte aligned (TERN_EALIGN otherwise).
+ *  - Errors are returned as a negative tern_status; nothing aborts.  Launch
+ *    failures return TERN_ECUDA.  Asynchronous device-side failures (a bounded
+ *    wait that ran out) are recorded in a per-device error word read by
+ *    tern_device_status().
+ *
+ * Packed weight layout (this library's format; the pages pack base-3 trits
+ * five to a byte, this format keeps the same trit digit in 2 bits):
+ *   Wpacked is uint32 [N][K/16].  Word n*(K/16) + k/16 holds weight (n, k) in
+ *   bits 2*(k%16) .. 2*(k%16)+1 as the digit c = w + 1:
+ *       c = 0 -> w = -1,   c = 1 -> w = 0,   c = 2 -> w = +1,   c = 3 invalid.
+ *   tern_pack never writes c = 3; the linear kernels do not check for it
+ *   (it is decoded as w = +2).
+ * Scales: fp16 [N][K/128], scale (n, g) applies to k in [128g, 128g+128).
+ */
+#ifndef TERN_H_
+#define TERN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TERN_OK = 0,
+  TERN_EINVAL = -1,   /* bad size / null pointer / unsupported shape */
+  TERN_EALIGN = -2,   /* a pointer is not 16-byte aligned */
+  TERN_ENOSPACE = -3, /* workspace smaller than tern_linear_workspace_bytes() */
+  TERN_ENODEV = -4,   /* no usable sm_103 device current */
+  TERN_ECUDA = -5,    /* a CUDA runtime call or launch failed */
+  TERN_ETIMEOUT = -6  /* a device-side bounded wait ran out (see tern_device_status) */
+} tern_status;
+
+/* Rung identifiers (tern_select_rung / tern_last_rung_id). */
+typedef enum {
+  TERN_RUNG_GEMV = 0,
+  TERN_RUNG_SMALL_T = 1,
+  TERN_RUNG_SMALL_T_TILED = 2,
+  TERN_RUNG_S8 = 3
+} tern_rung;
+
+/* Pack ternary int8 weights into the 2-bit layout above.
+ *   W        device int8 [N][K], values in {-1, 0, +1}
+ *   Wpacked  device uint32 [N][K/16], written
+ *   K, N     K > 0 and K % 16 == 0; N > 0
+ *   bad_count optional device int32; if not NULL, the number of inputs outside
+ *            {-1, 0, +1} is ADDED to *bad_count (those inputs are packed as 0).
+ * Format: "NInfer sm_89 fork" write-up, section 9 item 2 (ternary codes with
+ * per-128 fp16 scales), 2-bit reading of its base-3 digit. */
+int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count,
+              void* stream);
+
+/* Per-token int8 quantisation of bf16 activations ("s8" rung input).
+ *   x        device bf16 [T][K]
+ *   q        device int8 [T][K], written: clamp(rint(x / x_scale), -127, 127),
+ *            rint = round to nearest even
+ *   x_scale  device fp32 [T], written: max_k |x[t][k]| / 127 (IEEE fp32
+ *            division); a token whose absmax is 0 gets x_scale 0 and q 0.
+ *   T > 0, K > 0, K % 16 == 0.
+ * Source: int8 activations for the prefill rung, "NInfer sm_89 fork" write-up
+ * section 9 item 2 and the "s8" rung of the "ninfer-perf-tuning" skill page
+ * section 2; absmax/127 with round-to-nearest-even is the reading of
+ * "quantised per token". */
+int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T,
+                      int K, void* stream);
+
+/* Bytes of device workspace tern_linear needs for (T, K, N) under the rung the
+ * dispatcher would pick right now (and under any forced rung: the value
+ * covers every rung).  0 means no workspace is needed.  Host-only. */
+size_t tern_linear_workspace_bytes(int T, int K, int N);
+
+/* y = x W^T with group scales:
+ *   y[t][n] = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k]
+ * on the bf16 rungs (fp32 accumulation; |y - y_exact| within
+ * 1e-3 * sum|s w x| + 1e-6), and on the s8 rung (T >= 17)
+ *   q, xs = tern_quant_act_s8(x)
+ *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]   (exact integers)
+ *   y[t][n]      = xs[t] * sum_g s[n][g] * acc[t][n][g]   (fp32).
+ *   Wpacked  device uint32 [N][K/16] (layout above), read-only
+ *   scales   device fp16 [N][K/128], read-only
+ *   x        device bf16 [T][K], read-only
+ *   y        device fp32 [T][N], written (fully overwritten)
+ *   T >= 1, K >= 128 with K % 128 == 0, N >= 1
+ *   workspace, workspace_bytes: device scratch of at least
+ *            tern_linear_workspace_bytes(T, K, N) bytes (may be NULL when that
+ *            is 0).  Contents on entry are ignored; it must not be used by
+ *            anything else until the call's work on `stream` has finished.
+ * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
+ * Every rung is correct for every T. */
+int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
+                const uint16_t* x, float* y, int T, int K, int N,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Rung the dispatcher picks for T (after env overrides).  Host-only. */
+int tern_select_rung(int T);
+
+/* Name of a rung id ("gemv", "small_t", "small_t_tiled", "s8"), or "?". */
+const char* tern_rung_name(int rung);
+
+/* Rung launched by this thread's last successful tern_linear, or -1 / "none". */
+int tern_last_rung_id(void);
+const char* tern_last_rung(void);
+
+/* Static text for a tern_status. */
+const char* tern_status_string(int status);
+
+/* Re-read the environment (TERN_RUNG, TERN_SMALL_T_MAX, TERN_TILED_MAX,
+ * TERN_S8_MIN_T, TERN_DEBUG, TERN_DEBUG_MIN_T, TERN_DEBUG_BUDGET).  The
+ * environment is otherwise read once per process, on first use. */
+void tern_reload_env(void);
+
+/* Synchronises `stream`, then returns and clears the current device's
+ * asynchronous error word: TERN_OK, or TERN_ETIMEOUT if a kernel's bounded
+ * wait ran out since the last call. */
+int tern_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TERN_H_ */

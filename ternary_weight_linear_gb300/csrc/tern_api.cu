@@ -1,0 +1,346 @@
+// C ABI of the ternary-weight linear layer: argument checks, the T-band
+// dispatcher with its environment override and per-rung debug probe, tensor
+// map set-up, and the launches.
+//
+// Dispatcher: the rung map of the "ninfer-perf-tuning" skill page
+// (markdownregistry.com), section 2 — T = 1 decode entry, T = 2..8 small-T
+// tile, T = 9..16 tiled small-T, T >= 17 int8 "s8" — with env-overridable
+// thresholds read once per process, and a probe that prints which rung ran
+// (section 2: every reachable branch reports itself), limited by a minimum T
+// and a line budget.  Names of the variables are this library's own.
+#include <mutex>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tern.h"
+#include "tern_internal.h"
+
+namespace tern {
+
+__device__ int g_device_error;  // one per device (module globals are per device)
+
+namespace {
+
+// ------------------------------------------------------------------ config
+struct Config {
+  int forced = -1;      // TERN_RUNG
+  int small_t_max = 8;  // TERN_SMALL_T_MAX
+  int tiled_max = 16;   // TERN_TILED_MAX
+  int s8_min_t = 17;    // TERN_S8_MIN_T
+  bool debug = false;   // TERN_DEBUG
+  int debug_min_t = 1;  // TERN_DEBUG_MIN_T
+  long debug_budget = 1000;  // TERN_DEBUG_BUDGET (lines)
+};
+
+std::mutex g_mu;
+Config g_cfg;
+bool g_cfg_loaded = false;
+long g_debug_lines = 0;
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  long x = strtol(v, &end, 10);
+  if (end == v) return dflt;
+  return static_cast<int>(x);
+}
+
+int rung_from_name(const char* v) {
+  if (!v || !*v) return -1;
+  if (!strcmp(v, "gemv")) return TERN_RUNG_GEMV;
+  if (!strcmp(v, "small_t")) return TERN_RUNG_SMALL_T;
+  if (!strcmp(v, "small_t_tiled")) return TERN_RUNG_SMALL_T_TILED;
+  if (!strcmp(v, "s8")) return TERN_RUNG_S8;
+  return -1;
+}
+
+void load_config_locked() {
+  Config c;
+  c.forced = rung_from_name(getenv("TERN_RUNG"));
+  c.small_t_max = env_int("TERN_SMALL_T_MAX", 8);
+  c.tiled_max = env_int("TERN_TILED_MAX", 16);
+  c.s8_min_t = env_int("TERN_S8_MIN_T", 17);
+  c.debug = env_int("TERN_DEBUG", 0) != 0;
+  c.debug_min_t = env_int("TERN_DEBUG_MIN_T", 1);
+  c.debug_budget = env_int("TERN_DEBUG_BUDGET", 1000);
+  // keep the bands well formed
+  if (c.small_t_max < 1) c.small_t_max = 1;
+  if (c.small_t_max > 8) c.small_t_max = 8;
+  if (c.tiled_max < c.small_t_max) c.tiled_max = c.small_t_max;
+  if (c.tiled_max > 16) c.tiled_max = 16;
+  if (c.s8_min_t < 2) c.s8_min_t = 2;
+  g_cfg = c;
+  g_cfg_loaded = true;
+  g_debug_lines = 0;
+}
+
+Config config() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_cfg_loaded) load_config_locked();
+  return g_cfg;
+}
+
+int pick_rung(const Config& c, int T) {
+  if (c.forced >= 0) return c.forced;
+  if (T >= c.s8_min_t) return TERN_RUNG_S8;
+  if (T == 1) return TERN_RUNG_GEMV;
+  if (T <= c.small_t_max) return TERN_RUNG_SMALL_T;
+  return TERN_RUNG_SMALL_T_TILED;  // covers T up to tiled_max and any gap below s8_min_t
+}
+
+void probe(const Config& c, int rung, int T, int K, int N) {
+  if (!c.debug || T < c.debug_min_t) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_debug_lines >= c.debug_budget) return;
+  ++g_debug_lines;
+  fprintf(stderr, "tern: rung=%s T=%d K=%d N=%d\n", tern_rung_name(rung), T, K, N);
+  fflush(stderr);
+}
+
+thread_local int t_last_rung = -1;
+
+// ------------------------------------------------------------------ device state
+constexpr int kMaxDevices = 64;
+struct DevState {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+  int smallt_cpm[3] = {1, 1, 1};  // CTAs per SM for nt = 1, 2
+};
+DevState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DevState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TERN_ENODEV;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TERN_ENODEV;
+    if (prop.major != 10 || prop.minor != 3) return TERN_ENODEV;  // built for sm_103a only
+    d.sms = prop.multiProcessorCount;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return TERN_ECUDA;
+    d.err = static_cast<int*>(p);
+    if (smallt_set_attributes() != cudaSuccess) return TERN_ECUDA;
+    if (s8_set_attributes() != cudaSuccess) return TERN_ECUDA;
+    d.smallt_cpm[1] = smallt_ctas_per_sm(1);
+    d.smallt_cpm[2] = smallt_ctas_per_sm(2);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return TERN_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return TERN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2D uint8 tensor map: inner extent `inner` bytes, `outer` rows, row pitch `pitch` bytes.
+int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TERN_OK : TERN_ECUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Does the persistent split of U units over P CTAs cut any row block
+// (KS units each) between two CTAs?
+bool split_cuts_row_blocks(long long U, long long P, long long KS) {
+  for (long long p = 1; p < P; ++p)
+    if ((U * p / P) % KS != 0) return true;
+  return false;
+}
+
+int run_small_t(DevState* d, int nt, bool force_one_token, const uint32_t* Wp, const uint16_t* s,
+                const uint16_t* x, float* y, int T, int K, int N, cudaStream_t st) {
+  CUtensorMap tmW;
+  int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
+                       static_cast<uint64_t>(K) / 4, 128, kSTRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TERN_OK) return rc;
+  const long long KS = (K + kSTStageK - 1) / kSTStageK;
+  const long long NB = (N + kSTRows - 1) / kSTRows;
+  const long long U = NB * KS;
+  long long P = static_cast<long long>(d->sms) * d->smallt_cpm[nt];
+  if (P > U) P = U;
+  const bool cut = split_cuts_row_blocks(U, P, KS);
+  const int tile = force_one_token ? 1 : 8 * nt;
+  for (int tok0 = 0; tok0 < T; tok0 += tile) {
+    const int Tt = (T - tok0 < tile) ? T - tok0 : tile;
+    if (cut &&
+        cudaMemsetAsync(y + static_cast<size_t>(tok0) * N, 0, sizeof(float) * Tt * N, st) !=
+            cudaSuccess)
+      return TERN_ECUDA;
+    // Each launch sees only its tile's tokens: T passed as tok0 + Tt.
+    if (launch_smallt(nt, Tt == 1, &tmW, s, x, y, tok0 + Tt, K, N, tok0, static_cast<int>(P),
+                      d->err, st) != cudaSuccess)
+      return TERN_ECUDA;
+  }
+  return TERN_OK;
+}
+
+}  // namespace
+}  // namespace tern
+
+using namespace tern;
+
+extern "C" {
+
+const char* tern_rung_name(int rung) {
+  switch (rung) {
+    case TERN_RUNG_GEMV: return "gemv";
+    case TERN_RUNG_SMALL_T: return "small_t";
+    case TERN_RUNG_SMALL_T_TILED: return "small_t_tiled";
+    case TERN_RUNG_S8: return "s8";
+    default: return "?";
+  }
+}
+
+const char* tern_status_string(int st) {
+  switch (st) {
+    case TERN_OK: return "ok";
+    case TERN_EINVAL: return "invalid argument";
+    case TERN_EALIGN: return "pointer not 16-byte aligned";
+    case TERN_ENOSPACE: return "workspace too small";
+    case TERN_ENODEV: return "no sm_103 CUDA device current";
+    case TERN_ECUDA: return "CUDA runtime error";
+    case TERN_ETIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+void tern_reload_env(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  load_config_locked();
+}
+
+int tern_select_rung(int T) {
+  if (T < 1) return TERN_EINVAL;
+  return pick_rung(config(), T);
+}
+
+int tern_last_rung_id(void) { return t_last_rung; }
+const char* tern_last_rung(void) { return t_last_rung < 0 ? "none" : tern_rung_name(t_last_rung); }
+
+size_t tern_linear_workspace_bytes(int T, int K, int N) {
+  (void)N;
+  if (T < 1 || K < 1) return 0;
+  // s8 rung: int8 codes [T][K] + fp32 x_scale [T], each 256-byte aligned.
+  return align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
+}
+
+int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count, void* stream) {
+  if (!W || !Wpacked || K <= 0 || N <= 0 || (K % 16) != 0) return TERN_EINVAL;
+  if (!aligned16(W) || !aligned16(Wpacked)) return TERN_EALIGN;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  return launch_pack(W, Wpacked, K, N, bad_count, d->sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TERN_OK
+             : TERN_ECUDA;
+}
+
+int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T, int K, void* stream) {
+  if (!x || !q || !x_scale || T <= 0 || K <= 0 || (K % 16) != 0) return TERN_EINVAL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(x_scale)) return TERN_EALIGN;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  return launch_quant_s8(x, q, x_scale, T, K, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TERN_OK
+             : TERN_ECUDA;
+}
+
+int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* x, float* y,
+                int T, int K, int N, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!Wpacked || !scales || !x || !y || T < 1 || N < 1 || K < 128 || (K % 128) != 0)
+    return TERN_EINVAL;
+  if (!aligned16(Wpacked) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
+    return TERN_EALIGN;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  const Config c = config();
+  const int rung = pick_rung(c, T);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  switch (rung) {
+    case TERN_RUNG_GEMV:
+      rc = run_small_t(d, 1, true, Wpacked, scales, x, y, T, K, N, st);
+      break;
+    case TERN_RUNG_SMALL_T:
+      rc = run_small_t(d, 1, false, Wpacked, scales, x, y, T, K, N, st);
+      break;
+    case TERN_RUNG_SMALL_T_TILED:
+      rc = run_small_t(d, 2, false, Wpacked, scales, x, y, T, K, N, st);
+      break;
+    case TERN_RUNG_S8: {
+      const size_t need = tern_linear_workspace_bytes(T, K, N);
+      if (!workspace || workspace_bytes < need) return TERN_ENOSPACE;
+      if (!aligned16(workspace)) return TERN_EALIGN;
+      int8_t* q = static_cast<int8_t*>(workspace);
+      float* xs =
+          reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                   align_up(static_cast<size_t>(T) * K, 256));
+      if (launch_quant_s8(x, q, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
+      CUtensorMap tmW, tmQ;
+      rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
+                       static_cast<uint64_t>(K) / 4, 32, kS8TileN, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != TERN_OK) return rc;
+      rc = make_map_u8(&tmQ, q, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
+                       static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != TERN_OK) return rc;
+      rc = launch_s8(&tmW, &tmQ, scales, xs, y, T, K, N, d->err, st) == cudaSuccess ? TERN_OK
+                                                                                   : TERN_ECUDA;
+      break;
+    }
+    default:
+      return TERN_EINVAL;
+  }
+  if (rc == TERN_OK) {
+    t_last_rung = rung;
+    probe(c, rung, T, K, N);
+  }
+  return rc;
+}
+
+int tern_device_status(void* stream) {
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TERN_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return TERN_ECUDA;
+  if (v) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return TERN_ECUDA;
+    return TERN_ETIMEOUT;
+  }
+  return TERN_OK;
+}
+
+}  // extern "C"

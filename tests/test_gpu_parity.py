@@ -1,0 +1,275 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every rung is forced on every token band (each rung must be right for every
+T), on shapes that span several row blocks, several k stages and ragged tails
+in N, K and T; then the workload families at full size, on sampled outputs.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (assert_bf16_parity, assert_s8_parity, packed_to_numpy, sample_indices,
+                     to_device)
+
+pytestmark = pytest.mark.gpu
+
+RUNGS = ("gemv", "small_t", "small_t_tiled", "s8")
+
+
+@pytest.fixture(scope="module")
+def tl():
+    import torch
+    import ternary_weight_linear_gb300 as tl
+    tl.build()
+    tl.load()
+    torch.cuda.init()
+    return tl
+
+
+class forced_rung:
+    def __init__(self, tl, rung):
+        self.tl, self.rung = tl, rung
+
+    def __enter__(self):
+        self.old = os.environ.get("TERN_RUNG")
+        if self.rung is None:
+            os.environ.pop("TERN_RUNG", None)
+        else:
+            os.environ["TERN_RUNG"] = self.rung
+        self.tl.tern_reload_env()
+
+    def __exit__(self, *a):
+        if self.old is None:
+            os.environ.pop("TERN_RUNG", None)
+        else:
+            os.environ["TERN_RUNG"] = self.old
+        self.tl.tern_reload_env()
+
+
+def _run(tl, case, rung=None):
+    import torch
+    W, s, x = to_device(case)
+    Wp = tl.tern_pack(W)
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, s, x)
+        ran = tl.tern_last_rung()
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    return Wp, y.cpu().numpy(), ran
+
+
+def _check_case(tl, case, rung=None, full=True, samples=4096):
+    Wp, y, ran = _run(tl, case, rung)
+    wp_ref, bad = oracle.pack(case.W)
+    assert bad == 0
+    assert np.array_equal(packed_to_numpy(Wp), wp_ref), "tern_pack differs from the oracle"
+    T, K, N = case.T, case.K, case.N
+    if ran == "s8":
+        q_ref, xs_ref = oracle.quant_s8(case.x, T, K)
+        if full:
+            y_ref, m, _ = oracle.linear_s8(wp_ref, case.scales, q_ref, xs_ref, T, K, N)
+            assert_s8_parity(y, y_ref, m, f"{case.name} T={T} rung={ran}")
+        else:
+            ti, ni = sample_indices(T, N, samples, seed=K)
+            y_ref, m, _ = oracle.linear_s8_sampled(wp_ref, case.scales, q_ref, xs_ref, K, N, ti, ni)
+            assert_s8_parity(y[ti, ni], y_ref, m, f"{case.name} T={T} rung={ran}")
+    else:
+        if full:
+            y_ref, m = oracle.linear_f64(wp_ref, case.scales, case.x, T, K, N)
+            assert_bf16_parity(y, y_ref, m, f"{case.name} T={T} rung={ran}")
+        else:
+            ti, ni = sample_indices(T, N, samples, seed=K)
+            y_ref, m = oracle.linear_f64_sampled(wp_ref, case.scales, case.x, K, N, ti, ni)
+            assert_bf16_parity(y[ti, ni], y_ref, m, f"{case.name} T={T} rung={ran}")
+    return ran
+
+
+# ---------------------------------------------------------------- pack / quant
+
+def test_pack_bit_exact_and_bad_count(tl):
+    import torch
+    W = synth.ternary_weights(300, 640, 0.4, seed=3)
+    W[5, 7] = 2
+    W[299, 639] = -3
+    Wd = torch.from_numpy(W).cuda()
+    bad = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wp = tl.tern_pack(Wd, bad_count=bad)
+    ref, nbad = oracle.pack(W)
+    assert int(bad.item()) == nbad == 2
+    assert np.array_equal(packed_to_numpy(Wp), ref)
+
+
+@pytest.mark.parametrize("T,K", [(1, 128), (17, 5120), (508, 6144), (3, 16)])
+def test_quant_s8_bit_exact(tl, T, K):
+    import torch
+    xb = synth.activations(T, K, seed=T, outlier_frac=0.01)
+    xb[0, :4] = 0  # a few exact zeros
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    q, xs = tl.tern_quant_act_s8(x)
+    q_ref, xs_ref = oracle.quant_s8(xb, T, K)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+
+
+def test_quant_s8_golden_ties_and_zero_row(tl):
+    import torch
+    rows = [[127, 0.5, 1.5, 2.5, 3.5, 4.5, 126.5, 0] + [0] * 8,
+            [-127, -0.5, -1.5, -2.5, -3.5, -4.5, -126.5, 0] + [0] * 8,
+            [0.0] * 16]
+    x32 = np.array(rows, dtype=np.float32)
+    xb = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    q, xs = tl.tern_quant_act_s8(x)
+    q = q.cpu().numpy()
+    assert list(q[0, :8]) == [127, 0, 2, 2, 4, 4, 126, 0]
+    assert list(q[1, :8]) == [-127, 0, -2, -2, -4, -4, -126, 0]
+    assert not q[2].any() and float(xs[2].item()) == 0.0
+    assert float(xs[0].item()) == 1.0
+
+
+# ---------------------------------------------------------------- every rung, every band
+
+@pytest.mark.parametrize("rung", RUNGS)
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 16, 17, 40])
+def test_forced_rung_ragged(tl, rung, T):
+    # K = 640: one full 512-wide stage plus a 128 tail; N = 300: ragged row block.
+    case = synth.case("ragged", T, K=640, N=300, seed=T, p_zero=0.4, outliers=True)
+    ran = _check_case(tl, case, rung)
+    assert ran == rung
+
+
+@pytest.mark.parametrize("T,expect", [(1, "gemv"), (2, "small_t"), (8, "small_t"),
+                                      (9, "small_t_tiled"), (16, "small_t_tiled"), (17, "s8"),
+                                      (130, "s8")])
+def test_default_dispatch(tl, T, expect):
+    case = synth.case("disp", T, K=1024, N=256, seed=T)
+    assert _check_case(tl, case, None) == expect
+
+
+@pytest.mark.parametrize("K,N", [(128, 1), (128, 17), (256, 129), (1152, 520), (2048, 4096)])
+def test_shapes_bf16(tl, K, N):
+    for T in (1, 5, 13):
+        _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T))
+
+
+@pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 520, 200), (2048, 300, 129)])
+def test_shapes_s8(tl, K, N, T):
+    _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T))
+
+
+# ---------------------------------------------------------------- degenerate inputs
+
+def _dev_case(W, s, xb):
+    import torch
+    return (torch.from_numpy(W).cuda(),
+            torch.from_numpy(s.view(np.uint16)).view(torch.float16).cuda(),
+            torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda())
+
+
+@pytest.mark.parametrize("rung", RUNGS)
+def test_zero_weights_give_zero(tl, rung):
+    T, K, N = 20, 640, 200
+    W = np.zeros((N, K), dtype=np.int8)
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=1)
+    xb = synth.activations(T, K, seed=2, outlier_frac=0.01)
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, sd, xd).cpu().numpy()
+    assert np.all(np.abs(y) <= 1e-6)
+
+
+@pytest.mark.parametrize("rung", RUNGS)
+def test_one_hot_x_picks_scaled_weight(tl, rung):
+    T, K, N = 4, 512, 300
+    W = synth.ternary_weights(N, K, 1.0 / 3.0, seed=9)
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=10)
+    cols = [0, 200, 333, 511]
+    x32 = np.zeros((T, K), dtype=np.float32)
+    for t, k in enumerate(cols):
+        x32[t, k] = 1.0
+    xb = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, sd, xd).cpu().numpy()
+    for t, k in enumerate(cols):
+        expect = s[:, k // 128].astype(np.float64) * W[:, k]
+        if rung == "s8":
+            # x_scale = 1/127 in fp32, q = 127: exact up to that one rounding
+            np.testing.assert_allclose(y[t].astype(np.float64), expect, rtol=1e-6, atol=0)
+        else:
+            np.testing.assert_array_equal(y[t].astype(np.float64), expect)
+
+
+def test_s8_integer_accumulators_bit_exact(tl):
+    # scales = 1 and integer rows holding +-127: q = x and x_scale = 1, so the
+    # fp32 output equals the exact integer dot product (all partial sums < 2^24).
+    T, K, N = 64, 17408, 256
+    W = synth.ternary_weights(N, K, 0.4, seed=5)
+    s = np.ones((N, K // 128), dtype=np.float16)
+    rng = np.random.default_rng(6)
+    x32 = rng.integers(-127, 128, size=(T, K)).astype(np.float32)
+    x32[:, 3] = 127.0
+    x32[1] = 127.0  # every product at its extreme
+    xb = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, "s8"):
+        y = tl.tern_linear(Wp, sd, xd).cpu().numpy()
+    exact = x32.astype(np.int64) @ W.astype(np.int64).T
+    assert np.array_equal(y.astype(np.int64), exact)
+    assert np.array_equal(y, exact.astype(np.float32))
+
+
+# ---------------------------------------------------------------- workload families
+
+def test_tiny_config_full(tl):
+    _check_case(tl, synth.config_tiny(), full=True)
+
+
+@pytest.mark.parametrize("proj", ["gu", "dn"])
+def test_decode_config_full(tl, proj):
+    _check_case(tl, synth.config_decode(proj), full=True)
+
+
+@pytest.mark.parametrize("proj", ["gu", "dn"])
+@pytest.mark.parametrize("T", synth.VERIFY_T)
+def test_verify_config_sampled(tl, proj, T):
+    ran = _check_case(tl, synth.config_verify(proj, T), full=False)
+    assert ran == ("small_t" if T <= 8 else "small_t_tiled")
+
+
+@pytest.mark.parametrize("proj", ["gu", "dn", "ai", "ao"])
+@pytest.mark.parametrize("T", synth.PREFILL_T)
+def test_prefill_config_sampled(tl, proj, T):
+    assert _check_case(tl, synth.config_prefill(proj, T), full=False) == "s8"
+
+
+# ---------------------------------------------------------------- probe
+
+def test_debug_probe_reports_each_rung(tl):
+    import subprocess
+    import sys
+    code = r"""
+import numpy as np, torch, synth, ternary_weight_linear_gb300 as tl
+from helpers import to_device
+for T in (1, 4, 12, 20):
+    c = synth.case("p", T, K=256, N=64, seed=T)
+    W, s, x = to_device(c)
+    tl.tern_linear(tl.tern_pack(W), s, x)
+torch.cuda.synchronize()
+"""
+    env = dict(os.environ, TERN_DEBUG="1", TERN_DEBUG_MIN_T="1", TERN_DEBUG_BUDGET="3")
+    env.pop("TERN_RUNG", None)
+    here = os.path.dirname(os.path.abspath(__file__))
+    env["PYTHONPATH"] = os.pathsep.join([here, os.path.dirname(here), env.get("PYTHONPATH", "")])
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stderr.splitlines() if l.startswith("tern: rung=")]
+    # budget 3: the fourth call is not reported
+    assert [l.split()[1] for l in lines] == ["rung=gemv", "rung=small_t", "rung=small_t_tiled"]
