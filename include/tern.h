@@ -31,12 +31,16 @@
  *    tern_device_status().
  *
  * Packed weight layout (this library's format; the pages pack base-3 trits
- * five to a byte, this format keeps the same trit digit in 2 bits):
- *   Wpacked is uint32 [N][K/16].  Word n*(K/16) + k/16 holds weight (n, k) in
- *   bits 2*(k%16) .. 2*(k%16)+1 as the digit c = w + 1:
- *       c = 0 -> w = -1,   c = 1 -> w = 0,   c = 2 -> w = +1,   c = 3 invalid.
- *   tern_pack never writes c = 3; the linear kernels do not check for it
- *   (it is decoded as w = +2).
+ * five to a byte, this format spends 2 bits per weight on sign and magnitude):
+ *   Wpacked is uint32 [N][K/16], i.e. K/4 bytes per row.  Byte b of row n
+ *   (little-endian bytes within the words) holds weights k = 4b .. 4b+3.
+ *   Weight i of a byte has its "nonzero" bit at bit P[i] and its "negative"
+ *   bit at bit P[i] + 2, with P = {0, 1, 4, 5}; each nibble thus reads
+ *   [nz_lo, nz_hi, neg_lo, neg_hi] from bit 0 up:
+ *       (nz, neg) = (0, 0) -> 0,  (1, 0) -> +1,  (1, 1) -> -1,  (0, 1) invalid.
+ *   tern_pack never writes the invalid pair; the linear kernels decode it as 0.
+ *   The bit order lets the kernels turn a byte into the fp8 e4m3 encoding of
+ *   w/8 with one shift and one AND.
  * Scales: fp16 [N][K/128], scale (n, g) applies to k in [128g, 128g+128).
  */
 #ifndef TERN_H_
@@ -92,14 +96,14 @@ int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count,
 int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T,
                       int K, void* stream);
 
-/* Bytes of device workspace tern_linear needs for (T, K, N) under the rung the
- * dispatcher would pick right now (and under any forced rung: the value
- * covers every rung).  0 means no workspace is needed.  Host-only. */
+/* Bytes of device workspace tern_linear needs for (T, K, N); the value covers
+ * every rung (int8 codes and scales for the s8 rung, the per-call activation
+ * fragments for the small-T rungs).  Host-only; 0 for T < 1 or K < 1. */
 size_t tern_linear_workspace_bytes(int T, int K, int N);
 
 /* y = x W^T with group scales:
  *   y[t][n] = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k]
- * on the bf16 rungs (fp32 accumulation; |y - y_exact| within
+ * on the bf16-activation rungs (T <= 16; |y - y_exact| within
  * 1e-3 * sum|s w x| + 1e-6), and on the s8 rung (T >= 17)
  *   q, xs = tern_quant_act_s8(x)
  *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]   (exact integers)
@@ -110,9 +114,10 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  *   y        device fp32 [T][N], written (fully overwritten)
  *   T >= 1, K >= 128 with K % 128 == 0, N >= 1
  *   workspace, workspace_bytes: device scratch of at least
- *            tern_linear_workspace_bytes(T, K, N) bytes (may be NULL when that
- *            is 0).  Contents on entry are ignored; it must not be used by
- *            anything else until the call's work on `stream` has finished.
+ *            tern_linear_workspace_bytes(T, K, N) bytes, 16-byte aligned
+ *            (TERN_ENOSPACE if smaller).  Contents on entry are ignored; it
+ *            must not be used by anything else until the call's work on
+ *            `stream` has finished.
  * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
  * Every rung is correct for every T. */
 int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,

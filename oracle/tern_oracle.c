@@ -14,10 +14,14 @@
  *    FP16 scale per 128 weights).
  *
  *  - 2-bit packing.  The pages pack base-3 trits five to a byte; this layer
- *    stores one trit digit (w + 1, the digit a base-3 packing also stores) in a
- *    2-bit field instead.  Word n*(K/16) + k/16 of the packed matrix holds
- *    weight (n, k) in bits 2*(k%16) .. 2*(k%16)+1:
- *        code 0 -> -1,  code 1 -> 0,  code 2 -> +1,  code 3 -> invalid.
+ *    stores each weight in 2 bits as sign and magnitude: a "nonzero" bit
+ *    |w| and a "negative" bit.  Byte b of row n (bytes in little-endian order
+ *    within the uint32 words, so word n*(K/16) + k/16) holds the four weights
+ *    k = 4b + i, i = 0..3; weight i has its nonzero bit at bit P[i] and its
+ *    negative bit at bit P[i] + 2 of the byte, with P = {0, 1, 4, 5}:
+ *        (nz, neg) = (0, 0) -> 0,  (1, 0) -> +1,  (1, 1) -> -1,
+ *        (0, 1) -> invalid.
+ *    (Each nibble therefore reads [nz_lo, nz_hi, neg_lo, neg_hi].)
  *
  *  - bf16 rungs (T <= 16):  y[t,n] = sum_g s[n,g] * sum_{k in g} w[n,k] x[t,k]
  *    accumulated in fp64 here; m[t,n] = sum_k |s w x| is the tolerance scale.
@@ -32,7 +36,7 @@
  *    is the reading of "quantised per token to int8".
  *
  * Readings where the pages are silent (each also listed in the design notes):
- *  - the 2-bit code is the offset digit w+1 (linear in w);
+ *  - the 2-bit code is sign-magnitude with the bit order above;
  *  - the quantiser divides by xs = a/127 in IEEE fp32 and clamps to +-127;
  *  - a token whose absmax is 0 gets xs = 0 and q = 0.
  *
@@ -74,12 +78,20 @@ static double f16_to_f64(uint16_t h) {
 
 /* ---- packing ------------------------------------------------------------ */
 
-/* Weight (n, k) from the packed matrix; returns 2 for the invalid code 3 so
- * that callers can count it. */
+/* Bit position of the nonzero bit of weight i (0..3) within its byte; the
+ * negative bit sits two places higher. */
+static const int kNzBit[4] = {0, 1, 4, 5};
+
+/* Weight (n, k) from the packed matrix; returns 2 for the invalid pair
+ * (nz = 0, neg = 1) so that callers can count it. */
 static int unpack_one(const uint32_t* wp, int K, int n, int k) {
   uint32_t word = wp[(size_t)n * (size_t)(K / 16) + (size_t)(k / 16)];
-  int code = (int)((word >> (2 * (k % 16))) & 3u);
-  return code - 1; /* 0->-1, 1->0, 2->+1, 3->2 (invalid) */
+  uint32_t byte = (word >> (8 * ((k % 16) / 4))) & 0xffu;
+  int p = kNzBit[k % 4];
+  int nz = (int)((byte >> p) & 1u);
+  int neg = (int)((byte >> (p + 2)) & 1u);
+  if (!nz) return neg ? 2 : 0;
+  return neg ? -1 : 1;
 }
 
 /* W [N][K] int8 in {-1,0,1} -> packed [N][K/16] u32.  Values outside
@@ -95,14 +107,15 @@ long tern_oracle_pack(const int8_t* W, int K, int N, uint32_t* wp) {
         ++bad;
         w = 0;
       }
-      uint32_t code = (uint32_t)(w + 1);
-      wp[(size_t)n * (K / 16) + k / 16] |= code << (2 * (k % 16));
+      uint32_t nz = (w != 0), neg = (w < 0);
+      int p = 8 * ((k % 16) / 4) + kNzBit[k % 4];
+      wp[(size_t)n * (K / 16) + k / 16] |= (nz << p) | (neg << (p + 2));
     }
   }
   return bad;
 }
 
-/* packed -> W [N][K] int8; invalid codes become 0 and are counted. */
+/* packed -> W [N][K] int8; invalid pairs become 0 and are counted. */
 long tern_oracle_unpack(const uint32_t* wp, int K, int N, int8_t* W) {
   long bad = 0;
   for (int n = 0; n < N; ++n)

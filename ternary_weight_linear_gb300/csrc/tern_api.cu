@@ -111,7 +111,7 @@ struct DevState {
   bool ready = false;
   int sms = 0;
   int* err = nullptr;
-  int smallt_cpm[3] = {1, 1, 1};  // CTAs per SM for nt = 1, 2
+  int smallt_cpm[17] = {};  // CTAs per SM by token tile TT (1, 4, 8, 16)
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -132,8 +132,7 @@ int device_state(DevState** out) {
     d.err = static_cast<int*>(p);
     if (smallt_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (s8_set_attributes() != cudaSuccess) return TERN_ECUDA;
-    d.smallt_cpm[1] = smallt_ctas_per_sm(1);
-    d.smallt_cpm[2] = smallt_ctas_per_sm(2);
+    for (int tt : {1, 4, 8, 16}) d.smallt_cpm[tt] = smallt_ctas_per_sm(tt);
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -166,37 +165,42 @@ int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Does the persistent split of U units over P CTAs cut any row block
-// (KS units each) between two CTAs?
-bool split_cuts_row_blocks(long long U, long long P, long long KS) {
-  for (long long p = 1; p < P; ++p)
-    if ((U * p / P) % KS != 0) return true;
-  return false;
+size_t s8_workspace_bytes(int T, int K) {
+  return align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
 }
 
-int run_small_t(DevState* d, int nt, bool force_one_token, const uint32_t* Wp, const uint16_t* s,
-                const uint16_t* x, float* y, int T, int K, int N, cudaStream_t st) {
-  CUtensorMap tmW;
-  int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
-                       static_cast<uint64_t>(K) / 4, 128, kSTRows, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != TERN_OK) return rc;
-  const long long KS = (K + kSTStageK - 1) / kSTStageK;
-  const long long NB = (N + kSTRows - 1) / kSTRows;
-  const long long U = NB * KS;
-  long long P = static_cast<long long>(d->sms) * d->smallt_cpm[nt];
-  if (P > U) P = U;
-  const bool cut = split_cuts_row_blocks(U, P, KS);
-  const int tile = force_one_token ? 1 : 8 * nt;
-  for (int tok0 = 0; tok0 < T; tok0 += tile) {
-    const int Tt = (T - tok0 < tile) ? T - tok0 : tile;
-    if (cut &&
-        cudaMemsetAsync(y + static_cast<size_t>(tok0) * N, 0, sizeof(float) * Tt * N, st) !=
-            cudaSuccess)
-      return TERN_ECUDA;
-    // Each launch sees only its tile's tokens: T passed as tok0 + Tt.
-    if (launch_smallt(nt, Tt == 1, &tmW, s, x, y, tok0 + Tt, K, N, tok0, static_cast<int>(P),
+// Token tile for a rung and the tokens left: (TT, tokens in this launch).
+void small_t_tile(int rung, int left, int* tt, int* take) {
+  if (rung == TERN_RUNG_GEMV) {
+    *tt = 1;
+    *take = 1;
+  } else if (rung == TERN_RUNG_SMALL_T) {
+    *take = left < 8 ? left : 8;
+    *tt = *take <= 4 ? 4 : 8;
+  } else {
+    *take = left < 16 ? left : 16;
+    *tt = 16;
+  }
+}
+
+int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
+                float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st) {
+  CUtensorMap maps[17];
+  bool have[17] = {};
+  for (int tok0 = 0; tok0 < T;) {
+    int tt = 0, take = 0;
+    small_t_tile(rung, T - tok0, &tt, &take);
+    if (!have[tt]) {
+      int rc = make_map_u8(&maps[tt], Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
+                           static_cast<uint64_t>(K) / 4, 128, smallt_rows(tt),
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != TERN_OK) return rc;
+      have[tt] = true;
+    }
+    if (launch_smallt(tt, &maps[tt], s, x, ws, y, K, N, tok0, take, d->sms, d->smallt_cpm[tt],
                       d->err, st) != cudaSuccess)
       return TERN_ECUDA;
+    tok0 += take;
   }
   return TERN_OK;
 }
@@ -247,8 +251,11 @@ const char* tern_last_rung(void) { return t_last_rung < 0 ? "none" : tern_rung_n
 size_t tern_linear_workspace_bytes(int T, int K, int N) {
   (void)N;
   if (T < 1 || K < 1) return 0;
-  // s8 rung: int8 codes [T][K] + fp32 x_scale [T], each 256-byte aligned.
-  return align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
+  // s8 rung: int8 codes [T][K] + fp32 x_scale [T]; small-T rungs: the
+  // activation-fragment buffer of the widest token tile.  Enough for any rung.
+  const size_t a = s8_workspace_bytes(T, K);
+  const size_t b = smallt_xprep_bytes(16, K);
+  return a > b ? a : b;
 }
 
 int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count, void* stream) {
@@ -287,20 +294,18 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
   const int rung = pick_rung(c, T);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+  const size_t need = tern_linear_workspace_bytes(T, K, N);
+  if (!workspace || workspace_bytes < need) return TERN_ENOSPACE;
+  if (!aligned16(workspace)) return TERN_EALIGN;
+
   switch (rung) {
     case TERN_RUNG_GEMV:
-      rc = run_small_t(d, 1, true, Wpacked, scales, x, y, T, K, N, st);
-      break;
     case TERN_RUNG_SMALL_T:
-      rc = run_small_t(d, 1, false, Wpacked, scales, x, y, T, K, N, st);
-      break;
     case TERN_RUNG_SMALL_T_TILED:
-      rc = run_small_t(d, 2, false, Wpacked, scales, x, y, T, K, N, st);
+      rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, static_cast<uint8_t*>(workspace),
+                       st);
       break;
     case TERN_RUNG_S8: {
-      const size_t need = tern_linear_workspace_bytes(T, K, N);
-      if (!workspace || workspace_bytes < need) return TERN_ENOSPACE;
-      if (!aligned16(workspace)) return TERN_EALIGN;
       int8_t* q = static_cast<int8_t*>(workspace);
       float* xs =
           reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +

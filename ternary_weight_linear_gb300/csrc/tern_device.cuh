@@ -98,6 +98,40 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 1D bulk copy global -> shared, completing on `bar` (size and both addresses
+// multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 8-byte asynchronous copy global -> shared (LDGSTS); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_8(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the following kernel start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -111,90 +145,166 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
+// Shared-memory loads through ordinary pointers: the compiler sees them as
+// memory reads, keeps them after the mbarrier waits (which clobber memory) and
+// is free to schedule them early against the arithmetic.
+__device__ __forceinline__ uint2 lds_v2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 lds_v4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // ---------------------------------------------------------------- decode
-// 2-bit trit digits c = w + 1 -> bf16 pairs holding w exactly.
+// Packed codes: each nibble of a word holds two weights as [nz_lo, nz_hi,
+// neg_lo, neg_hi]; byte b of a word holds weights 4b .. 4b+3 with weight i's
+// nonzero bit at bit P[i] = {0, 1, 4, 5}[i] and its sign two bits higher.
 //
-// A packed word holds 16 digits: field j (bits 2j, 2j+1) for j = 0..15.  The
-// decoder yields 8 bf16x2 pairs; pair p (p = 0..7) has field p in its low half
-// and field p+8 in its high half.  Method: OR the isolated field into the
-// mantissa of the bf16 constant 128 (0x4300, whose unit in the last place is
-// 1), giving 128 + c * 4^i for a field at mantissa position i (bits 2i,
-// 2i+1, i = 0..2); one exact fused multiply-add by 4^-i and -(128 * 4^-i + 1)
-// then leaves c - 1 = w.  Both halves use the same position, so one
-// instruction decodes two weights.
-__device__ __forceinline__ uint32_t bf16x2_fma_bits(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t v, uint32_t mask, uint32_t magic) {
-  uint32_t d;
-  // d = (v & mask) | magic
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "r"(mask), "r"(magic));
-  return d;
-}
-
-// Decode the field pair at mantissa position i (0..2) of both halves of v.
+// fp8 e4m3 decode: masking a byte with 0xA0 keeps bit 5 (exponent bit worth
+// 2^-3 when alone: 0x20 = +0.125) and bit 7 (sign).  So for the weight whose
+// bits sit at (5, 7) the masked byte IS the e4m3 encoding of w/8 (0x00, 0x20,
+// 0xA0; the invalid pair gives 0x80 = -0).  Shifting the word left by
+// 5 - P[i] brings weight i of every byte to that position, giving four
+// weights per AND:  e4[i] byte b = e4m3(w[4b + i] / 8).
 template <int I>
-__device__ __forceinline__ uint32_t decode_pos(uint32_t v) {
-  constexpr uint32_t kMask = 0x00030003u << (2 * I);
-  // multiplier 4^-I and addend -(128 * 4^-I + 1), both exact in bf16
-  constexpr uint32_t kMul = I == 0 ? 0x3F803F80u : (I == 1 ? 0x3E803E80u : 0x3D803D80u);
-  constexpr uint32_t kAdd = I == 0 ? 0xC301C301u : (I == 1 ? 0xC204C204u : 0xC110C110u);
-  return bf16x2_fma_bits(lop_and_or(v, kMask, 0x43004300u), kMul, kAdd);
+__device__ __forceinline__ uint32_t decode_e4m3(uint32_t v) {
+  constexpr uint32_t kShift = I == 0 ? 5u : (I == 1 ? 4u : (I == 2 ? 1u : 0u));
+  return (v << kShift) & 0xA0A0A0A0u;
 }
 
-// All 8 pairs of one word: out[p] = (w[field p], w[field p+8]) as bf16x2.
-__device__ __forceinline__ void decode_word_bf16(uint32_t v, uint32_t out[8]) {
-  const uint32_t v6 = v >> 6;
-  const uint32_t v12 = v >> 12;
-  out[0] = decode_pos<0>(v);
-  out[1] = decode_pos<1>(v);
-  out[2] = decode_pos<2>(v);
-  out[3] = decode_pos<0>(v6);
-  out[4] = decode_pos<1>(v6);
-  out[5] = decode_pos<2>(v6);
-  out[6] = decode_pos<0>(v12);
-  out[7] = decode_pos<1>(v12);
+// e4m3-decoded weights -> int8 w in natural byte order: for a packed word v,
+// out[b] holds w[4b .. 4b+3] (byte i of out[b] = w[4b + i]).
+__device__ __forceinline__ void decode_word_s8(uint32_t v, uint32_t out[4]) {
+  uint32_t t[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t r = i == 0 ? decode_e4m3<0>(v)
+                     : i == 1 ? decode_e4m3<1>(v)
+                     : i == 2 ? decode_e4m3<2>(v) : decode_e4m3<3>(v);
+    const uint32_t nz = (r >> 5) & 0x01010101u;
+    const uint32_t ng = (r >> 7) & nz;
+    t[i] = nz | (ng * 0xFEu);  // byte: 0, +1 (0x01) or -1 (0xFF); no carries
+  }
+  // 4x4 byte transpose: out[b] byte i = t[i] byte b
+  const uint32_t a01 = __byte_perm(t[0], t[1], 0x5140);  // t0b0 t1b0 t0b1 t1b1
+  const uint32_t a23 = __byte_perm(t[2], t[3], 0x5140);
+  const uint32_t b01 = __byte_perm(t[0], t[1], 0x7362);  // t0b2 t1b2 t0b3 t1b3
+  const uint32_t b23 = __byte_perm(t[2], t[3], 0x7362);
+  out[0] = __byte_perm(a01, a23, 0x5410);
+  out[1] = __byte_perm(a01, a23, 0x7632);
+  out[2] = __byte_perm(b01, b23, 0x5410);
+  out[3] = __byte_perm(b01, b23, 0x7632);
 }
 
-// 4 digits of one byte (fields 0..3 of the low byte of b) -> 4 int8 w values
-// (byte i = w of field i), using carry-free byte arithmetic.
-__device__ __forceinline__ uint32_t decode_byte_s8(uint32_t b) {
-  uint32_t x = (b | (b << 12)) & 0x000F000Fu;   // fields 0,1 -> bits 0..3; 2,3 -> 16..19
-  x = (x | (x << 6)) & 0x03030303u;             // field i -> bits 8i, 8i+1
-  // c - 1 per byte without borrows: ((c | 0x80) - 1) ^ 0x80
-  return ((x | 0x80808080u) - 0x01010101u) ^ 0x80808080u;
+// One lane of the (fully converged) warp is elected; returns true there.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+// Tensor-memory (TMEM) allocation, 32x32b loads/stores (each thread of a warp
+// owns one TMEM lane of its warp's 32-lane quarter), fences, the f8f6f4 MMA
+// with A in TMEM and B in shared memory, and commit-to-mbarrier.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t r[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] x B[smem desc]; kind::f8f6f4, cta_group::1.
+__device__ __forceinline__ void mma_f8f6f4_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,
+                                              uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+      "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+// Shared-memory matrix descriptor: K-major, no swizzle (8-row x 16-byte core
+// matrices), lbo = byte stride between core matrices along K, sbo = along
+// M/N.  Bits: start>>4 [0,14), lbo>>4 [16,30), sbo>>4 [32,46), version 1 at 46.
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor for kind::f8f6f4, e4m3 x e4m3 -> f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- MMA
 __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
                                                uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_e4m3_16832(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void mma_s8_16832(int d[4], const uint32_t a[4], uint32_t b0,
                                              uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])

@@ -8,23 +8,23 @@
 
 namespace tern {
 
-// Small-T bf16 rungs: rows per CTA row block and k per pipeline stage.
-constexpr int kSTRows = 128;
-constexpr int kSTStageK = 512;        // 128 packed bytes per row
+// Small-T rungs (T <= 16): k per pipeline stage and ring depth.  Token tiles
+// are TT = 1, 4, 8 or 16 tokens.
+constexpr int kSTStageK = 512;  // 128 packed bytes per row
 constexpr int kSTStages = 4;
-constexpr int kSTConsumerWarps = 4;
-constexpr int kSTThreads = (kSTConsumerWarps + 1) * 32;
 
-size_t smallt_smem_bytes(int nt);
-
-// Launch one token tile of the small-T kernel.
-//   nt = 1 (8 tokens) or 2 (16 tokens); t1 = token tile known to hold one token.
-//   tok0: first token of the tile.  num_ctas: persistent grid size.
-cudaError_t launch_smallt(int nt, bool t1, const CUtensorMap* tmW, const uint16_t* scales,
-                          const uint16_t* x, float* y, int T, int K, int N, int tok0,
-                          int num_ctas, int* err, cudaStream_t stream);
+// Bytes of the activation-fragment buffer one TT tile needs for K.
+size_t smallt_xprep_bytes(int tt, int K);
+// Rows per CTA row block for TT (the TMA box height).
+int smallt_rows(int tt);
 cudaError_t smallt_set_attributes();
-int smallt_ctas_per_sm(int nt);
+int smallt_ctas_per_sm(int tt);
+// Launch the prep kernel and the main kernel (programmatic dependent) for
+// tokens [tok0, tok0 + Tt) with Tt <= tt.  xprep: workspace of
+// smallt_xprep_bytes(tt, K) bytes.
+cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales,
+                          const uint16_t* x, uint8_t* xprep, float* y, int K, int N, int tok0,
+                          int Tt, int num_sms, int ctas_per_sm, int* err, cudaStream_t stream);
 
 // s8 rung.
 constexpr int kS8TileN = 128;

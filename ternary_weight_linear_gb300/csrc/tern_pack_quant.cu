@@ -1,10 +1,16 @@
-// tern_pack: int8 ternary weights -> 2-bit trit digits (c = w + 1).
+// tern_pack: int8 ternary weights -> 2-bit sign-magnitude codes.
 // tern_quant_act_s8: per-token absmax/127 int8 quantisation of bf16 rows.
 #include "tern_device.cuh"
 #include "tern_internal.h"
 
 namespace tern {
 namespace {
+
+// Bit of weight j's "nonzero" flag inside its byte; the "negative" flag sits
+// two bits higher.  Each nibble holds two weights as [nz_lo, nz_hi, neg_lo,
+// neg_hi], so that one AND with 0xA0 per byte isolates one weight as the
+// fp8 e4m3 encoding of w/8 (bit 5 = exponent bit for 2^-3, bit 7 = sign).
+__device__ __constant__ int kPackNzBit[4] = {0, 1, 4, 5};
 
 // One thread per packed word: 16 int8 weights in, one uint32 out.
 __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ W,
@@ -19,15 +25,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ W,
     const uint32_t b[4] = {v.x, v.y, v.z, v.w};
     uint32_t word = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 4; ++q) {      // output byte q <- weights 4q .. 4q+3
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 4; ++j) {    // weight j of the byte
         int w = static_cast<int8_t>((b[q] >> (8 * j)) & 0xFFu);
         if (w < -1 || w > 1) {
           ++bad;
           w = 0;
         }
-        word |= static_cast<uint32_t>(w + 1) << (2 * (4 * q + j));
+        const int p = 8 * q + kPackNzBit[j];
+        word |= (static_cast<uint32_t>(w != 0) << p) | (static_cast<uint32_t>(w < 0) << (p + 2));
       }
     }
     Wp[i] = word;

@@ -101,11 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        uint4 o;
-        o.x = decode_byte_s8(words[m] & 0xFFu);
-        o.y = decode_byte_s8((words[m] >> 8) & 0xFFu);
-        o.z = decode_byte_s8((words[m] >> 16) & 0xFFu);
-        o.w = decode_byte_s8(words[m] >> 24);
+        uint32_t d[4];
+        decode_word_s8(words[m], d);  // 16 int8 weights in k order
+        const uint4 o = make_uint4(d[0], d[1], d[2], d[3]);
         const int c = 4 * hh + m;
         *reinterpret_cast<uint4*>(smem + S8Layout::kDecOff + r * 128 + ((c ^ (r & 7)) << 4)) = o;
       }

@@ -78,14 +78,14 @@ def test_pack_layout_golden_words():
 
 def test_pack_word_and_row_order():
     # Two rows, K = 48: word index n*(K/16) + k/16.  One nonzero weight per row
-    # at a hand-chosen position; every other field is 0b01.
+    # at a hand-chosen position; every other weight is 0 (no bits set).
     W = np.zeros((2, 48), dtype=np.int8)
-    W[0, 17] = -1   # word 1 of row 0, field 1 -> 0x55555551
-    W[1, 40] = 1    # word 2 of row 1, field 8 -> 0x55565555
+    W[0, 17] = -1   # word 1 of row 0, byte 0, i = 1 -> 0x0000000A
+    W[1, 40] = 1    # word 2 of row 1, byte 2, i = 0 -> 0x00010000
     wp, _ = oracle.pack(W)
-    expect = np.full((2, 3), 0x55555555, dtype=np.uint32)
-    expect[0, 1] = 0x55555551
-    expect[1, 2] = 0x55565555
+    expect = np.zeros((2, 3), dtype=np.uint32)
+    expect[0, 1] = 0x0000000A
+    expect[1, 2] = 0x00010000
     assert np.array_equal(wp, expect)
 
 
@@ -103,13 +103,14 @@ def test_pack_counts_invalid_values():
     W[0, 9] = -5
     wp, bad = oracle.pack(W)
     assert bad == 2
-    assert int(wp[0, 0]) == 0x55555555  # invalid values stored as 0
+    assert int(wp[0, 0]) == 0  # invalid values stored as 0
 
 
-def test_unpack_counts_invalid_code():
-    wp = np.array([[0x55555555 | (3 << 6)]], dtype=np.uint32)  # field 3 = 0b11
+def test_unpack_counts_invalid_pair():
+    # weight 3 of byte 0: negative bit (bit 7) set without its nonzero bit (bit 5)
+    wp = np.array([[0x00000080]], dtype=np.uint32)
     W, bad = oracle.unpack(wp, 16)
-    assert bad == 1 and W[0, 3] == 0
+    assert bad == 1 and W[0, 3] == 0 and not W.any()
 
 
 # ---------------------------------------------------------------- bf16 rungs
