@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary-weight linear layer on GB300.
+
+Headline metric: ternary linear weight GB/s at T = 1 (decode GEMV), as a
+fraction of the measured HBM peak; alongside it, int8-operand TOPS of the s8
+prefill rung at T = 2048.
+
+Step (N = 1): one T = 1 decode pass over a stack of L layers of the 27B-like
+MLP projections (fused gate+up 5120 x 34816, then down 17408 x 5120), weights
+resident in HBM, captured once as a CUDA graph and replayed.  The stack holds
+L * 71 MB of packed weights (L = 8: 570 MB, more than 4x the 129 MB L2), so a
+step streams every weight byte from HBM; no L2 flush is needed.
+
+Inputs are synthetic and seeded (ternary with P(0) = 0.4, log-normal group
+scales, N(0,1) activations with 1% outlier channels x20), generated on the
+device.  The weights are packed by the library's own tern_pack.
+
+Reference arm (--impl reference): the CPU oracle (the library's test
+definition, plain C) timed on this host's cores on a bounded sample of the
+same step.  Multi-GPU (torchrun): every rank runs its own replica (the layer
+does not shard); value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+GU = (5120, 2 * 17408)
+DN = (17408, 5120)
+GROUP = 128
+
+
+def weight_bytes(K, N):
+    return K * N // 4 + N * (K // GROUP) * 2
+
+
+def algorithmic_bytes(T, K, N):
+    """Bytes one call must move at least: packed weights, scales, bf16 x, fp32 y."""
+    return weight_bytes(K, N) + 2 * T * K + 4 * T * N
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def profile_traffic(kernel_src, summary_name):
+    """DRAM bytes per launch recorded by the committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m_bytes or not m_sha:
+        return None
+    with open(kernel_src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return float(m_bytes.group(1)) if sha == m_sha.group(1) else None
+
+
+# ---------------------------------------------------------------- ours
+
+def make_layer(tl, torch, K, N, gen, dev):
+    # ternary weights with P(0) = 0.4, P(+1) = P(-1) = 0.3
+    r = torch.randint(0, 10, (N, K), generator=gen, device=dev, dtype=torch.int8)
+    W = torch.zeros_like(r)
+    W[(r >= 4) & (r < 7)] = 1
+    W[r >= 7] = -1
+    Wp = tl.tern_pack(W)
+    del r, W
+    s = torch.exp(torch.randn(N, K // GROUP, generator=gen, device=dev) * 0.3 - 3.5).half()
+    return Wp, s
+
+
+def make_x(torch, T, K, gen, dev):
+    x = torch.randn(T, K, generator=gen, device=dev)
+    ch = torch.randperm(K, generator=gen, device=dev)[: max(1, round(0.01 * K))]
+    x[:, ch] *= 20.0
+    return x.bfloat16()
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import ternary_weight_linear_gb300 as tl
+
+    tl.build()
+    tl.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    peaks, peak_kind = load_peaks()
+
+    L = args.layers
+    layers = [(make_layer(tl, torch, *GU, gen, dev), make_layer(tl, torch, *DN, gen, dev))
+              for _ in range(L)]
+    T = 1
+    x_gu = make_x(torch, T, GU[0], gen, dev)
+    x_dn = make_x(torch, T, DN[0], gen, dev)
+    y_gu = [torch.empty(T, GU[1], device=dev) for _ in range(L)]
+    y_dn = [torch.empty(T, DN[1], device=dev) for _ in range(L)]
+    ws_bytes = max(tl.tern_linear_workspace_bytes(T, *GU), tl.tern_linear_workspace_bytes(T, *DN))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    step_bytes = L * (weight_bytes(*GU) + weight_bytes(*DN))
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step_calls():
+        for i, ((gw, gs), (dw, ds)) in enumerate(layers):
+            tl.tern_linear(gw, gs, x_gu, y_gu[i], ws)
+            tl.tern_linear(dw, ds, x_dn, y_dn[i], ws)
+
+    with torch.cuda.stream(stream):
+        step_calls()  # library init outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step_calls()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if tl.tern_device_status() != 0:
+        raise RuntimeError("device error word set after warm-up")
+
+    # ---- timed region: K graph replays
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9  # GB/s, whole job
+
+    # ---- dominant kernel: the gate+up T=1 call, timed back to back
+    reps = 200
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g2, stream=stream):
+            for i in range(L):
+                tl.tern_linear(layers[i][0][0], layers[i][0][1], x_gu, y_gu[i], ws)
+    g2.replay()
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(True), torch.cuda.Event(True)
+    with torch.cuda.stream(stream):
+        e2.record(stream)
+        for _ in range(reps):
+            g2.replay()
+        e3.record(stream)
+    torch.cuda.synchronize()
+    gu_us = e2.elapsed_time(e3) * 1e3 / (reps * L)
+    gu_alg = algorithmic_bytes(T, *GU)
+    gu_gbs = gu_alg / (gu_us * 1e-6) / 1e9
+    traffic = profile_traffic(os.path.join(ROOT, "ternary_weight_linear_gb300", "csrc", "tern_smallt.cu"),
+                              "smallt_kernel_gu_t1.md")
+    roofline = {"bound": "hbm", "kernel": "tern_linear T=1 gate+up 5120x34816 (prep + smallt_kernel)",
+                "achieved": round(gu_gbs, 1), "peak": peaks["hbm_gbs"], "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": round(gu_gbs / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": gu_alg,
+                "avg_launch_us": round(gu_us, 3)}
+
+    # ---- s8 prefill rung at T = 2048 (gate+up and down)
+    T8 = 2048
+    x8_gu = make_x(torch, T8, GU[0], gen, dev)
+    x8_dn = make_x(torch, T8, DN[0], gen, dev)
+    y8_gu = torch.empty(T8, GU[1], device=dev)
+    y8_dn = torch.empty(T8, DN[1], device=dev)
+    ws8 = torch.empty(max(tl.tern_linear_workspace_bytes(T8, *GU), tl.tern_linear_workspace_bytes(T8, *DN)),
+                      dtype=torch.uint8, device=dev)
+    (gw, gs), (dw, ds) = layers[0]
+    for _ in range(3):
+        tl.tern_linear(gw, gs, x8_gu, y8_gu, ws8)
+        tl.tern_linear(dw, ds, x8_dn, y8_dn, ws8)
+    torch.cuda.synchronize()
+    reps8 = 10
+    e4, e5 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e4.record()
+    for _ in range(reps8):
+        tl.tern_linear(gw, gs, x8_gu, y8_gu, ws8)
+        tl.tern_linear(dw, ds, x8_dn, y8_dn, ws8)
+    e5.record()
+    torch.cuda.synchronize()
+    s8_ms = e4.elapsed_time(e5) / reps8
+    s8_ops = 2.0 * T8 * (GU[0] * GU[1] + DN[0] * DN[1])
+    s8_tops = s8_ops / (s8_ms * 1e-3) / 1e12
+    # int8 tensor rate on GB300: the s8 rung's MMA instruction is mma.sync
+    # m16n8k32 s8; its peak is not in the measured-peaks file, so the fraction
+    # is reported against the bf16 tensor peak as the nominal dense ceiling.
+    s8 = {"metric": "int8 TOPS at T=2048 (s8 rung, gate+up + down)", "value": round(s8_tops, 1),
+          "unit": "TOPS", "ms_per_pass": round(s8_ms, 3),
+          "roofline": {"bound": "tensor", "achieved": round(s8_tops, 1),
+                       "peak": peaks.get("bf16_tflops", 1900.0), "peak_kind": peak_kind + " bf16",
+                       "unit": "TOPS", "frac": round(s8_tops / peaks.get("bf16_tflops", 1900.0), 4),
+                       "traffic": None}}
+
+    # ---- end to end through the C ABI with host buffers
+    import numpy as np
+    xh_gu = x_gu.cpu().pin_memory()
+    xh_dn = x_dn.cpu().pin_memory()
+    yh = torch.empty(T, DN[1], dtype=torch.float32).pin_memory()
+    e2e_steps = max(10, min(200, args.steps // 10))
+    h2d = (xh_gu.numel() * 2 + xh_dn.numel() * 2) * L
+    d2h = yh.numel() * 4
+    torch.cuda.synchronize()
+    ee0, ee1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    with torch.cuda.stream(stream):
+        ee0.record(stream)
+        for _ in range(e2e_steps):
+            for i, ((gw, gs), (dw, ds)) in enumerate(layers):
+                x_gu.copy_(xh_gu, non_blocking=True)
+                tl.tern_linear(gw, gs, x_gu, y_gu[i], ws)
+                x_dn.copy_(xh_dn, non_blocking=True)
+                tl.tern_linear(dw, ds, x_dn, y_dn[i], ws)
+            yh.copy_(y_dn[-1], non_blocking=True)
+        ee1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
+    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    if not np.isfinite(yh.numpy()).all():
+        raise RuntimeError("non-finite output")
+    if tl.tern_device_status() != 0:
+        raise RuntimeError("device error word set")
+
+    launches = args.steps * L * 2 * 2  # per call: activation prep + main kernel
+    out = {
+        "metric": "ternary linear weight GB/s at T=1 (frac of HBM peak); int8 TOPS at T=2048",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 tensor-core products, fp32 accumulation",
+        "data": "synthetic",
+        "config": {"workload": f"decode GEMV T=1 over {L} layers x (gate+up 5120x34816, down 17408x5120), "
+                               "27B-like MLP shapes",
+                   "layers": L, "T": T, "weight_bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (weights per step > 4x L2, no flush)",
+                   "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
+        "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
+        "roofline": roofline,
+        "s8_t2048": s8,
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "path": "pinned host x -> device copy, tern_linear via the C ABI (eager), y -> pinned host"},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(sample_layers=1)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def cpu_baseline(sample_layers=1):
+    """The CPU oracle on one layer of the same step (gate+up then down, T = 1),
+    on this host's cores.  Returns weight GB/s."""
+    import numpy as np
+    import oracle
+    import synth
+
+    oracle.build()
+    cg = synth.config_decode("gu")
+    cd = synth.config_decode("dn")
+    wpg, _ = oracle.pack(cg.W)
+    wpd, _ = oracle.pack(cd.W)
+    del cg.W, cd.W
+    # repeat the layer pass for about 10 s of CPU work
+    t0 = time.perf_counter()
+    passes = 0
+    while passes < sample_layers or time.perf_counter() - t0 < 10.0:
+        oracle.linear_f64(wpg, cg.scales, cg.x, 1, *GU)
+        oracle.linear_f64(wpd, cd.scales, cd.x, 1, *DN)
+        passes += 1
+    dt = time.perf_counter() - t0
+    b = passes * (weight_bytes(*GU) + weight_bytes(*DN))
+    return {"value": round(b / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{passes} passes over one layer of the step (gate+up and down at T=1, "
+                      "full outputs), about 10 s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    oracle.build()
+    cg = synth.config_decode("gu")
+    cd = synth.config_decode("dn")
+    wpg, _ = oracle.pack(cg.W)
+    wpd, _ = oracle.pack(cd.W)
+    # bounded sample per step: 2048 rows of gate+up and 512 rows of down
+    rows_g, rows_d = 2048, 512
+    wg, sg = wpg[:rows_g], cg.scales[:rows_g]
+    wd, sd = wpd[:rows_d], cd.scales[:rows_d]
+    per_step = weight_bytes(GU[0], rows_g) + weight_bytes(DN[0], rows_d)
+    for _ in range(args.warmup):
+        oracle.linear_f64(wg, sg, cg.x, 1, GU[0], rows_g)
+        oracle.linear_f64(wd, sd, cd.x, 1, DN[0], rows_d)
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.linear_f64(wg, sg, cg.x, 1, GU[0], rows_g)
+        oracle.linear_f64(wd, sd, cd.x, 1, DN[0], rows_d)
+    dt = (time.perf_counter() - t0) / steps
+    value = per_step / dt / 1e9
+    out = {"impl": "reference",
+           "metric": "ternary linear weight GB/s at T=1 (frac of HBM peak); int8 TOPS at T=2048",
+           "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": steps,
+           "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "decode GEMV T=1, gate+up 5120x34816 and down 17408x5120 "
+                                  "bounded row sample per step",
+                      "rows_per_step": {"gate_up": rows_g, "down": rows_d}},
+           "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+                            "kind": "oracle",
+                            "sample": f"{rows_g} gate+up rows + {rows_d} down rows per step, T=1"},
+           "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -17,7 +17,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libtern.so")
 SOURCES = ["tern_api.cu", "tern_pack_quant.cu", "tern_smallt.cu", "tern_s8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+NVFLAGS = ["-I" + os.path.join(HERE, "..", "include"), "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
            "-Xptxas", "-warn-spills"]
 
 

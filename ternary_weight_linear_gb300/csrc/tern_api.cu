@@ -17,7 +17,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "../../include/tern.h"
+#include "tern.h"
 #include "tern_internal.h"
 
 namespace tern {

@@ -168,6 +168,16 @@ __device__ __forceinline__ uint32_t decode_e4m3(uint32_t v) {
   return (v << kShift) & 0xA0A0A0A0u;
 }
 
+// Same decode with the left shift done as an integer multiply by mul = 2^shift
+// held in a register the compiler cannot fold (mul[I] = 32, 16, 2, 1): the
+// multiply issues on the FMA pipe and the AND on the ALU pipe, so a stream of
+// decodes uses both pipes instead of two ALU slots per result.
+__device__ __forceinline__ uint32_t decode_e4m3_mul(uint32_t v, uint32_t mul) {
+  uint32_t p;
+  asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(p) : "r"(v), "r"(mul));
+  return p & 0xA0A0A0A0u;
+}
+
 // e4m3-decoded weights -> int8 w in natural byte order: for a packed word v,
 // out[b] holds w[4b .. 4b+3] (byte i of out[b] = w[4b + i]).
 __device__ __forceinline__ void decode_word_s8(uint32_t v, uint32_t out[4]) {
@@ -253,6 +263,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t r[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t r[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
 }
 // D[tmem] (+)= A[tmem] x B[smem desc]; kind::f8f6f4, cta_group::1.
 __device__ __forceinline__ void mma_f8f6f4_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,

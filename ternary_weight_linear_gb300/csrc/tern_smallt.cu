@@ -383,14 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<const uint32_t*>(smem + C::kSOff + s * C::kSBytes + r * 8 + 4 * h);
       const float* fv =
           reinterpret_cast<const float*>(smem + C::kXOff + s * C::kXBytes + C::kXFrag);
+      // Only the accumulator columns that carry tokens are read back (TMEM
+      // loads are the scarce resource of this loop): piece 0 of token t is
+      // column t, piece 1 is column H + t.
       uint32_t d[2][NC];
 #pragma unroll
       for (int gg = 0; gg < 2; ++gg) {
         const int g = 2 * h + gg;
         if (g < ng) {
-          tmem_ld16(tbase + lane_off + C::kDCol + (b * 4 + g) * NC, d[gg]);
-          if constexpr (NC == 32)
-            tmem_ld16(tbase + lane_off + C::kDCol + (b * 4 + g) * NC + 16, d[gg] + 16);
+          const uint32_t dbase = tbase + lane_off + C::kDCol + (b * 4 + g) * NC;
+          if constexpr (TT == 1) {
+            tmem_ld1(dbase, d[gg][0]);
+            tmem_ld1(dbase + H, d[gg][H]);
+          } else if constexpr (TT == 4) {
+            tmem_ld4(dbase, d[gg]);
+            tmem_ld4(dbase + H, d[gg] + H);
+          } else {
+            tmem_ld16(dbase, d[gg]);
+            if constexpr (NC == 32) tmem_ld16(dbase + 16, d[gg] + 16);
+          }
         }
       }
       tmem_wait_ld();
