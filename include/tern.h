@@ -124,6 +124,44 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
                 const uint16_t* x, float* y, int T, int K, int N,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the fixed device scratch tern_linear_small_t_noalloc uses. */
+#define TERN_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* tern_linear for T = 1..16 without a caller workspace and without allocating.
+ *
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory or hand over a workspace: plug-in interfaces
+ * that pass only input and output buffers, engines that reserve all device
+ * memory at start-up and forbid allocation afterwards, and latency-critical
+ * code where cudaMalloc / cudaFree would synchronise the device.
+ *
+ *   Wpacked, scales, x, y, T, K, N, stream: as for tern_linear.
+ *   1 <= T <= 16 (TERN_EINVAL otherwise).  The rung comes from T alone:
+ *   "gemv" at T = 1, "small_t" at T = 2..8, "small_t_tiled" at T = 9..16; the
+ *   environment overrides of tern_linear do not apply.
+ *
+ * Scratch.  The activation fragments live in one file-scope device array of
+ * TERN_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library; every GPU that loads
+ * the library holds it until the process exits.  A call whose fragments do
+ * not fit returns TERN_ENOSPACE before any device work: K <= 64512 for
+ * T <= 8 and K <= 32256 for T = 9..16.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Set-up.  The first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and performs the library's
+ * per-device set-up (kernel attributes); make that first call before any
+ * stream capture.
+ *
+ * Sharing.  Every call on a device uses the same array, and the array keeps
+ * the last call's contents.  Each call rewrites every scratch byte it reads
+ * before reading it, so nothing needs clearing between calls.  Calls whose
+ * work overlaps on the GPU (e.g. on two streams without ordering between
+ * them) race on the array and give wrong results: order them on one stream
+ * or with events. */
+int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
+                                const uint16_t* x, float* y, int T, int K, int N,
+                                void* stream);
+
 /* Rung the dispatcher picks for T (after env overrides).  Host-only. */
 int tern_select_rung(int T);
 

@@ -22,7 +22,7 @@ __all__ = [
     "tern_pack", "tern_quant_act_s8", "tern_linear", "tern_linear_workspace_bytes",
     "tern_select_rung", "tern_rung_name", "tern_last_rung", "tern_last_rung_id",
     "tern_reload_env", "tern_device_status", "tern_status_string", "TernError", "load",
-    "RUNGS", "EXPORTED_SYMBOLS",
+    "tern_linear_small_t_noalloc", "RUNGS", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
 RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8"}
@@ -32,7 +32,11 @@ EXPORTED_SYMBOLS = (
     "tern_pack", "tern_quant_act_s8", "tern_linear_workspace_bytes", "tern_linear",
     "tern_select_rung", "tern_rung_name", "tern_last_rung_id", "tern_last_rung",
     "tern_status_string", "tern_reload_env", "tern_device_status",
+    "tern_linear_small_t_noalloc",
 )
+
+# Size of the library's fixed scratch for tern_linear_small_t_noalloc.
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +82,8 @@ def load() -> ctypes.CDLL:
         lib.tern_reload_env.restype = None
         lib.tern_device_status.argtypes = [P]
         lib.tern_device_status.restype = I
+        lib.tern_linear_small_t_noalloc.argtypes = [P, P, P, P, I, I, I, P]
+        lib.tern_linear_small_t_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -171,6 +177,28 @@ def tern_linear(Wpacked: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
         _dev(x, "x", torch.bfloat16), _dev(y, "y", torch.float32, (T, N)),
         T, K, N, pws, nws, _stream(stream))
     _check("tern_linear", rc)
+    return y
+
+
+def tern_linear_small_t_noalloc(Wpacked: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
+                                y: torch.Tensor, stream=None) -> torch.Tensor:
+    """tern_linear for T = 1..16 that takes no workspace and allocates nothing.
+
+    For callers that cannot allocate device memory (plug-in interfaces that
+    pass only inputs and outputs, engines that forbid allocation after
+    start-up, latency-critical code where cudaMalloc/cudaFree would
+    synchronise the device).  The library's fixed 1 MiB device scratch is
+    shared by every call on a device, so calls must not overlap on the GPU.
+    The first call on a device does per-device set-up and should come before
+    any stream capture.  `y` must be given (fp32 [T, N])."""
+    T, K = x.shape
+    N = Wpacked.shape[0]
+    rc = load().tern_linear_small_t_noalloc(
+        _dev(Wpacked, "Wpacked", torch.int32, (N, K // 16)),
+        _dev(scales, "scales", torch.float16, (N, K // 128)),
+        _dev(x, "x", torch.bfloat16), _dev(y, "y", torch.float32, (T, N)),
+        T, K, N, _stream(stream))
+    _check("tern_linear_small_t_noalloc", rc)
     return y
 
 

@@ -24,6 +24,11 @@ namespace tern {
 
 __device__ int g_device_error;  // one per device (module globals are per device)
 
+// Fixed scratch of tern_linear_small_t_noalloc, one copy per device that loads
+// the library.  In host code this name only stands in for the symbol; its
+// device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[TERN_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 // ------------------------------------------------------------------ config
@@ -205,6 +210,24 @@ int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, co
   return TERN_OK;
 }
 
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TERN_ENODEV;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_noalloc_ptr[dev]) {
+    uint8_t* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess)
+      return TERN_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TERN_OK;
+}
+
 }  // namespace
 }  // namespace tern
 
@@ -328,6 +351,33 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
   if (rc == TERN_OK) {
     t_last_rung = rung;
     probe(c, rung, T, K, N);
+  }
+  return rc;
+}
+
+int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
+                                const uint16_t* x, float* y, int T, int K, int N,
+                                void* stream) {
+  if (!Wpacked || !scales || !x || !y || T < 1 || T > 16 || N < 1 || K < 128 ||
+      (K % 128) != 0)
+    return TERN_EINVAL;
+  if (!aligned16(Wpacked) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
+    return TERN_EALIGN;
+  const int rung = T == 1 ? TERN_RUNG_GEMV : T <= 8 ? TERN_RUNG_SMALL_T : TERN_RUNG_SMALL_T_TILED;
+  int tt = 0, take = 0;
+  small_t_tile(rung, T, &tt, &take);
+  if (smallt_xprep_bytes(tt, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  uint8_t* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != TERN_OK) return rc;
+  rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch,
+                   static_cast<cudaStream_t>(stream));
+  if (rc == TERN_OK) {
+    t_last_rung = rung;
+    probe(config(), rung, T, K, N);
   }
   return rc;
 }
