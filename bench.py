@@ -193,10 +193,11 @@ def run_ours(args, rank, world, local):
     y_gu = [torch.empty(T, GU[1], device=dev) for _ in range(L)]
     y_dn = [torch.empty(T, DN[1], device=dev) for _ in range(L)]
     ws_bytes = max(tl.tern_linear_workspace_bytes(T, *GU), tl.tern_linear_workspace_bytes(T, *DN))
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # sync area must start zeroed
     step_bytes = L * (weight_bytes(*GU) + weight_bytes(*DN))
 
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())  # inputs and the zeroed workspace
 
     def step_calls():
         for i, ((gw, gs), (dw, ds)) in enumerate(layers):
@@ -274,7 +275,7 @@ def run_ours(args, rank, world, local):
     x8_dn = make_x(torch, T8, DN[0], gen, dev)
     y8_gu = torch.empty(T8, GU[1], device=dev)
     y8_dn = torch.empty(T8, DN[1], device=dev)
-    ws8 = torch.empty(max(tl.tern_linear_workspace_bytes(T8, *GU), tl.tern_linear_workspace_bytes(T8, *DN)),
+    ws8 = torch.zeros(max(tl.tern_linear_workspace_bytes(T8, *GU), tl.tern_linear_workspace_bytes(T8, *DN)),
                       dtype=torch.uint8, device=dev)
     (gw, gs), (dw, ds) = layers[0]
     for _ in range(3):

@@ -96,9 +96,13 @@ int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count,
 int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T,
                       int K, void* stream);
 
+/* Bytes of the synchronisation area at the start of every workspace. */
+#define TERN_SYNC_BYTES 4096u
+
 /* Bytes of device workspace tern_linear needs for (T, K, N); the value covers
- * every rung (int8 codes and scales for the s8 rung, the per-call activation
- * fragments for the small-T rungs).  Host-only; 0 for T < 1 or K < 1. */
+ * every rung: the synchronisation area, then int8 codes and scales for the s8
+ * rung, or partial sums and activation blocks for the small-T rungs.
+ * Host-only; 0 for T < 1 or K < 1. */
 size_t tern_linear_workspace_bytes(int T, int K, int N);
 
 /* y = x W^T with group scales:
@@ -115,9 +119,21 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  *   T >= 1, K >= 128 with K % 128 == 0, N >= 1
  *   workspace, workspace_bytes: device scratch of at least
  *            tern_linear_workspace_bytes(T, K, N) bytes, 16-byte aligned
- *            (TERN_ENOSPACE if smaller).  Contents on entry are ignored; it
- *            must not be used by anything else until the call's work on
- *            `stream` has finished.
+ *            (TERN_ENOSPACE if smaller).  Its first TERN_SYNC_BYTES bytes are
+ *            a synchronisation area (a counter the CTAs of a launch use to
+ *            order their updates of rows they share) owned by the library:
+ *            zero it once before the workspace's first use (e.g. with
+ *            cudaMemset), then leave it alone; every call that completes
+ *            without a device-side error leaves it valid for the next.
+ *            After TERN_ETIMEOUT from tern_device_status, zero it again.  The
+ *            rest of the workspace is scratch whose contents on entry are
+ *            ignored.  The workspace must not be used by anything else (nor
+ *            by another tern_linear call) until the call's work on `stream`
+ *            has finished.
+ * The small-T kernels use programmatic dependent launch: a kernel may start
+ * (and warm L2 with its weights) while the previous kernel on the stream
+ * finishes, but reads x / weights and writes y / the workspace only after it
+ * has completed.
  * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
  * Every rung is correct for every T. */
 int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
@@ -125,7 +141,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of the fixed device scratch tern_linear_small_t_noalloc uses. */
-#define TERN_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define TERN_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* tern_linear for T = 1..16 without a caller workspace and without allocating.
  *
@@ -140,11 +156,12 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
  *   "gemv" at T = 1, "small_t" at T = 2..8, "small_t_tiled" at T = 9..16; the
  *   environment overrides of tern_linear do not apply.
  *
- * Scratch.  The activation fragments live in one file-scope device array of
- * TERN_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library; every GPU that loads
- * the library holds it until the process exits.  A call whose fragments do
- * not fit returns TERN_ENOSPACE before any device work: K <= 64512 for
- * T <= 8 and K <= 32256 for T = 9..16.  The call allocates nothing: no
+ * Scratch.  The call's workspace (the synchronisation area, partial sums and
+ * activation blocks) lives in one file-scope device array of
+ * TERN_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that loads
+ * the library holds it until the process exits.  A call whose workspace does
+ * not fit returns TERN_ENOSPACE before any device work: K <= 257536 for
+ * T = 1..8 and K <= 128512 for T = 9..16.  The call allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
  * Set-up.  The first call on a device (with that device current) looks up the
@@ -153,11 +170,14 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
  * stream capture.
  *
  * Sharing.  Every call on a device uses the same array, and the array keeps
- * the last call's contents.  Each call rewrites every scratch byte it reads
- * before reading it, so nothing needs clearing between calls.  Calls whose
- * work overlaps on the GPU (e.g. on two streams without ordering between
- * them) race on the array and give wrong results: order them on one stream
- * or with events. */
+ * the last call's contents.  The array is zero when the library loads; its
+ * synchronisation area is left valid by every call that completes without a
+ * device-side error, and every other byte a call reads it has written first,
+ * so nothing needs clearing between calls.  When tern_device_status reports
+ * TERN_ETIMEOUT it also zeroes the array's synchronisation area on that
+ * device.  Calls whose work overlaps on the GPU (e.g. on two streams without
+ * ordering between them) race on the array and give wrong results: order
+ * them on one stream or with events. */
 int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
                                 const uint16_t* x, float* y, int T, int K, int N,
                                 void* stream);
@@ -182,7 +202,9 @@ void tern_reload_env(void);
 
 /* Synchronises `stream`, then returns and clears the current device's
  * asynchronous error word: TERN_OK, or TERN_ETIMEOUT if a kernel's bounded
- * wait ran out since the last call. */
+ * wait ran out since the last call (in which case it also zeroes the
+ * synchronisation area of tern_linear_small_t_noalloc's scratch, if that
+ * scratch is set up on this device). */
 int tern_device_status(void* stream);
 
 #ifdef __cplusplus

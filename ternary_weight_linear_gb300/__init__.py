@@ -22,7 +22,7 @@ __all__ = [
     "tern_pack", "tern_quant_act_s8", "tern_linear", "tern_linear_workspace_bytes",
     "tern_select_rung", "tern_rung_name", "tern_last_rung", "tern_last_rung_id",
     "tern_reload_env", "tern_device_status", "tern_status_string", "TernError", "load",
-    "tern_linear_small_t_noalloc", "RUNGS", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
+    "tern_linear_small_t_noalloc", "RUNGS", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES", "SYNC_BYTES",
 ]
 
 RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8"}
@@ -36,7 +36,10 @@ EXPORTED_SYMBOLS = (
 )
 
 # Size of the library's fixed scratch for tern_linear_small_t_noalloc.
-NOALLOC_SCRATCH_BYTES = 1 << 20
+NOALLOC_SCRATCH_BYTES = 4 << 20
+# Leading bytes of every workspace owned by the library (TERN_SYNC_BYTES):
+# zero before first use, then left alone.
+SYNC_BYTES = 4096
 
 _lock = threading.Lock()
 _lib = None
@@ -161,14 +164,21 @@ def tern_linear(Wpacked: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
                 y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 stream=None) -> torch.Tensor:
     """y [T, N] fp32 = ternary linear of bf16 x [T, K] with packed weights [N, K/16]
-    and fp16 group scales [N, K/128]."""
+    and fp16 group scales [N, K/128].
+
+    `workspace` (uint8, at least tern_linear_workspace_bytes(T, K, N) bytes) is
+    allocated zeroed per call when omitted.  A workspace kept across calls
+    must start with SYNC_BYTES zero bytes before its first use and then be
+    left alone (the library keeps that area valid); zero it again after
+    tern_device_status reports a timeout."""
     T, K = x.shape
     N = Wpacked.shape[0]
     if y is None:
         y = torch.empty((T, N), dtype=torch.float32, device=x.device)
     need = tern_linear_workspace_bytes(T, K, N)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        # zeros: the leading synchronisation area must start zeroed
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
     pws = _dev(workspace, "workspace", torch.uint8) if workspace is not None else None
     nws = workspace.numel() if workspace is not None else 0
     rc = load().tern_linear(
@@ -187,7 +197,7 @@ def tern_linear_small_t_noalloc(Wpacked: torch.Tensor, scales: torch.Tensor, x: 
     For callers that cannot allocate device memory (plug-in interfaces that
     pass only inputs and outputs, engines that forbid allocation after
     start-up, latency-critical code where cudaMalloc/cudaFree would
-    synchronise the device).  The library's fixed 1 MiB device scratch is
+    synchronise the device).  The library's fixed 4 MiB device scratch is
     shared by every call on a device, so calls must not overlap on the GPU.
     The first call on a device does per-device set-up and should come before
     any stream capture.  `y` must be given (fp32 [T, N])."""

@@ -116,7 +116,6 @@ struct DevState {
   bool ready = false;
   int sms = 0;
   int* err = nullptr;
-  int smallt_cpm[17] = {};  // CTAs per SM by token tile TT (1, 4, 8, 16)
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -137,7 +136,6 @@ int device_state(DevState** out) {
     d.err = static_cast<int*>(p);
     if (smallt_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (s8_set_attributes() != cudaSuccess) return TERN_ECUDA;
-    for (int tt : {1, 4, 8, 16}) d.smallt_cpm[tt] = smallt_ctas_per_sm(tt);
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -174,10 +172,10 @@ size_t s8_workspace_bytes(int T, int K) {
   return align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
 }
 
-// Token tile for a rung and the tokens left: (TT, tokens in this launch).
-void small_t_tile(int rung, int left, int* tt, int* take) {
+// Token tile for a rung, the tokens left and K: (TT, tokens in this launch).
+void small_t_tile(int rung, int left, int K, int* tt, int* take) {
   if (rung == TERN_RUNG_GEMV) {
-    *tt = 1;
+    *tt = K <= kSmallTT1MaxK ? 1 : 4;
     *take = 1;
   } else if (rung == TERN_RUNG_SMALL_T) {
     *take = left < 8 ? left : 8;
@@ -188,13 +186,14 @@ void small_t_tile(int rung, int left, int* tt, int* take) {
   }
 }
 
+// ws: workspace whose first kSyncBytes are the zeroed sync area.
 int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
                 float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st) {
   CUtensorMap maps[17];
   bool have[17] = {};
   for (int tok0 = 0; tok0 < T;) {
     int tt = 0, take = 0;
-    small_t_tile(rung, T - tok0, &tt, &take);
+    small_t_tile(rung, T - tok0, K, &tt, &take);
     if (!have[tt]) {
       int rc = make_map_u8(&maps[tt], Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                            static_cast<uint64_t>(K) / 4, 128, smallt_rows(tt),
@@ -202,8 +201,8 @@ int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, co
       if (rc != TERN_OK) return rc;
       have[tt] = true;
     }
-    if (launch_smallt(tt, &maps[tt], s, x, ws, y, K, N, tok0, take, d->sms, d->smallt_cpm[tt],
-                      d->err, st) != cudaSuccess)
+    if (launch_smallt(tt, &maps[tt], s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
+                      tok0, take, d->sms, d->err, st) != cudaSuccess)
       return TERN_ECUDA;
     tok0 += take;
   }
@@ -274,11 +273,12 @@ const char* tern_last_rung(void) { return t_last_rung < 0 ? "none" : tern_rung_n
 size_t tern_linear_workspace_bytes(int T, int K, int N) {
   (void)N;
   if (T < 1 || K < 1) return 0;
-  // s8 rung: int8 codes [T][K] + fp32 x_scale [T]; small-T rungs: the
-  // activation-fragment buffer of the widest token tile.  Enough for any rung.
+  // The sync area, then the larger rung scratch: int8 codes [T][K] + fp32
+  // x_scale [T] (s8), or partial sums + activation blocks of the widest
+  // small-T token tile.  Enough for any rung.
   const size_t a = s8_workspace_bytes(T, K);
-  const size_t b = smallt_xprep_bytes(16, K);
-  return a > b ? a : b;
+  const size_t b = smallt_work_bytes(16, K);
+  return kSyncBytes + (a > b ? a : b);
 }
 
 int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count, void* stream) {
@@ -329,10 +329,10 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
                        st);
       break;
     case TERN_RUNG_S8: {
-      int8_t* q = static_cast<int8_t*>(workspace);
-      float* xs =
-          reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                   align_up(static_cast<size_t>(T) * K, 256));
+      // after the sync area, which the s8 rung leaves untouched
+      uint8_t* scratch = static_cast<uint8_t*>(workspace) + kSyncBytes;
+      int8_t* q = reinterpret_cast<int8_t*>(scratch);
+      float* xs = reinterpret_cast<float*>(scratch + align_up(static_cast<size_t>(T) * K, 256));
       if (launch_quant_s8(x, q, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
       CUtensorMap tmW, tmQ;
       rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
@@ -365,8 +365,8 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
     return TERN_EALIGN;
   const int rung = T == 1 ? TERN_RUNG_GEMV : T <= 8 ? TERN_RUNG_SMALL_T : TERN_RUNG_SMALL_T_TILED;
   int tt = 0, take = 0;
-  small_t_tile(rung, T, &tt, &take);
-  if (smallt_xprep_bytes(tt, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
+  small_t_tile(rung, T, K, &tt, &take);
+  if (kSyncBytes + smallt_work_bytes(tt, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;
@@ -393,6 +393,17 @@ int tern_device_status(void* stream) {
   if (v) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return TERN_ECUDA;
+    // counters of an interrupted call may be left set in the no-alloc scratch
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+      uint8_t* p = nullptr;
+      {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        p = g_noalloc_ptr[dev];
+      }
+      if (p && cudaMemsetAsync(p, 0, kSyncBytes, st) != cudaSuccess) return TERN_ECUDA;
+      if (p && cudaStreamSynchronize(st) != cudaSuccess) return TERN_ECUDA;
+    }
     return TERN_ETIMEOUT;
   }
   return TERN_OK;

@@ -86,6 +86,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Wait until *ctr >= target (acquire, GPU scope).  Gives up after
+// kWaitLimitNs: ORs kErrTimeout into *err and returns false.
+__device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* ctr,
+                                                      unsigned long long target, int* err) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (it == 0) t0 = global_timer_ns();
+    else if ((it & 15u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // 2D tiled load of a box into shared memory, completing on `bar`.
 // x is the innermost coordinate (in elements of the tensor map's type).
@@ -96,6 +113,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+// L2 prefetch of one tensor-map box (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
 }
 
 // 1D bulk copy global -> shared, completing on `bar` (size and both addresses
@@ -112,6 +144,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // 8-byte asynchronous copy global -> shared (LDGSTS); src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async_8(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
                : "memory");
 }
@@ -180,6 +219,18 @@ __device__ __forceinline__ uint32_t decode_e4m3_mul(uint32_t v, uint32_t mul) {
 
 // e4m3-decoded weights -> int8 w in natural byte order: for a packed word v,
 // out[b] holds w[4b .. 4b+3] (byte i of out[b] = w[4b + i]).
+// 4x4 byte transpose: out[b] byte i = in[i] byte b.
+__device__ __forceinline__ void transpose_bytes_4x4(const uint32_t in[4], uint32_t out[4]) {
+  const uint32_t a01 = __byte_perm(in[0], in[1], 0x5140);  // i0b0 i1b0 i0b1 i1b1
+  const uint32_t a23 = __byte_perm(in[2], in[3], 0x5140);
+  const uint32_t b01 = __byte_perm(in[0], in[1], 0x7362);  // i0b2 i1b2 i0b3 i1b3
+  const uint32_t b23 = __byte_perm(in[2], in[3], 0x7362);
+  out[0] = __byte_perm(a01, a23, 0x5410);
+  out[1] = __byte_perm(a01, a23, 0x7632);
+  out[2] = __byte_perm(b01, b23, 0x5410);
+  out[3] = __byte_perm(b01, b23, 0x7632);
+}
+
 __device__ __forceinline__ void decode_word_s8(uint32_t v, uint32_t out[4]) {
   uint32_t t[4];
 #pragma unroll
@@ -191,15 +242,7 @@ __device__ __forceinline__ void decode_word_s8(uint32_t v, uint32_t out[4]) {
     const uint32_t ng = (r >> 7) & nz;
     t[i] = nz | (ng * 0xFEu);  // byte: 0, +1 (0x01) or -1 (0xFF); no carries
   }
-  // 4x4 byte transpose: out[b] byte i = t[i] byte b
-  const uint32_t a01 = __byte_perm(t[0], t[1], 0x5140);  // t0b0 t1b0 t0b1 t1b1
-  const uint32_t a23 = __byte_perm(t[2], t[3], 0x5140);
-  const uint32_t b01 = __byte_perm(t[0], t[1], 0x7362);  // t0b2 t1b2 t0b3 t1b3
-  const uint32_t b23 = __byte_perm(t[2], t[3], 0x7362);
-  out[0] = __byte_perm(a01, a23, 0x5410);
-  out[1] = __byte_perm(a01, a23, 0x7632);
-  out[2] = __byte_perm(b01, b23, 0x5410);
-  out[3] = __byte_perm(b01, b23, 0x7632);
+  transpose_bytes_4x4(t, out);
 }
 
 // One lane of the (fully converged) warp is elected; returns true there.

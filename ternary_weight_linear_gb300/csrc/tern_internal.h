@@ -8,23 +8,34 @@
 
 namespace tern {
 
-// Small-T rungs (T <= 16): k per pipeline stage and ring depth.  Token tiles
-// are TT = 1, 4, 8 or 16 tokens.
+// Small-T rungs (T <= 16): k per pipeline stage.  Token tiles are TT = 1, 4,
+// 8 or 16 tokens.
 constexpr int kSTStageK = 512;  // 128 packed bytes per row
-constexpr int kSTStages = 4;
+// Grid cap of the small-T kernel (one CTA per SM).
+constexpr int kSmallTMaxCtas = 160;
+// Largest K of the one-token kernel (its activation blocks stay in shared
+// memory); a one-token call with larger K runs on the four-token tile.
+constexpr int kSmallTT1MaxK = 24576;
 
-// Bytes of the activation-fragment buffer one TT tile needs for K.
-size_t smallt_xprep_bytes(int tt, int K);
-// Rows per CTA row block for TT (the TMA box height).
+// Workspace layout shared by all rungs: a synchronisation area of kSyncBytes
+// that must hold zeros when a call starts (the small-T kernels leave it zeroed
+// again), followed by the rung's scratch.
+constexpr size_t kSyncBytes = 4096;
+static_assert(kSmallTMaxCtas * 4 * sizeof(int) <= kSyncBytes, "sync area");
+
+// Partial-sum scratch of a TT tile: [kSmallTMaxCtas][2][TT][128] fp32.
+size_t smallt_partials_bytes(int tt);
+// Scratch after the sync area for a TT tile and K: partial sums, then (TT > 1)
+// the activation blocks built by the prep kernel.
+size_t smallt_work_bytes(int tt, int K);
+// Rows per CTA row block (the TMA box height).
 int smallt_rows(int tt);
 cudaError_t smallt_set_attributes();
-int smallt_ctas_per_sm(int tt);
-// Launch the prep kernel and the main kernel (programmatic dependent) for
-// tokens [tok0, tok0 + Tt) with Tt <= tt.  xprep: workspace of
-// smallt_xprep_bytes(tt, K) bytes.
+// Launch the small-T kernel(s) for tokens [tok0, tok0 + Tt) with Tt <= tt.
+// sync: the zeroed sync area; work: smallt_work_bytes(tt, K) bytes.
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales,
-                          const uint16_t* x, uint8_t* xprep, float* y, int K, int N, int tok0,
-                          int Tt, int num_sms, int ctas_per_sm, int* err, cudaStream_t stream);
+                          const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
+                          int tok0, int Tt, int num_sms, int* err, cudaStream_t stream);
 
 // s8 rung.
 constexpr int kS8TileN = 128;

@@ -8,39 +8,62 @@
 // fp32 lane-ops per weight at full HBM rate; a CUDA-core or mma.sync GEMV
 // spends more than that on decode and fragment traffic alone).
 //
-// 1. Activation split (xprep_kernel, once per call).  Per token and per
-//    128-wide group, x is scaled by a power of two 2^p so that the group's
-//    absmax lies in [128, 256), then split exactly into two fp8 e4m3 pieces
-//    x 2^p = h1 + h2 (h1 = RN_e4m3(x 2^p), h2 = RN_e4m3(x 2^p - h1)).  A bf16
-//    value has 8 significant bits and each piece holds 4, so the split is
-//    exact for every element within 2^-10 of its group's absmax; smaller ones
-//    keep an absolute error below 2^-10 * 2^-p.  The pieces are the columns of
-//    the MMA's B operand (column piece * H + token), written straight into the
-//    tcgen05 K-major shared-memory layout, one contiguous block per 512-wide k
-//    stage, followed by the per-(group, token) factors f = 2^(3-p).
+// 1. Activation split.  Per token and per 128-wide group, x is scaled by a
+//    power of two 2^p so that the group's absmax lies in [128, 256), then
+//    split exactly into two fp8 e4m3 pieces x 2^p = h1 + h2
+//    (h1 = RN_e4m3(x 2^p), h2 = RN_e4m3(x 2^p - h1)).  A bf16 value has 8
+//    significant bits and each piece holds 4, so the split is exact for every
+//    element within 2^-10 of its group's absmax; smaller ones keep an
+//    absolute error below 2^-10 * 2^-p.  The pieces are the columns of the
+//    MMA's B operand (column piece * H + token) in the tcgen05 K-major
+//    shared-memory layout, one block per 512-wide k stage, with the
+//    per-(group, token) factors f = 2^(3-p).  At T = 1 four warps of the
+//    main kernel build the blocks of every stage the CTA visits once, into
+//    shared memory where they stay (a compact layout: see kX1Lbo); for wider
+//    token tiles a prep kernel builds all blocks once per call and the main
+//    kernel copies each stage's block in with its weights.
 // 2. Weights as fp8, decoded into tensor memory.  The packed code puts each
 //    weight's nonzero bit and sign bit at the 2^-3 exponent bit and the sign
 //    bit of an e4m3 byte once shifted, so one shift and one AND turn a packed
-//    word into four exact e4m3 values w/8.  Each decode thread owns one of
-//    the CTA's 128 rows (one TMEM lane) and stores its decoded row chunk with
-//    tcgen05.st into a double-buffered A operand in TMEM.
+//    word into four exact e4m3 values w/8.  Decode threads own rows of the
+//    CTA's 128-row block (one TMEM lane each) and store decoded row chunks
+//    with tcgen05.st into the A operand in TMEM.
 // 3. One thread issues tcgen05.mma kind::f8f6f4 (A in TMEM, B in shared
 //    memory, fp32 accumulator in TMEM), one 128 x N x 128 accumulator per
-//    128-wide group; the decode threads read it back with tcgen05.ld and fold
-//    it into their row's running sums with s[n][g] * f[g][token].
+//    128-wide group; fold threads read it back with tcgen05.ld and fold it
+//    into their row's running sums with s[n][g] * f[g][token].
 //
 // Pipeline (one CTA per SM, persistent; TMEM 512 columns):
-//   warp 4   producer: one 2D TMA box of packed weights (128 rows x 128 B,
-//            128-byte swizzle) + one bulk copy of the stage's activation block
-//            + cp.async of the stage's fp16 scales, into a ring of stages;
-//   warps 0-3 decode stage i into A[i & 1], then fold stage i-1;
-//   warp 5   allocates TMEM and issues the MMAs of stage i once A[i & 1] is
-//            full and D[i & 1] has been drained.
-// The (row block, 512-wide k stage) units are cut into equal contiguous
-// ranges, one per CTA, so every SM streams the same bytes; a row block that
-// straddles two CTAs is finished with fp32 atomics into a y the prep kernel
-// zeroed.  The main kernel is a programmatic dependent of the prep kernel, so
-// its prologue and first weight loads overlap the prep.
+//   warp 12    producer: one 2D TMA box of packed weights (128 rows x 128 B,
+//              128-byte swizzle) per stage into the weight ring (plus, for
+//              T > 1, a bulk copy of the stage's activation block); the
+//              stage's fp16 scales (cp.async) into a longer scale ring;
+//   warps 15-18 (T = 1) build the resident activation blocks and factors;
+//   warps 0-7  decode (two groups of 32 rows per warp) into A slots;
+//   warps 13-14 issue the MMAs of half-stage 0 / 1 of every stage once its
+//              A slot is full and its D slot has been drained (warp 13 also
+//              allocates TMEM);
+//   warps 8-11 fold D slots into per-row running sums (one row per thread)
+//              and write y at the end of each row block.
+//
+// Work split: the (row block, 512-wide k stage) units are cut into equal
+// contiguous ranges, one per CTA, so every SM streams the same bytes.  A row
+// block whole inside one CTA is written to y directly.  A row block split
+// between CTAs is summed with fp32 atomics into y: at its start every CTA
+// zeroes the y rows of its split row blocks and counts itself in the
+// workspace's arrival counter, and it adds into y only once the counter
+// shows that all CTAs of the launch have zeroed (by then, in practice, long
+// since true).  The atomics make the order of those few additions, and so
+// the last bits of split rows, vary from run to run.
+//
+// TMEM is used in half-stage slots: the decode warps of groups 0-1 and of
+// groups 2-3 each fill their own A slot, the MMAs of a half-stage write their
+// own D slot, so decode, MMA and fold can run several half-stages apart.
+//
+// Calls chain by programmatic dependent launch: every kernel lets the next one
+// launch as soon as all of its CTAs run; the next kernel's CTAs set up, warm
+// L2 with their first weight tiles and wait for the previous grid before they
+// read anything it may have written (weights, x) or write y / the workspace.
 //
 // The pages' kernel for this band (the "small_t" rung of the
 // "ninfer-perf-tuning" skill page, sections 2 and 6) decodes through a LUT
@@ -58,127 +81,187 @@ namespace {
 
 constexpr int kRows = 128;       // rows per CTA row block (MMA M, TMEM lanes)
 constexpr int kDecWarps = 8;     // two decode threads per row (groups split in halves)
-constexpr int kThreads = (kDecWarps + 2) * 32;
-constexpr int kProducerWarp = kDecWarps;
-constexpr int kMmaWarp = kDecWarps + 1;
+constexpr int kFoldWarps = 4;    // one fold thread per row
+constexpr int kProducerWarp = kDecWarps + kFoldWarps;
+// Two MMA-issuing warps: the first issues half-stage 0 of every stage, the
+// second half-stage 1, so a single issuing thread never paces the tensor pipe.
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kMmaWarps = 2;
+constexpr int kXWarp0 = kMmaWarp + kMmaWarps;  // (T = 1) activation warps, one per group
 constexpr uint32_t kXLbo = 128;            // K-direction core-matrix stride in the B block
 constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (512 k per stage)
+// T = 1 activation block of one stage: only B columns 0 (h1) and 8 (h2) carry
+// data.  With a 16-byte K-direction stride, column r of a core matrix aliases
+// column 0 of the core matrix r steps further along K, so each piece needs a
+// single 512-byte row (plus 112 bytes of overrun): the other 14 accumulator
+// columns receive shifted dot products that are never read.
+constexpr uint32_t kX1Lbo = 16;
+constexpr uint32_t kX1Sbo = 640;       // h2 row
+constexpr int kX1Stage = 1280;         // bytes per stage (h1 row, h2 row, overrun)
+constexpr int kX1MaxStages = kSmallTT1MaxK / kSTStageK;
 
 template <int TT>
 struct TC {
   static constexpr int kH = TT <= 8 ? 8 : 16;  // B columns per piece
   static constexpr int kNC = 2 * kH;           // MMA N: 16 or 32
-  static constexpr int kXFrag = kNC * kSTStageK;
-  static constexpr int kXF = 4 * kH * 4;       // f[group 4][kH] fp32
-  static constexpr int kXBytes = kXFrag + kXF;
-  static constexpr int kStages = kNC == 16 ? 6 : 5;
+  static constexpr int kXFrag = kNC * kSTStageK;  // B operand of one 512-wide k stage
+  static constexpr int kXF = 4 * kH * 4;          // f[group 4][kH] fp32
+  static constexpr int kXBytes = kXFrag + kXF;    // one stage block of the prep buffer
+  static constexpr bool kInKernelX = TT == 1;     // x blocks built by the main kernel
+  static constexpr int kXWarps = kInKernelX ? 4 : 0;
+  static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
+  // TMEM is used in half-stage slots (256 k: two groups): A slots of 64
+  // columns (256 k of e4m3), D slots of 2 x kNC columns (two groups).
+  static constexpr int kNAH = TT <= 8 ? 5 : 4;
+  static constexpr int kNDH = TT <= 8 ? 6 : 4;
+  static constexpr int kStages = TT == 1 ? 8 : TT <= 8 ? 6 : 5;  // weight (+ activation) ring
+  // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
+  // ring does not wait for the MMAs, so the fold must never wait for scales).
+  static constexpr int kLead = kInKernelX ? 4 : 0;
+  // scale (+ factor) ring: held until folded, which trails the weight ring
+  // by up to (kNAH + kNDH) / 2 stages
+  static constexpr int kSStages = kStages + kLead + (kNAH + kNDH + 1) / 2;
   static constexpr int kWBytes = kRows * 128;
-  static constexpr int kSBytes = kRows * 8;
+  static constexpr int kSBytes = kRows * 8 + (kInKernelX ? 0 : kXF);  // scales [128][4], f
   static constexpr int kWOff = 0;  // 1024-aligned for the 128-byte swizzle
-  static constexpr int kXOff = kWOff + kStages * kWBytes;
-  static constexpr int kSOff = kXOff + kStages * kXBytes;
-  static constexpr int kBarOff = kSOff + kStages * kSBytes;
-  // full, empty, afull[2], mdone[2], dfree[2], xch_full, xch_empty
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kXOff = kWOff + kStages * kWBytes;  // activation ring (T > 1)
+  static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
+  static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) f[stage][4]
+  static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * 16 : 0);
+  static constexpr int kNumBars =
+      2 * kStages + 2 * kSStages + 2 * kNAH + 2 * kNDH + (kInKernelX ? kX1MaxStages : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
-  static constexpr int kXchOff = kTmemSlot + 16;             // partial sums [TT][128] fp32
-  static constexpr int kBytes = kXchOff + TT * kRows * 4;
-  static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kACol = 0;    // A[2]: 128 columns each (512 k of e4m3)
-  static constexpr uint32_t kDCol = 256;  // D[2]: 4 groups x kNC columns each
+  static constexpr int kFirstOff = kTmemSlot + 16;  // fold: parked first row block sums
+  static constexpr int kX1Off = (kFirstOff + TT * kRows * 4 + 127) / 128 * 128;  // (T = 1)
+  // shared memory for K: fixed part, the T = 1 blocks, alignment slack
+  static constexpr int smem_bytes(int KS) {
+    return kX1Off + (kInKernelX ? KS * kX1Stage : 0) + 1024;
+  }
+  static constexpr int kAllocMax = smem_bytes(kInKernelX ? kX1MaxStages : 0);
+  static constexpr uint32_t kACol = 0;             // A[kNAH]: 64 columns each
+  static constexpr uint32_t kDCol = kNAH * 64;     // D[kNDH]: 2 x kNC columns each
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kDCol + 2 * 4 * kNC <= kTmemCols, "TMEM budget");
-  static_assert(kXBytes % 16 == 0, "bulk copy size");
+  static_assert(kDCol + kNDH * 2 * kNC <= kTmemCols, "TMEM budget");
+  static_assert(kXFrag % 16 == 0 && kXF % 16 == 0 && kXBytes % 16 == 0, "bulk copy sizes");
+  static_assert(kSBytes % 16 == 0 && kBarOff % 8 == 0, "alignment");
+  static_assert(kAllocMax <= 227 * 1024, "shared memory");
 };
 
+// x 2^p -> (h1, h2), two e4m3 pieces with h1 + h2 == x 2^p for |x 2^p| < 256
+// (up to the e4m3 resolution of the remainder, see above).
+__device__ __forceinline__ void split_e4m3(float xs, uint8_t& h1, uint8_t& h2) {
+  const __nv_fp8_storage_t a = __nv_cvt_float_to_fp8(xs, __NV_SATFINITE, __NV_E4M3);
+  const float af = __half2float(__half(__nv_cvt_fp8_to_halfraw(a, __NV_E4M3)));
+  h1 = a;
+  h2 = __nv_cvt_float_to_fp8(xs - af, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Power-of-two exponent p with m 2^p in [128, 256), and f = 2^(3-p); 0 / 0 for m = 0.
+__device__ __forceinline__ void group_exponent(float m, int& p, float& f) {
+  p = 0;
+  f = 0.f;
+  if (m > 0.f) {
+    int e;
+    (void)frexpf(m, &e);  // m = fr * 2^e, fr in [0.5, 1)
+    p = 8 - e;
+    f = ldexpf(1.0f, 3 - p);
+  }
+}
+
+// CTA owning unit u when U units are cut into P equal contiguous ranges
+// (CTA c holds units [U c / P, U (c + 1) / P)).
+__device__ __forceinline__ int owner_of(long long u, long long U, long long P) {
+  return static_cast<int>(((u + 1) * P - 1) / U);
+}
+
 // ------------------------------------------------------------------ prep
-// One warp per (token slot t < H, 128-wide group).  Lane l holds k = 4l .. 4l+3
-// of the group.  Slot order inside each 16-wide block of k is the transpose
-// the decoder produces: slot 4i + b holds k = 4b + i.
+// Activation blocks of one token tile for all stages (T > 1).  One warp per
+// (token slot t < H, 128-wide group).  Lane l holds k = 4l .. 4l+3 of the
+// group.  Slot order inside each 16-wide block of k is the transpose the
+// decoder produces: slot 4i + b holds k = 4b + i.
 template <int TT>
 __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ x,
-                                                    uint8_t* __restrict__ out, float* y, int K,
-                                                    int N, int tok0, int Tt, int KS, int zero_y) {
+                                                    uint8_t* __restrict__ out, int K, int tok0,
+                                                    int Tt, int KS) {
   grid_dependents_launch();
+  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
   using C = TC<TT>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int task = blockIdx.x * 8 + warp;
   const int groups = 4 * KS;
-  if (task < C::kH * groups) {
-    const int t = task / groups;
-    const int gi = task % groups;
-    const int ks = gi >> 2, jg = gi & 3;
-    const int kbase = gi * 128 + 4 * lane;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (t < Tt && kbase < K) {
-      const uint2 raw =
-          *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
-      v[0] = __uint_as_float(raw.x << 16);
-      v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-      v[2] = __uint_as_float(raw.y << 16);
-      v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    }
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    int p = 0;
-    float f = 0.f;
-    if (m > 0.f) {
-      int e;
-      (void)frexpf(m, &e);  // m = fr * 2^e, fr in [0.5, 1)
-      p = 8 - e;            // m * 2^p in [128, 256)
-      f = ldexpf(1.0f, 3 - p);
-    }
-    uint8_t* st = out + static_cast<size_t>(ks) * C::kXBytes;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float xs = ldexpf(v[i], p);
-      const __nv_fp8_storage_t h1 = __nv_cvt_float_to_fp8(xs, __NV_SATFINITE, __NV_E4M3);
-      const float h1f = __half2float(__half(__nv_cvt_fp8_to_halfraw(h1, __NV_E4M3)));
-      const __nv_fp8_storage_t h2 = __nv_cvt_float_to_fp8(xs - h1f, __NV_SATFINITE, __NV_E4M3);
-      // k = 4 lane + i: 16-block lane/4, position b = lane%4, i -> slot 4i + b
-      const int slot = 128 * jg + 16 * (lane >> 2) + 4 * i + (lane & 3);
-#pragma unroll
-      for (int piece = 0; piece < 2; ++piece) {
-        const int n = piece * C::kH + t;
-        const int off = (n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15);
-        st[off] = piece ? h2 : h1;
-      }
-    }
-    if (lane == 0) reinterpret_cast<float*>(st + C::kXFrag)[jg * C::kH + t] = f;
+  if (task >= C::kH * groups) return;
+  const int t = task / groups;
+  const int gi = task % groups;
+  const int ks = gi >> 2, jg = gi & 3;
+  const int kbase = gi * 128 + 4 * lane;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (t < Tt && kbase < K) {
+    const uint2 raw =
+        *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
+    v[0] = __uint_as_float(raw.x << 16);
+    v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(raw.y << 16);
+    v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
   }
-  if (zero_y) {
-    const long long total = static_cast<long long>(Tt) * N;
-    float* yt = y + static_cast<size_t>(tok0) * N;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x)
-      yt[i] = 0.f;
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int p;
+  float f;
+  group_exponent(m, p, f);
+  uint8_t* st = out + static_cast<size_t>(ks) * C::kXBytes;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint8_t hp[2];
+    split_e4m3(ldexpf(v[i], p), hp[0], hp[1]);
+    // k = 4 lane + i: 16-block lane/4, position b = lane%4, i -> slot 4i + b
+    const int slot = 128 * jg + 16 * (lane >> 2) + 4 * i + (lane & 3);
+#pragma unroll
+    for (int piece = 0; piece < 2; ++piece) {
+      const int n = piece * C::kH + t;
+      const int off = (n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15);
+      st[off] = hp[piece];
+    }
   }
+  if (lane == 0) reinterpret_cast<float*>(st + C::kXFrag)[jg * C::kH + t] = f;
 }
 
 // ------------------------------------------------------------------ main
+// x: bf16 activations (read at T = 1); xprep: prep blocks (T > 1).
+// arrivals: the workspace's launch-arrival counter (see the fold warps).
 template <int TT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     smallt_kernel(const __grid_constant__ CUtensorMap tmW, const uint16_t* __restrict__ scales,
-                  const uint8_t* __restrict__ xprep, float* __restrict__ y, int K, int N,
+                  const uint16_t* __restrict__ x, const uint8_t* __restrict__ xprep,
+                  float* __restrict__ y, unsigned long long* __restrict__ arrivals, int K, int N,
                   int tok0, int Tt, int KS, long long U, int* err) {
   using C = TC<TT>;
   constexpr int S = C::kStages;
+  constexpr int SS = C::kSStages;
+  constexpr int NA = C::kNAH;
+  constexpr int ND = C::kNDH;
   constexpr int H = C::kH;
   constexpr int NC = C::kNC;
+
+  // The next kernel on the stream may launch now; it waits for this grid
+  // before touching anything this one writes.
+  grid_dependents_launch();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* empty = full + S;
-  uint64_t* afull = empty + S;
-  uint64_t* mdone = afull + 2;
-  uint64_t* dfree = mdone + 2;
-  uint64_t* xch_full = dfree + 2;
-  uint64_t* xch_empty = xch_full + 1;
+  uint64_t* empty = full + S;     // weights decoded and activation block consumed
+  uint64_t* sfull = empty + S;    // scales + factors landed
+  uint64_t* sempty = sfull + SS;  // ... and folded
+  uint64_t* afull = sempty + SS;  // A slot a written by its four decoders
+  uint64_t* afree = afull + NA;   // MMAs reading A slot a completed
+  uint64_t* mdone = afree + NA;   // MMAs writing D slot d completed
+  uint64_t* dfree = mdone + ND;   // D slot d read back by the fold warps
+  uint64_t* xready = dfree + ND;  // (T = 1) activation block of stage ks built
+  uint8_t* xres = smem + C::kX1Off;                              // (T = 1) blocks
+  float* ftab = reinterpret_cast<float*>(smem + C::kFOff);       // (T = 1) f[ks][4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
-  float* xbuf = reinterpret_cast<float*>(smem + C::kXchOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,16 +269,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 32);          // producer lanes (+ TMA / bulk bytes)
-      mbar_init(&empty[s], kDecWarps);  // stage folded
+      mbar_init(&full[s], 1);  // producer's expect_tx arrival
+      // the decoders (+ both MMA warps' commits when the stage holds activations)
+      mbar_init(&empty[s], C::kInKernelX ? kDecWarps : kDecWarps + kMmaWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&afull[b], kDecWarps);  // A[b] decoded
-      mbar_init(&mdone[b], 1);          // MMAs reading A[b] / writing D[b] done (commit)
-      mbar_init(&dfree[b], kDecWarps);  // D[b] drained
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(&sfull[s], 32);
+      mbar_init(&sempty[s], kFoldWarps);
     }
-    mbar_init(xch_full, kDecWarps / 2);   // upper decode half's partial sums written
-    mbar_init(xch_empty, kDecWarps / 2);  // ... and consumed
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(&afull[a], kDecWarps / 2);
+      mbar_init(&afree[a], 1);
+    }
+    for (int d = 0; d < ND; ++d) {
+      mbar_init(&mdone[d], 1);
+      mbar_init(&dfree[d], kFoldWarps);
+    }
+    if constexpr (C::kInKernelX)
+      for (int k = 0; k < KS; ++k) mbar_init(&xready[k], C::kXWarps);
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -206,60 +297,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const long long P = gridDim.x;
-  const long long begin = U * blockIdx.x / P;
-  const long long end = U * (blockIdx.x + 1) / P;
+  const int cta = blockIdx.x;
+  const long long begin = U * cta / P;
+  const long long end = U * (cta + 1) / P;
   const int nunits = static_cast<int>(end - begin);
   // first unit's (row block, k stage); later ones advance incrementally
   const int rb0 = static_cast<int>(begin / KS);
   const int ks0 = static_cast<int>(begin - static_cast<long long>(rb0) * KS);
+  // Every role but the producer (which first warms L2) waits for the previous
+  // grid here, so that no bounded wait below starts its clock while a slow
+  // predecessor is still running.
+  if (warp != kProducerWarp) grid_dependency_wait();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    int it = 0;
-    bool dep_ready = false;
-    int rb = rb0, ks = ks0;
-    for (; it < nunits; ++it) {
-      const int s = it % S;
-      if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
-      uint8_t* xs = smem + C::kXOff + s * C::kXBytes;
-      if (lane == 0) {
-        mbar_expect_tx(&full[s], C::kWBytes + C::kXBytes);
-        tma_load_2d(smem + C::kWOff + s * C::kWBytes, &tmW, ks * 128, rb * kRows, &full[s]);
-        if (!dep_ready) {
-          grid_dependency_wait();  // the activation blocks come from the prep kernel
-          dep_ready = true;
+    // Warm L2 with the first stages' weights and the first row block's
+    // scales while the previous grid finishes; load only after it has.
+    if (lane == 0) {
+      int rb = rb0, ks = ks0;
+      for (int it = 0; it < nunits && it < S; ++it) {
+        tma_prefetch_2d(&tmW, ks * 128, rb * kRows);
+        if (++ks == KS) {
+          ks = 0;
+          ++rb;
         }
-        bulk_load(xs, xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXBytes, &full[s]);
       }
-      // fp16 scales of groups 4 ks .. 4 ks + 3 for rows lane + 32 i
-      uint2* sb = reinterpret_cast<uint2*>(smem + C::kSOff + s * C::kSBytes);
-      const int g0 = ks * 4;
+      const int rows = N - rb0 * kRows < kRows ? N - rb0 * kRows : kRows;
+      const uint32_t sbytes = (static_cast<uint32_t>(rows) * G * 2) & ~15u;
+      if (sbytes) bulk_prefetch_l2(scales + static_cast<size_t>(rb0) * kRows * G, sbytes);
+    }
+    grid_dependency_wait();
+    // Scale stream: unit su's fp16 scales of groups 4 ks .. 4 ks + 3 for rows
+    // lane + 32 i (and, T > 1, its factors f), into scale ring slot su % SS.
+    int su = 0, srb = rb0, sks = ks0;
+    auto issue_scales = [&]() -> bool {
+      const int ss = su % SS;
+      if (su >= SS &&
+          !__all_sync(0xffffffffu, mbar_wait(&sempty[ss], ((su / SS) & 1) ^ 1, err)))
+        return false;
+      uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
+      if constexpr (!C::kInKernelX) {
+        if (lane == 0) {
+          mbar_expect_tx(&sfull[ss], C::kXF);
+          bulk_load(sst + kRows * 8, xprep + static_cast<size_t>(sks) * C::kXBytes + C::kXFrag,
+                    C::kXF, &sfull[ss]);
+        }
+      }
+      uint2* sb = reinterpret_cast<uint2*>(sst);
+      const int g0 = sks * 4;
       if ((G & 3) == 0) {
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
-          const int n = rb * kRows + r;
+          const int n = srb * kRows + r;
           const bool in = n < N;
           cp_async_8(&sb[r], scales + static_cast<size_t>(in ? n : 0) * G + g0, in ? 8u : 0u);
         }
-        cp_async_mbar_arrive(&full[s]);
+        cp_async_mbar_arrive(&sfull[ss]);
       } else {
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
-          const int n = rb * kRows + r;
+          const int n = srb * kRows + r;
           uint2 v = make_uint2(0, 0);
           if (n < N) {
             const uint16_t* src = scales + static_cast<size_t>(n) * G + g0;
-            uint32_t h[4];
+            uint32_t hv[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = (g0 + j < G) ? src[j] : 0u;
-            v = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            for (int j = 0; j < 4; ++j) hv[j] = (g0 + j < G) ? src[j] : 0u;
+            v = make_uint2(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16));
           }
           sb[r] = v;
         }
-        mbar_arrive(&full[s]);
+        mbar_arrive(&sfull[ss]);
       }
+      ++su;
+      if (++sks == KS) {
+        sks = 0;
+        ++srb;
+      }
+      return true;
+    };
+    bool ok = true;
+    while (ok && su < nunits && su < C::kLead) ok = issue_scales();
+    int it = 0;
+    int rb = rb0, ks = ks0;
+    for (; it < nunits && ok; ++it) {
+      const int s = it % S;
+      if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
+      if (lane == 0) {
+        if constexpr (C::kInKernelX) {
+          mbar_arrive_expect_tx(&full[s], C::kWBytes);  // activations are resident
+          tma_load_2d(smem + C::kWOff + s * C::kWBytes, &tmW, ks * 128, rb * kRows, &full[s]);
+        } else {
+          mbar_arrive_expect_tx(&full[s], C::kWBytes + C::kXFrag);
+          tma_load_2d(smem + C::kWOff + s * C::kWBytes, &tmW, ks * 128, rb * kRows, &full[s]);
+          bulk_load(smem + C::kXOff + s * C::kXFrag,
+                    xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXFrag, &full[s]);
+        }
+      }
+      if (su < nunits) ok = issue_scales();
       if (++ks == KS) {
         ks = 0;
         ++rb;
@@ -268,174 +405,163 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Stay until this CTA's copies have landed (bounded).
     for (int d = (it > S ? it - S : 0); d < it; ++d)
       if (!mbar_wait(&full[d % S], (d / S) & 1, err)) break;
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop so that addresses and descriptors stay
-    // warp-uniform; one elected lane issues.
+    for (int d = (su > SS ? su - SS : 0); d < su; ++d)
+      if (!mbar_wait(&sfull[d % SS], (d / SS) & 1, err)) break;
+  } else if (warp >= kXWarp0) {
+    // ------------------------------------------------------------ activations (T = 1)
+    // Activation warp xw builds group xw of every stage this CTA visits, in
+    // visiting order, once: lane l splits k = 128 xw + 4l .. +3 of the stage.
+    if constexpr (C::kInKernelX) {
+      const int xw = warp - kXWarp0;
+      grid_dependency_wait();
+      const uint16_t* xt = x + static_cast<size_t>(tok0) * K;
+      const int nq = nunits < KS ? nunits : KS;
+      // loads of the next kXLoads stages stay in flight while one is built
+      constexpr int kXLoads = 8;
+      uint2 raw[kXLoads];
+      auto load_stage = [&](int q) -> uint2 {
+        const int ks = (ks0 + q) % KS;
+        const int k = ks * kSTStageK + 128 * xw + 4 * lane;
+        return (q < nq && k < K) ? *reinterpret_cast<const uint2*>(xt + k) : make_uint2(0, 0);
+      };
+#pragma unroll
+      for (int j = 0; j < kXLoads; ++j) raw[j] = load_stage(j);
+      for (int q0 = 0; q0 < nq; q0 += kXLoads) {
+#pragma unroll
+        for (int j = 0; j < kXLoads; ++j) {
+          const int q = q0 + j;
+          if (q >= nq) break;
+          const int ks = (ks0 + q) % KS;
+          const uint2 cur = raw[j];
+          raw[j] = load_stage(q + kXLoads);
+          const float v[4] = {__uint_as_float(cur.x << 16), __uint_as_float(cur.x & 0xFFFF0000u),
+                              __uint_as_float(cur.y << 16), __uint_as_float(cur.y & 0xFFFF0000u)};
+          float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          // floor(log2 m) from the bits; p = 7 - that puts m 2^p in [128, 256)
+          float sc1 = 0.f, sc2 = 0.f, f = 0.f;
+          if (m > 0.f) {
+            const uint32_t mb = __float_as_uint(m);
+            const int el =
+                (mb >> 23) ? static_cast<int>(mb >> 23) - 127 : (31 - __clz(mb)) - 149;
+            const int p = 7 - el;                // in [-120, 156]
+            const int p1 = p >> 1, p2 = p - p1;  // each in [-60, 78]
+            sc1 = __uint_as_float(static_cast<uint32_t>(p1 + 127) << 23);
+            sc2 = __uint_as_float(static_cast<uint32_t>(p2 + 127) << 23);
+            // f = 2^(3-p) = 2^(el-4): a normal power of two unless el is tiny
+            f = el - 4 >= -126 ? __uint_as_float(static_cast<uint32_t>(el - 4 + 127) << 23)
+                               : ldexpf(1.0f, el - 4);
+          }
+          uint32_t h1 = 0, h2 = 0;  // byte i: piece of k = 4l + i
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const float2 xs = make_float2((v[2 * hf] * sc1) * sc2, (v[2 * hf + 1] * sc1) * sc2);
+            const __nv_fp8x2_storage_t a =
+                __nv_cvt_float2_to_fp8x2(xs, __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw ar = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
+            const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&ar));
+            const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
+                make_float2(xs.x - af.x, xs.y - af.y), __NV_SATFINITE, __NV_E4M3);
+            h1 |= static_cast<uint32_t>(a) << (16 * hf);
+            h2 |= static_cast<uint32_t>(c) << (16 * hf);
+          }
+          // 16-block 8 xw + l/4, position b = l%4: value i goes to slot 4i + b
+          uint8_t* blk = xres + ks * kX1Stage + (8 * xw + (lane >> 2)) * 16 + (lane & 3);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            blk[4 * i] = static_cast<uint8_t>(h1 >> (8 * i));
+            blk[kX1Sbo + 4 * i] = static_cast<uint8_t>(h2 >> (8 * i));
+          }
+          if (lane == 0) ftab[ks * 4 + xw] = f;
+          fence_proxy_async_smem();  // the MMA reads the block through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xready[ks]);
+        }
+      }
+    }
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each warp runs its loop whole so that addresses and descriptors stay
+    // warp-uniform; one elected lane issues.  Half-stage hu = 2 it + hh
+    // (groups 2 hh, 2 hh + 1) uses A slot hu % NA and D slot hu % ND and is
+    // issued by MMA warp hh.
+    const int hh = warp - kMmaWarp;
     const bool leader = elect_one();
     constexpr uint32_t idesc = idesc_e4m3_f32(kRows, NC);
     // Descriptor of stage 0's B block; a stage / k chunk only moves the start
     // address field (address >> 4 in the low bits).
-    const uint64_t desc0 = smem_desc_kmajor(smem_addr(smem + C::kXOff), kXLbo, kXSbo);
+    const uint64_t desc0 =
+        C::kInKernelX ? smem_desc_kmajor(smem_addr(xres), kX1Lbo, kX1Sbo)
+                      : smem_desc_kmajor(smem_addr(smem + C::kXOff), kXLbo, kXSbo);
+    constexpr uint32_t kLbo = C::kInKernelX ? kX1Lbo : kXLbo;
     int it = 0;
     int ks = ks0;
-    for (; it < nunits; ++it) {
-      const int b = it & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&afull[b], (it >> 1) & 1, err))) break;
-      if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(&dfree[b], ((it >> 1) & 1) ^ 1, err)))
-        break;
-      tc_fence_after();
-      const uint64_t dstage = desc0 + static_cast<uint64_t>(((it % S) * C::kXBytes) >> 4);
-      const uint32_t dcol = tbase + C::kDCol + b * 4 * NC;
-      const uint32_t acol = tbase + C::kACol + b * 128;
+    bool ok = true;
+    for (; it < nunits && ok; ++it) {
+      const int s = it % S;
       const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
-      if (leader) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          if (g < ng) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8f6f4_ts(dcol + g * NC, acol + g * 32 + kk * 8,
-                            dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kXLbo) >> 4), idesc,
-                            kk > 0);
-          }
-        }
-        mma_commit(&mdone[b]);
+      const uint64_t dstage =
+          desc0 + static_cast<uint64_t>(
+                      (C::kInKernelX ? ks * kX1Stage : s * C::kXFrag) >> 4);
+      if constexpr (C::kInKernelX) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
       }
-      __syncwarp();
+      {
+        const int hu = 2 * it + hh;
+        const int a = hu % NA;
+        const int d = hu % ND;
+        if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (hu / NA) & 1, err)) ||
+            (hu >= ND &&
+             !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err)))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dcol = tbase + C::kDCol + d * 2 * NC;
+        const uint32_t acol = tbase + C::kACol + a * 64;
+        if (leader) {
+#pragma unroll
+          for (int gg = 0; gg < 2; ++gg) {
+            const int g = 2 * hh + gg;
+            if (g < ng) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
+                              dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
+                              idesc, kk > 0);
+            }
+          }
+          if (!C::kInKernelX) mma_commit(&empty[s]);
+          mma_commit(&afree[a]);
+          mma_commit(&mdone[d]);
+        }
+        __syncwarp();
+      }
       if (++ks == KS) ks = 0;
     }
-    // Before TMEM is released, the last MMAs issued must have completed.
-    for (int d = (it > 2 ? it - 2 : 0); d < it; ++d)
-      if (!mbar_wait(&mdone[d & 1], (d >> 1) & 1, err)) break;
-  } else {
-    // ------------------------------------------------------------ decode + fold
+    // Before TMEM is released, this warp's last MMAs must have completed.
+    if (it > 0) {
+      const int hu = 2 * (it - 1) + hh;
+      mbar_wait(&mdone[hu % ND], (hu / ND) & 1, err);
+    }
+  } else if (warp < kDecWarps) {
+    // ------------------------------------------------------------ decode
     // Warp w owns TMEM lane quarter q = w % 4 (rows 32 q .. 32 q + 31) and the
     // two groups 2 h, 2 h + 1 (h = w / 4) of every stage.
     const int q = warp & 3;
     const int h = warp >> 2;
     const int r = q * 32 + lane;  // row within the block == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    float yacc[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
-    int cur_rb = -1;
-    bool cur_from_start = false;
-    int cur_last_ks = -1;
-    bool dep_ready = false;
-    bool ok = true;
-    int nflush = 0;
-
-    // Both halves hold partial sums of the same rows: the upper half hands its
-    // sums over through shared memory, the lower half adds and writes y.
-    auto flush = [&](int rb, bool whole) -> bool {
-      if (!dep_ready) {
-        grid_dependency_wait();  // y was zeroed by the prep kernel
-        dep_ready = true;
-      }
-      bool fine = true;
-      if (h == 1) {
-        if (nflush > 0)
-          fine = __all_sync(0xffffffffu, mbar_wait(xch_empty, (nflush - 1) & 1, err));
-        if (fine) {
-#pragma unroll
-          for (int t = 0; t < TT; ++t) xbuf[t * kRows + r] = yacc[t];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xch_full);
-      } else {
-        fine = __all_sync(0xffffffffu, mbar_wait(xch_full, nflush & 1, err));
-        if (fine) {
-          const int n = rb * kRows + r;
-#pragma unroll
-          for (int t = 0; t < TT; ++t) {
-            const float v = yacc[t] + xbuf[t * kRows + r];
-            if (n < N && t < Tt) {
-              float* dst = y + static_cast<size_t>(tok0 + t) * N + n;
-              if (whole) *dst = v;
-              else atomicAdd(dst, v);
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xch_empty);
-      }
-#pragma unroll
-      for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
-      ++nflush;
-      return fine;
-    };
-
-    auto fold = [&](int j, int rb, int ks) -> bool {
-      const int b = j & 1;
-      const int s = j % S;
-      if (!__all_sync(0xffffffffu, mbar_wait(&mdone[b], (j >> 1) & 1, err))) return false;
-      tc_fence_after();
-      if (rb != cur_rb) {
-        if (cur_rb >= 0 && !flush(cur_rb, cur_from_start && cur_last_ks == KS - 1)) return false;
-        cur_rb = rb;
-        cur_from_start = (ks == 0);
-      }
-      cur_last_ks = ks;
-      const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
-      // scales of groups 2h, 2h+1 for this row
-      const uint32_t sw =
-          *reinterpret_cast<const uint32_t*>(smem + C::kSOff + s * C::kSBytes + r * 8 + 4 * h);
-      const float* fv =
-          reinterpret_cast<const float*>(smem + C::kXOff + s * C::kXBytes + C::kXFrag);
-      // Only the accumulator columns that carry tokens are read back (TMEM
-      // loads are the scarce resource of this loop): piece 0 of token t is
-      // column t, piece 1 is column H + t.
-      uint32_t d[2][NC];
-#pragma unroll
-      for (int gg = 0; gg < 2; ++gg) {
-        const int g = 2 * h + gg;
-        if (g < ng) {
-          const uint32_t dbase = tbase + lane_off + C::kDCol + (b * 4 + g) * NC;
-          if constexpr (TT == 1) {
-            tmem_ld1(dbase, d[gg][0]);
-            tmem_ld1(dbase + H, d[gg][H]);
-          } else if constexpr (TT == 4) {
-            tmem_ld4(dbase, d[gg]);
-            tmem_ld4(dbase + H, d[gg] + H);
-          } else {
-            tmem_ld16(dbase, d[gg]);
-            if constexpr (NC == 32) tmem_ld16(dbase + 16, d[gg] + 16);
-          }
-        }
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int gg = 0; gg < 2; ++gg) {
-        const int g = 2 * h + gg;
-        if (g < ng) {
-          const float sg = __half2float(__ushort_as_half(
-              static_cast<unsigned short>(gg ? (sw >> 16) : (sw & 0xFFFFu))));
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-            yacc[t] = fmaf(sg * fv[g * H + t],
-                           __uint_as_float(d[gg][t]) + __uint_as_float(d[gg][H + t]), yacc[t]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&dfree[b]);
-        mbar_arrive(&empty[s]);
-      }
-      return true;
-    };
-
-    int it = 0;
-    int rb = rb0, ks = ks0, prb = rb0, pks = ks0;  // this unit and the previous one
-    for (; it < nunits && ok; ++it) {
+    int ks = ks0;
+    for (int it = 0; it < nunits; ++it) {
       const int s = it % S;
-      const int b = it & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / S) & 1, err))) {
-        ok = false;
+      const int hu = 2 * it + h;  // this warp's half-stage
+      const int a = hu % NA;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / S) & 1, err))) break;
+      if (hu >= NA && !__all_sync(0xffffffffu, mbar_wait(&afree[a], ((hu / NA) & 1) ^ 1, err)))
         break;
-      }
-      // A[b] is free: the MMAs of unit it-2 completed (waited in fold(it-2)).
+      tc_fence_after();
       const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + r * 128;
       const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
 #pragma unroll
@@ -445,34 +571,195 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 c0 = lds_v4(wrow + (((2 * g) ^ (r & 7)) << 4));
           const uint4 c1 = lds_v4(wrow + (((2 * g + 1) ^ (r & 7)) << 4));
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint32_t a[32];
+          uint32_t av[32];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            a[4 * j + 0] = decode_e4m3<0>(w[j]);
-            a[4 * j + 1] = decode_e4m3<1>(w[j]);
-            a[4 * j + 2] = decode_e4m3<2>(w[j]);
-            a[4 * j + 3] = decode_e4m3<3>(w[j]);
+            av[4 * j + 0] = decode_e4m3<0>(w[j]);
+            av[4 * j + 1] = decode_e4m3<1>(w[j]);
+            av[4 * j + 2] = decode_e4m3<2>(w[j]);
+            av[4 * j + 3] = decode_e4m3<3>(w[j]);
           }
-          tmem_st32(tbase + lane_off + C::kACol + b * 128 + g * 32, a);
+          tmem_st32(tbase + lane_off + C::kACol + a * 64 + gg * 32, av);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[b]);
-      if (it >= 1 && !fold(it - 1, prb, pks)) {
-        ok = false;
-        break;
+      if (lane == 0) {
+        mbar_arrive(&afull[a]);
+        mbar_arrive(&empty[s]);
       }
-      prb = rb;
-      pks = ks;
-      if (++ks == KS) {
-        ks = 0;
-        ++rb;
+      if (++ks == KS) ks = 0;
+    }
+  } else {
+    // ------------------------------------------------------------ fold
+    // Fold warp f owns TMEM lane quarter f (rows 32 f .. 32 f + 31) and all
+    // four groups of every stage: y[t][row] += s[row][g] * f[g][t] *
+    // (D[g][piece 0, t] + D[g][piece 1, t]).
+    const int fq = warp - kDecWarps;  // == warp % 4
+    const int r = fq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
+    float yacc[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
+
+    // Row blocks split between CTAs are summed with fp32 atomics into y.
+    // Every CTA first zeroes the y rows of its split row blocks, then adds to
+    // the launch-arrival counter; a CTA adds into y only once the counter
+    // shows that every fold warp of the launch has done its zeroing.  Each
+    // launch adds exactly 1024 in total, so the counter is a multiple of 1024
+    // between launches and needs no reset.
+    auto is_split = [&](int rb) {
+      const long long u = static_cast<long long>(rb) * KS;
+      return owner_of(u, U, P) != owner_of(u + KS - 1, U, P);
+    };
+    grid_dependency_wait();  // y and the workspace may be in use by earlier work
+    const int rb_last = static_cast<int>((end - 1) / KS);
+    {
+      const int zr[2] = {rb0, rb_last};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if ((i == 1 && rb_last == rb0) || !is_split(zr[i])) continue;
+        const int n = zr[i] * kRows + r;
+        if (n < N)
+          for (int t = 0; t < Tt; ++t) y[static_cast<size_t>(tok0 + t) * N + n] = 0.f;
       }
     }
-    if (ok && nunits > 0 && fold(nunits - 1, prb, pks) && cur_rb >= 0)
-      flush(cur_rb, cur_from_start && cur_last_ks == KS - 1);
+    __threadfence();
+    __syncwarp();
+    unsigned long long arrival_target = 0;
+    if (lane == 0) {
+      const unsigned long long add =
+          (cta == 0 && fq == 0) ? 1024ull - 4ull * static_cast<unsigned long long>(P) + 1ull : 1ull;
+      arrival_target = (atomicAdd(arrivals, add) & ~1023ull) + 1024ull;
+    }
+    arrival_target = __shfl_sync(0xffffffffu, arrival_target, 0);
+
+    // A split row block's sums are added into y only after the arrival
+    // counter shows every CTA has zeroed; so that the fold never stalls on
+    // that check mid-stream, the first row block's sums (when split) wait in
+    // shared memory and all atomics are issued once this CTA's last unit is
+    // folded.
+    float* first_part = reinterpret_cast<float*>(smem + C::kFirstOff);  // [TT][128]
+    bool first_parked = false;
+    auto flush = [&](int rb) {
+      const int n = rb * kRows + r;
+      if (!is_split(rb)) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+          if (n < N && t < Tt) y[static_cast<size_t>(tok0 + t) * N + n] = yacc[t];
+      } else if (rb == rb0 && rb != rb_last) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) first_part[t * kRows + r] = yacc[t];
+        first_parked = true;
+      } else {
+        bool fine = true;
+        if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
+        fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
+        if (fine) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+            if (n < N && t < Tt) atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n], yacc[t]);
+          if (first_parked) {
+            const int n0 = rb0 * kRows + r;
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+              if (n0 < N && t < Tt)
+                atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0], first_part[t * kRows + r]);
+            first_parked = false;
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
+    };
+
+    int ks = ks0;
+    bool ok = true;
+    for (int j = 0; j < nunits && ok; ++j) {
+      const int ss = j % SS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[ss], (j / SS) & 1, err))) break;
+      const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
+      const uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
+      const uint2 sw = lds_v2(sst + r * 8);
+      // f[g][t] at fv[g * FH + t]
+      constexpr int FH = C::kInKernelX ? 1 : H;
+      const float* fv = C::kInKernelX ? ftab + ks * 4
+                                      : reinterpret_cast<const float*>(sst + kRows * 8);
+      if constexpr (C::kInKernelX) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int hu = 2 * j + hh;
+        const int d = hu % ND;
+        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dbase = tbase + lane_off + C::kDCol + d * 2 * NC;
+        // only the accumulator columns that carry tokens are read back:
+        // piece 0 of token t is column t, piece 1 is H + t
+        uint32_t dv[2][NC];
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          const int g = 2 * hh + gg;
+          if (g < ng) {
+            const uint32_t col = dbase + gg * NC;
+            if constexpr (TT == 1) {
+              tmem_ld1(col, dv[gg][0]);
+              tmem_ld1(col + H, dv[gg][H]);
+            } else if constexpr (TT == 4) {
+              tmem_ld4(col, dv[gg]);
+              tmem_ld4(col + H, dv[gg] + H);
+            } else {
+              tmem_ld16(col, dv[gg]);
+              if constexpr (NC == 32) tmem_ld16(col + 16, dv[gg] + 16);
+            }
+          }
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dfree[d]);
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          const int g = 2 * hh + gg;
+          if (g < ng) {
+            const uint32_t s2 = hh ? sw.y : sw.x;
+            const float sg = __half2float(__ushort_as_half(
+                static_cast<unsigned short>(gg ? (s2 >> 16) : (s2 & 0xFFFFu))));
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+              yacc[t] = fmaf(sg * fv[g * FH + t],
+                             __uint_as_float(dv[gg][t]) + __uint_as_float(dv[gg][H + t]),
+                             yacc[t]);
+          }
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[ss]);
+      if (++ks == KS) {
+        flush(static_cast<int>((begin + j) / KS));
+        ks = 0;
+      }
+    }
+    // a row block whose last stage lies beyond this CTA's range
+    if (ok && ks != 0) flush(rb_last);
+    if (ok && first_parked) {
+      // the last row block was whole: add the parked first one now
+      bool fine = true;
+      if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
+      fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
+      const int n0 = rb0 * kRows + r;
+      if (fine)
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+          if (n0 < N && t < Tt)
+            atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0], first_part[t * kRows + r]);
+    }
   }
 
   tc_fence_before();
@@ -484,55 +771,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int TT>
 cudaError_t set_attr_one() {
   return cudaFuncSetAttribute(smallt_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TC<TT>::kAlloc);
+                              TC<TT>::kAllocMax);
+}
+
+cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
 }
 
 template <int TT>
 cudaError_t launch_tt(const CUtensorMap* tmW, const uint16_t* scales, const uint16_t* x,
-                      uint8_t* xprep, float* y, int K, int N, int tok0, int Tt, int num_sms,
-                      int* err, cudaStream_t stream) {
+                      int* sync, uint8_t* work, float* y, int K, int N, int tok0, int Tt,
+                      int num_sms, int* err, cudaStream_t stream) {
   using C = TC<TT>;
   const int KS = (K + kSTStageK - 1) / kSTStageK;
   const long long NB = (N + kRows - 1) / kRows;
   const long long U = NB * KS;
   long long P = num_sms;  // one CTA per SM: each holds all 512 TMEM columns
+  if (P > kSmallTMaxCtas) P = kSmallTMaxCtas;
   if (P > U) P = U;
-  // Does the split of U units over P CTAs cut a row block between two CTAs?
-  bool cut = false;
-  for (long long p = 1; p < P && !cut; ++p) cut = (U * p / P) % KS != 0;
+  uint8_t* xprep = work;
 
-  const int tasks = C::kH * 4 * KS;
-  xprep_kernel<TT><<<(tasks + 7) / 8, 256, 0, stream>>>(x, xprep, y, K, N, tok0, Tt, KS,
-                                                         cut ? 1 : 0);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(P));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kAlloc;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, scales,
-                            static_cast<const uint8_t*>(xprep), y, K, N, tok0, Tt, KS, U, err);
+  if constexpr (!C::kInKernelX) {
+    const int tasks = C::kH * 4 * KS;
+    cudaLaunchConfig_t pc = pdl_config(attr, dim3((tasks + 7) / 8), dim3(256), 0, stream);
+    cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, KS);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(static_cast<unsigned>(P)), dim3(C::kThreads),
+                                      C::smem_bytes(KS), stream);
+  return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, scales, x,
+                            static_cast<const uint8_t*>(xprep), y,
+                            reinterpret_cast<unsigned long long*>(sync), K, N, tok0, Tt, KS, U,
+                            err);
 }
 
 }  // namespace
 
-size_t smallt_xprep_bytes(int tt, int K) {
+size_t smallt_work_bytes(int tt, int K) {
   const int KS = (K + kSTStageK - 1) / kSTStageK;
-  int per = 0;
+  size_t prep = 0;
   switch (tt) {
-    case 1: per = TC<1>::kXBytes; break;
-    case 4: per = TC<4>::kXBytes; break;
-    case 8: per = TC<8>::kXBytes; break;
-    default: per = TC<16>::kXBytes; break;
+    case 1: prep = 0; break;  // built inside the main kernel
+    case 4: prep = static_cast<size_t>(TC<4>::kXBytes) * KS; break;
+    case 8: prep = static_cast<size_t>(TC<8>::kXBytes) * KS; break;
+    default: prep = static_cast<size_t>(TC<16>::kXBytes) * KS; break;
   }
-  return static_cast<size_t>(per) * KS;
+  return prep;
 }
 
 int smallt_rows(int) { return kRows; }
@@ -546,18 +841,18 @@ cudaError_t smallt_set_attributes() {
   return cudaSuccess;
 }
 
-int smallt_ctas_per_sm(int) { return 1; }
-
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales,
-                          const uint16_t* x, uint8_t* xprep, float* y, int K, int N, int tok0,
-                          int Tt, int num_sms, int ctas_per_sm, int* err, cudaStream_t stream) {
-  (void)ctas_per_sm;
+                          const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
+                          int tok0, int Tt, int num_sms, int* err, cudaStream_t stream) {
   switch (tt) {
-    case 1: return launch_tt<1>(tmW, scales, x, xprep, y, K, N, tok0, Tt, num_sms, err, stream);
-    case 4: return launch_tt<4>(tmW, scales, x, xprep, y, K, N, tok0, Tt, num_sms, err, stream);
-    case 8: return launch_tt<8>(tmW, scales, x, xprep, y, K, N, tok0, Tt, num_sms, err, stream);
+    case 1:
+      return launch_tt<1>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+    case 4:
+      return launch_tt<4>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+    case 8:
+      return launch_tt<8>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
     default:
-      return launch_tt<16>(tmW, scales, x, xprep, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<16>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
   }
 }
 

@@ -149,6 +149,35 @@ def test_default_dispatch(tl, T, expect):
     assert _check_case(tl, case, None) == expect
 
 
+@pytest.mark.parametrize("K", [24576, 25088])
+def test_gemv_k_limit_of_the_one_token_tile(tl, K):
+    # 24576 is the largest K whose activation blocks stay resident in the
+    # one-token kernel; 25088 runs on the four-token tile.  N = 300 over 64+
+    # stages cuts most row blocks between CTAs.
+    _check_case(tl, synth.case("bigk", 1, K=K, N=300, seed=K))
+
+
+def test_workspace_reused_across_calls(tl):
+    import torch
+    cases = [synth.case("ws_a", 1, K=1152, N=700, seed=5),
+             synth.case("ws_b", 12, K=17408, N=300, seed=6),
+             synth.case("ws_c", 3, K=640, N=1000, seed=7)]
+    need = max(tl.tern_linear_workspace_bytes(c.T, c.K, c.N) for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for c in cases:
+            W, s, x = to_device(c)
+            y = tl.tern_linear(tl.tern_pack(W), s, x, workspace=ws)
+            torch.cuda.synchronize()
+            assert tl.tern_device_status() == 0
+            wp_ref, _ = oracle.pack(c.W)
+            y_ref, m = oracle.linear_f64(wp_ref, c.scales, c.x, c.T, c.K, c.N)
+            assert_bf16_parity(y.cpu().numpy(), y_ref, m, f"{c.name} pass {rep}")
+    # the launch-arrival counter advances by whole launches
+    ctr = int(ws[:8].cpu().numpy().view(np.uint64)[0])
+    assert ctr % 1024 == 0 and ctr > 0
+
+
 @pytest.mark.parametrize("K,N", [(128, 1), (128, 17), (256, 129), (1152, 520), (2048, 4096)])
 def test_shapes_bf16(tl, K, N):
     for T in (1, 5, 13):

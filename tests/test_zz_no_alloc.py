@@ -33,15 +33,16 @@ def _noalloc_raw(tl, T, K, N):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(tl):
-    assert tl.NOALLOC_SCRATCH_BYTES == 1 << 20
+    assert tl.NOALLOC_SCRATCH_BYTES == 4 << 20
     # T outside 1..16
     assert _noalloc_raw(tl, 17, 512, 64) == -1
     assert _noalloc_raw(tl, 0, 512, 64) == -1
-    # K whose activation fragments exceed the 1 MiB scratch
-    assert _noalloc_raw(tl, 1, 64640, 64) == -3
-    assert _noalloc_raw(tl, 8, 64640, 64) == -3
-    assert _noalloc_raw(tl, 9, 32384, 64) == -3
-    assert _noalloc_raw(tl, 16, 32384, 64) == -3
+    # K whose activation blocks exceed the 4 MiB scratch (the largest K that
+    # fits is 257536 for T <= 8 and 128512 for T <= 16)
+    assert _noalloc_raw(tl, 1, 257664, 64) == -3
+    assert _noalloc_raw(tl, 8, 257664, 64) == -3
+    assert _noalloc_raw(tl, 9, 128640, 64) == -3
+    assert _noalloc_raw(tl, 16, 128640, 64) == -3
     assert "workspace" in tl.tern_status_string(-3)
 
 
