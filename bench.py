@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile", choices=["gu", "dn"], default=None,
+                    help="only call tern_linear on one projection at T=1 (for profilers)")
+    ap.add_argument("--profile-calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -263,7 +266,7 @@ def run_ours(args, rank, world, local):
     gu_gbs = gu_alg / (gu_us * 1e-6) / 1e9
     traffic = profile_traffic(os.path.join(ROOT, "ternary_weight_linear_gb300", "csrc", "tern_smallt.cu"),
                               "smallt_kernel_gu_t1.md")
-    roofline = {"bound": "hbm", "kernel": "tern_linear T=1 gate+up 5120x34816 (prep + smallt_kernel)",
+    roofline = {"bound": "hbm", "kernel": "tern_linear T=1 gate+up 5120x34816 (smallt_kernel<1>)",
                 "achieved": round(gu_gbs, 1), "peak": peaks["hbm_gbs"], "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": round(gu_gbs / peaks["hbm_gbs"], 4),
                 "traffic": traffic, "algorithmic_bytes_per_launch": gu_alg,
@@ -331,7 +334,7 @@ def run_ours(args, rank, world, local):
     if tl.tern_device_status() != 0:
         raise RuntimeError("device error word set")
 
-    launches = args.steps * L * 2 * 2  # per call: activation prep + main kernel
+    launches = args.steps * L * 2  # per T=1 call: one smallt_kernel<1> launch
     out = {
         "metric": "ternary linear weight GB/s at T=1 (frac of HBM peak); int8 TOPS at T=2048",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -431,9 +434,37 @@ def run_reference(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+def run_profile(args):
+    """A few T=1 calls on one synthetic projection, nothing else: the command
+    a profiler wraps to capture the decode kernel."""
+    import torch
+    import ternary_weight_linear_gb300 as tl
+
+    tl.build()
+    tl.load()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    K, N = GU if args.profile == "gu" else DN
+    Wp, s = make_layer(tl, torch, K, N, gen, dev)
+    x = make_x(torch, 1, K, gen, dev)
+    y = torch.empty(1, N, device=dev)
+    ws = torch.zeros(tl.tern_linear_workspace_bytes(1, K, N), dtype=torch.uint8, device=dev)
+    for _ in range(args.profile_calls):
+        tl.tern_linear(Wp, s, x, y, ws)
+    torch.cuda.synchronize()
+    status = tl.tern_device_status()
+    print(json.dumps({"profile": args.profile, "calls": args.profile_calls, "status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
