@@ -100,8 +100,9 @@ int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T,
 #define TERN_SYNC_BYTES 4096u
 
 /* Bytes of device workspace tern_linear needs for (T, K, N); the value covers
- * every rung: the synchronisation area, then int8 codes and scales for the s8
- * rung, or partial sums and activation blocks for the small-T rungs.
+ * every rung: the synchronisation area, then for the s8 rung the int8 codes
+ * split into two fp8 pieces (2 T K bytes) and the token scales, or the
+ * activation blocks of the small-T rungs.
  * Host-only; 0 for T < 1 or K < 1. */
 size_t tern_linear_workspace_bytes(int T, int K, int N);
 

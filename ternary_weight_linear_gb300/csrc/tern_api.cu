@@ -168,8 +168,10 @@ int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// s8 scratch: the two fp8 pieces [T][K] each, then x_scale [T] (rounded up to
+// 256 bytes, so the kernel may read it in whole 16-byte chunks).
 size_t s8_workspace_bytes(int T, int K) {
-  return align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
+  return 2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
 }
 
 // Token tile for a rung, the tokens left and K: (TT, tokens in this launch).
@@ -273,8 +275,8 @@ const char* tern_last_rung(void) { return t_last_rung < 0 ? "none" : tern_rung_n
 size_t tern_linear_workspace_bytes(int T, int K, int N) {
   (void)N;
   if (T < 1 || K < 1) return 0;
-  // The sync area, then the larger rung scratch: int8 codes [T][K] + fp32
-  // x_scale [T] (s8), or partial sums + activation blocks of the widest
+  // The sync area, then the larger rung scratch: two fp8 activation pieces
+  // [T][K] + fp32 x_scale [T] (s8), or the activation blocks of the widest
   // small-T token tile.  Enough for any rung.
   const size_t a = s8_workspace_bytes(T, K);
   const size_t b = smallt_work_bytes(16, K);
@@ -331,18 +333,25 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
     case TERN_RUNG_S8: {
       // after the sync area, which the s8 rung leaves untouched
       uint8_t* scratch = static_cast<uint8_t*>(workspace) + kSyncBytes;
-      int8_t* q = reinterpret_cast<int8_t*>(scratch);
-      float* xs = reinterpret_cast<float*>(scratch + align_up(static_cast<size_t>(T) * K, 256));
-      if (launch_quant_s8(x, q, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
-      CUtensorMap tmW, tmQ;
+      const size_t piece = align_up(static_cast<size_t>(T) * K, 256);
+      uint8_t* p1 = scratch;
+      uint8_t* p2 = scratch + piece;
+      float* xs = reinterpret_cast<float*>(scratch + 2 * piece);
+      if (launch_quant_pieces(x, p1, p2, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
+      CUtensorMap tmW, tmP1, tmP2;
       rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                        static_cast<uint64_t>(K) / 4, 32, kS8TileN, CU_TENSOR_MAP_SWIZZLE_NONE);
       if (rc != TERN_OK) return rc;
-      rc = make_map_u8(&tmQ, q, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
+      rc = make_map_u8(&tmP1, p1, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
                        static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != TERN_OK) return rc;
-      rc = launch_s8(&tmW, &tmQ, scales, xs, y, T, K, N, d->err, st) == cudaSuccess ? TERN_OK
-                                                                                   : TERN_ECUDA;
+      rc = make_map_u8(&tmP2, p2, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
+                       static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != TERN_OK) return rc;
+      rc = launch_s8(&tmW, &tmP1, &tmP2, scales, xs, y, T, K, N, d->sms, d->err, st) ==
+                   cudaSuccess
+               ? TERN_OK
+               : TERN_ECUDA;
       break;
     }
     default:

@@ -37,20 +37,25 @@ cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales
                           const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
                           int tok0, int Tt, int num_sms, int* err, cudaStream_t stream);
 
-// s8 rung.
+// s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.
 constexpr int kS8TileN = 128;
 constexpr int kS8TileT = 128;
-constexpr int kS8Stages = 4;
 size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
-cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmQ, const uint16_t* scales,
-                      const float* x_scale, float* y, int T, int K, int N, int* err,
-                      cudaStream_t stream);
+// tmW: packed weights, box 32 B x kS8TileN rows, no swizzle.  tmP1 / tmP2:
+// the two fp8 activation pieces [T][K], box 128 B x kS8TileT rows, 128-byte
+// swizzle.  x_scale: [T] floats, readable up to T rounded up to 4.
+cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
+                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
+                      int num_sms, int* err, cudaStream_t stream);
 
 // Pack and quantise.
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,
                         cudaStream_t stream);
 cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int K,
                             cudaStream_t stream);
+// The s8 rung's activations: the int8 codes split into two exact e4m3 pieces.
+cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
+                                int K, cudaStream_t stream);
 
 }  // namespace tern

@@ -1,7 +1,10 @@
 // tern_pack: int8 ternary weights -> 2-bit sign-magnitude codes.
 // tern_quant_act_s8: per-token absmax/127 int8 quantisation of bf16 rows.
+// The s8 rung's own input: the same codes split into two exact fp8 pieces.
 #include "tern_device.cuh"
 #include "tern_internal.h"
+
+#include <cuda_fp8.h>
 
 namespace tern {
 namespace {
@@ -95,6 +98,63 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
   }
 }
 
+// s8 rung input: the codes q of quant_s8_kernel (same arithmetic), split
+// exactly into two fp8 e4m3 pieces p1 = 16 floor((q + 8) / 16) and
+// p2 = q - p1 (multiples of 16 up to 128, and integers in [-8, 7]: all exact
+// in e4m3), written as p1[T][K] and p2[T][K] in the decoder's k order: within
+// every 16-wide block of k, byte slot 4i + b holds k = 4b + i.
+__global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t* __restrict__ x,
+                                                                 uint8_t* __restrict__ p1,
+                                                                 uint8_t* __restrict__ p2,
+                                                                 float* __restrict__ xs, int K) {
+  const int t = blockIdx.x;
+  const uint16_t* row = x + static_cast<size_t>(t) * K;
+  const int chunks = K >> 3;
+  float a = 0.f;
+  for (int c = threadIdx.x; c < chunks; c += kQThreads) {
+    const uint4 v = ldg_nc_v4(row + 8 * c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  __shared__ float red[kQThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  a = red[0];
+#pragma unroll
+  for (int i = 1; i < kQThreads / 32; ++i) a = fmaxf(a, red[i]);
+  const float scale = a / 127.0f;  // IEEE single-precision division
+  if (threadIdx.x == 0) xs[t] = scale;
+  for (int blk = threadIdx.x; blk < (K >> 4); blk += kQThreads) {
+    const uint4 v0 = ldg_nc_v4(row + 16 * blk);
+    const uint4 v1 = ldg_nc_v4(row + 16 * blk + 8);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      int q = 0;
+      if (a > 0.f) {
+        const float v = (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
+        const float r = fminf(fmaxf(rintf(v / scale), -127.f), 127.f);
+        q = static_cast<int>(r);
+      }
+      const int h = (q + 8) >> 4;  // floor((q + 8) / 16), in [-8, 8]
+      const uint32_t e1 = __nv_cvt_float_to_fp8(static_cast<float>(16 * h), __NV_SATFINITE,
+                                                __NV_E4M3);
+      const uint32_t e2 = __nv_cvt_float_to_fp8(static_cast<float>(q - 16 * h), __NV_SATFINITE,
+                                                __NV_E4M3);
+      const int slot = 4 * (k & 3) + (k >> 2);  // k = 4b + i -> slot 4i + b
+      o1[slot >> 2] |= e1 << (8 * (slot & 3));
+      o2[slot >> 2] |= e2 << (8 * (slot & 3));
+    }
+    const size_t off = static_cast<size_t>(t) * K + 16 * blk;
+    *reinterpret_cast<uint4*>(p1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    *reinterpret_cast<uint4*>(p2 + off) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,
@@ -111,6 +171,12 @@ cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, i
 cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int K,
                             cudaStream_t stream) {
   quant_s8_kernel<<<T, kQThreads, 0, stream>>>(x, q, xs, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
+                                int K, cudaStream_t stream) {
+  quant_pieces_kernel<<<T, kQThreads, 0, stream>>>(x, p1, p2, xs, K);
   return cudaGetLastError();
 }
 

@@ -1,211 +1,318 @@
-// s8 rung (T >= 17): int8 per-token activations x ternary-as-int8 weights,
-// exact int32 accumulation per 128-wide group, fp32 output
-//     y[t][n] = xs[t] * sum_g s[n][g] * acc[t][n][g].
+// s8 rung (T >= 17): int8 per-token activations x ternary weights, exact
+// integer accumulation per 128-wide group, fp32 output
+//     y[t][n] = xs[t] * sum_g s[n][g] * acc[t][n][g],
+//     acc[t][n][g] = sum_{k in g} q[t][k] w[n][k].
 //
-// Tile: 128 output rows x 128 tokens per CTA, 8 warps (2 x 4), each warp 64
-// rows x 32 tokens.  Per 128-wide k group:
-//   * TMA brings the group's packed weights (128 rows x 32 bytes) and its
-//     activation codes (128 tokens x 128 bytes, 128-byte swizzle) into a
-//     4-deep ring;
-//   * all threads decode the packed weights once into an int8 tile in shared
-//     memory (swizzled 16-byte chunks), shared by the four token warps;
-//   * mma.sync.m16n8k32 s8 x s8 -> s32 over the group, fragments loaded with
-//     ldmatrix; the per-group int32 result is exact (|acc| <= 127 * 128);
-//   * the epilogue turns it into fp32 exactly (1.5 * 2^23 bias) and folds it
-//     into the running sum with the row's group scale.
+// On 5th-generation tensor cores.  sm_103a has no integer tcgen05 MMA, so the
+// integers travel as exact fp8 e4m3 values:
+//   * w / 8 in {-1/8, 0, 1/8} (the packed code decodes to it with a shift and
+//     an AND, as in the small-T rungs);
+//   * q = p1 + p2 with p1 = 16 floor((q + 8) / 16) and p2 = q - p1, both
+//     exact in e4m3 (prepared by the pieces quantiser);
+// and the two pieces are fed as two halves of the contraction into the same
+// fp32 accumulator, which then holds exactly acc / 8 (|acc| <= 127 * 128, far
+// inside fp32's exact integer range; every product is a multiple of 1/8).
+//
+// Tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N).  Per
+// 128-wide group a stage holds the packed weights (TMA, 128 rows x 32 B) and
+// the two piece blocks (TMA, 128 tokens x 128 B each, 128-byte swizzle, the
+// canonical K-major SW128 layout of the MMA's B operand).  Warp roles:
+//   warps 0-3   decode the group's weights into an A slot in TMEM
+//               (tcgen05.st, one row per thread);
+//   warp 13     issues 8 MMAs per group (4 per piece, K = 32 each) into a D
+//               slot (128 columns), committing to the slot's barriers;
+//   warps 4-11  fold: read the D slot (each warp 32 rows x 64 tokens), add
+//               8 s[n][g] * D into register accumulators, and at the end of
+//               the tile write y = xs[t] * acc;
+//   warp 12     producer (TMA) and the tile's x_scale block.
+// Work: persistent CTAs walk the (row block, token tile) tiles with the token
+// tile fastest, so CTAs that run at the same time share the row block's
+// weights in L2, and the pieces of all tokens stay L2-resident.
+//
 // This is the "s8" prefill rung of the "ninfer-perf-tuning" skill page
-// (section 2 rung map; int8 m16n8k32 MMA per the "NInfer sm_89 fork"
-// write-up, section 9 item 2).
+// (section 2 rung map), with int8 activations as in the "NInfer sm_89 fork"
+// write-up (section 9 item 2); the pages run it on int8 mma.sync.
 #include "tern_device.cuh"
 #include "tern_internal.h"
 
 namespace tern {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWStage = kS8TileN * 32;   // packed weights of one group
-constexpr int kQStage = kS8TileT * 128;  // activation codes of one group
-struct S8Layout {
-  static constexpr int kQOff = 0;                                  // 1024-aligned stages
-  static constexpr int kDecOff = kQOff + kS8Stages * kQStage;      // decoded int8 [128][128]
-  static constexpr int kWOff = kDecOff + kS8TileN * 128;
-  static constexpr int kBarOff = kWOff + kS8Stages * kWStage;
-  static constexpr int kBytes = kBarOff + kS8Stages * 8;
+constexpr int kRowsS = 128;   // weight rows per tile
+constexpr int kTokS = 128;    // tokens per tile
+constexpr int kStagesS = 4;   // stage ring
+constexpr int kNAS = 4;       // A slots (32 TMEM columns = one group of e4m3)
+constexpr int kNDS = 2;       // D slots (128 columns)
+constexpr int kDecW = 4;
+constexpr int kFoldW = 8;
+constexpr int kProdW = kDecW + kFoldW;
+constexpr int kMmaW = kProdW + 1;
+constexpr int kThreadsS = (kMmaW + 1) * 32;
+
+struct SL {
+  static constexpr int kPB = kTokS * 128;   // one piece block of a group (16 KB)
+  static constexpr int kWB = kRowsS * 32;   // packed weights of a group (4 KB)
+  static constexpr int kP1Off = 0;          // 1024-aligned (128-byte swizzle atoms)
+  static constexpr int kP2Off = kP1Off + kStagesS * kPB;
+  static constexpr int kWOff = kP2Off + kStagesS * kPB;
+  static constexpr int kXsOff = kWOff + kStagesS * kWB;  // x_scale of 2 tiles
+  static constexpr int kBarOff = kXsOff + 2 * kTokS * 4;
+  static constexpr int kNumBars = 2 * kStagesS + 2 * kNAS + 2 * kNDS + 4;
+  static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kACol = 0;
+  static constexpr uint32_t kDCol = kNAS * 32;
+  static_assert(kDCol + kNDS * kTokS <= 512, "TMEM budget");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-    s8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
-              const uint16_t* __restrict__ scales, const float* __restrict__ x_scale,
-              float* __restrict__ y, int T, int K, int N, int* err) {
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes, 8-row atoms 1024 bytes apart (stride byte
+// offset), layout type 2 (SWIZZLE_128B) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__global__ void __launch_bounds__(kThreadsS, 1)
+    s8tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmP1,
+                const __grid_constant__ CUtensorMap tmP2, const uint16_t* __restrict__ scales,
+                const float* __restrict__ x_scale, float* __restrict__ y, int T, int K, int N,
+                int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S8Layout::kBarOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
+  uint64_t* empty = full + kStagesS;   // weights decoded and pieces read by the MMAs
+  uint64_t* afull = empty + kStagesS;  // A slot written
+  uint64_t* afree = afull + kNAS;      // MMAs reading the A slot done
+  uint64_t* mdone = afree + kNAS;      // MMAs writing the D slot done
+  uint64_t* dfree = mdone + kNDS;      // D slot read back
+  uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
+  uint64_t* xsfree = xsfull + 2;       // [2] ... and used
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
+  const float* xs_tile = reinterpret_cast<const float*>(smem + SL::kXsOff);
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int wm = warp >> 2;  // 0..1: rows 64 wm
-  const int wt = warp & 3;   // 0..3: tokens 32 wt
-  const int g = lane >> 2, t4 = lane & 3;
-  const int n0 = blockIdx.x * kS8TileN;
-  const int t0 = blockIdx.y * kS8TileT;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int G = K >> 7;
+  const int RB = (N + kRowsS - 1) / kRowsS;
+  const int TB = (T + kTokS - 1) / kTokS;
+  const int tiles = RB * TB;
+  const int ntiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int units = ntiles * G;
 
-  if (tid == 0) {
-    for (int s = 0; s < kS8Stages; ++s) mbar_init(&full[s], 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecW + 1);
+    }
+    for (int a = 0; a < kNAS; ++a) {
+      mbar_init(&afull[a], kDecW);
+      mbar_init(&afree[a], 1);
+    }
+    for (int d = 0; d < kNDS; ++d) {
+      mbar_init(&mdone[d], 1);
+      mbar_init(&dfree[d], kFoldW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&xsfull[b], 1);
+      mbar_init(&xsfree[b], kFoldW);
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmW);
-    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmP1);
+    prefetch_tensormap(&tmP2);
   }
+  if (warp == kMmaW) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
 
-  auto issue = [&](int grp) {
-    const int s = grp % kS8Stages;
-    mbar_arrive_expect_tx(&full[s], kWStage + kQStage);
-    tma_load_2d(smem + S8Layout::kWOff + s * kWStage, &tmW, grp * 32, n0, &full[s]);
-    tma_load_2d(smem + S8Layout::kQOff + s * kQStage, &tmQ, grp * 128, t0, &full[s]);
-  };
-  int issued = 0;  // groups issued so far (meaningful in thread 0)
-  if (tid == 0)
-    for (; issued < kS8Stages && issued < G; ++issued) issue(issued);
-
-  float yacc[4][4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) yacc[a][b][e] = 0.f;
-
-  const uint32_t dec = smem_addr(smem + S8Layout::kDecOff);
-  bool ok = true;
-  for (int grp = 0; grp < G; ++grp) {
-    const int s = grp % kS8Stages;
-    // row scales for this group (8 rows per thread), fetched before the wait
-    float sc[4][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int n = n0 + 64 * wm + 16 * mt + g + 8 * h;
-        sc[mt][h] = n < N ? __half2float(__ushort_as_half(scales[static_cast<size_t>(n) * G + grp]))
-                          : 0.f;
+  if (warp == kProdW) {
+    // ------------------------------------------------------------ producer
+    int u = 0;
+    bool ok = true;
+    for (int m = 0; m < ntiles && ok; ++m) {
+      const int tile = blockIdx.x + m * gridDim.x;
+      const int rb = tile / TB, tb = tile % TB;
+      // this tile's x_scale block (padded to whole 16-byte chunks: the
+      // workspace rounds the x_scale array up to 256 bytes)
+      const int xb = m & 1;
+      if (m >= 2 && !__all_sync(0xffffffffu, mbar_wait(&xsfree[xb], ((m >> 1) & 1) ^ 1, err))) break;
+      if (lane == 0) {
+        const int cnt = T - tb * kTokS < kTokS ? T - tb * kTokS : kTokS;
+        const uint32_t bytes = static_cast<uint32_t>((cnt * 4 + 15) & ~15);
+        mbar_arrive_expect_tx(&xsfull[xb], bytes);
+        bulk_load(smem + SL::kXsOff + xb * kTokS * 4, x_scale + tb * kTokS, bytes, &xsfull[xb]);
       }
-    const bool landed = mbar_wait(&full[s], (grp / kS8Stages) & 1, err);
-    // decode: thread -> row tid/2, 16 packed bytes (64 weights) -> 4 chunks
-    if (landed) {
-      const int r = tid >> 1, hh = tid & 1;
-      const uint4 pw =
-          *reinterpret_cast<const uint4*>(smem + S8Layout::kWOff + s * kWStage + r * 32 + hh * 16);
-      const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint32_t d[4];
-        decode_word_s8(words[m], d);  // 16 int8 weights in k order
-        const uint4 o = make_uint4(d[0], d[1], d[2], d[3]);
-        const int c = 4 * hh + m;
-        *reinterpret_cast<uint4*>(smem + S8Layout::kDecOff + r * 128 + ((c ^ (r & 7)) << 4)) = o;
-      }
-    }
-    // One vote per group: every thread either saw the stage land or timed out,
-    // so all threads take the same branch and no barrier is left waiting.
-    if (!__syncthreads_and(landed)) {
-      ok = false;
-      break;
-    }
-
-    int cacc[4][4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) cacc[a][b][e] = 0;
-
-    const uint32_t qst = smem_addr(smem + S8Layout::kQOff + s * kQStage);
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc) {
-      uint32_t af[4][4];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int row = 64 * wm + 16 * mt + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int ch = 2 * kc + (lane >> 4);
-        ldmatrix_x4(af[mt], dec + row * 128 + ((ch ^ (row & 7)) << 4));
-      }
-      uint32_t bf[4][2];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int tok = 32 * wt + 8 * (2 * p + (lane >> 4)) + (lane & 7);
-        const int ch = 2 * kc + ((lane >> 3) & 1);
-        uint32_t r[4];
-        ldmatrix_x4(r, qst + tok * 128 + ((ch ^ (tok & 7)) << 4));
-        bf[2 * p][0] = r[0];
-        bf[2 * p][1] = r[1];
-        bf[2 * p + 1][0] = r[2];
-        bf[2 * p + 1][1] = r[3];
-      }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma_s8_16832(cacc[mt][nt], af[mt], bf[nt][0], bf[nt][1]);
-    }
-    // exact int32 -> fp32, then fold in with the group scale
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        yacc[mt][nt][0] = fmaf(sc[mt][0], int_to_float_exact(cacc[mt][nt][0]), yacc[mt][nt][0]);
-        yacc[mt][nt][1] = fmaf(sc[mt][0], int_to_float_exact(cacc[mt][nt][1]), yacc[mt][nt][1]);
-        yacc[mt][nt][2] = fmaf(sc[mt][1], int_to_float_exact(cacc[mt][nt][2]), yacc[mt][nt][2]);
-        yacc[mt][nt][3] = fmaf(sc[mt][1], int_to_float_exact(cacc[mt][nt][3]), yacc[mt][nt][3]);
-      }
-    __syncthreads();  // stage s and the decoded tile are free again
-    if (tid == 0 && issued < G) issue(issued++);
-  }
-  if (!ok) {
-    // Leave only after the copies this CTA issued have landed (bounded).
-    if (tid == 0) {
-      const int first = issued > kS8Stages ? issued - kS8Stages : 0;
-      for (int gi = first; gi < issued; ++gi)
-        if (!mbar_wait(&full[gi % kS8Stages], (gi / kS8Stages) & 1, err)) break;
-    }
-    return;
-  }
-
-  // y[t][n] = xs[t] * acc
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      const int tok = t0 + 32 * wt + 8 * nt + 2 * t4 + e2;
-      if (tok >= T) continue;
-      const float xsv = x_scale[tok];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + 64 * wm + 16 * mt + g + 8 * h;
-          if (n < N) y[static_cast<size_t>(tok) * N + n] = xsv * yacc[mt][nt][2 * h + e2];
+      for (int g = 0; g < G; ++g, ++u) {
+        const int s = u % kStagesS;
+        if (u >= kStagesS &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((u / kStagesS) & 1) ^ 1, err))) {
+          ok = false;
+          break;
         }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], SL::kWB + 2 * SL::kPB);
+          tma_load_2d(smem + SL::kWOff + s * SL::kWB, &tmW, g * 32, rb * kRowsS, &full[s]);
+          tma_load_2d(smem + SL::kP1Off + s * SL::kPB, &tmP1, g * 128, tb * kTokS, &full[s]);
+          tma_load_2d(smem + SL::kP2Off + s * SL::kPB, &tmP2, g * 128, tb * kTokS, &full[s]);
+        }
+      }
     }
+    // no copy of this CTA may still be in flight when it exits
+    for (int d = (u > kStagesS ? u - kStagesS : 0); d < u; ++d)
+      if (!mbar_wait(&full[d % kStagesS], (d / kStagesS) & 1, err)) break;
+    for (int m = (ntiles > 2 ? ntiles - 2 : 0); m < ntiles; ++m)
+      if (!mbar_wait(&xsfull[m & 1], (m >> 1) & 1, err)) break;
+  } else if (warp < kDecW) {
+    // ------------------------------------------------------------ decode
+    const int r = warp * 32 + lane;  // row of the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    for (int u = 0; u < units; ++u) {
+      const int s = u % kStagesS;
+      const int a = u % kNAS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (u / kStagesS) & 1, err))) break;
+      if (u >= kNAS && !__all_sync(0xffffffffu, mbar_wait(&afree[a], ((u / kNAS) & 1) ^ 1, err)))
+        break;
+      tc_fence_after();
+      const uint8_t* wrow = smem + SL::kWOff + s * SL::kWB + r * 32;
+      const uint4 c0 = lds_v4(wrow);
+      const uint4 c1 = lds_v4(wrow + 16);
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint32_t av[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        av[4 * j + 0] = decode_e4m3<0>(w[j]);
+        av[4 * j + 1] = decode_e4m3<1>(w[j]);
+        av[4 * j + 2] = decode_e4m3<2>(w[j]);
+        av[4 * j + 3] = decode_e4m3<3>(w[j]);
+      }
+      tmem_st32(tbase + lane_off + SL::kACol + a * 32, av);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&afull[a]);
+        mbar_arrive(&empty[s]);
+      }
+    }
+  } else if (warp == kMmaW) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, kTokS);
+    const uint32_t p1base = smem_addr(smem + SL::kP1Off);
+    const uint32_t p2base = smem_addr(smem + SL::kP2Off);
+    int u = 0;
+    for (; u < units; ++u) {
+      const int s = u % kStagesS;
+      const int a = u % kNAS;
+      const int d = u % kNDS;
+      // the pieces landed (the decode warps saw it too; waiting here orders
+      // the tensor core's reads after the copy for this warp as well)
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (u / kStagesS) & 1, err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (u / kNAS) & 1, err))) break;
+      if (u >= kNDS && !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((u / kNDS) & 1) ^ 1, err)))
+        break;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t dcol = tbase + SL::kDCol + d * kTokS;
+        const uint32_t acol = tbase + SL::kACol + a * 32;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const uint32_t bb = (p ? p2base : p1base) + s * SL::kPB;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8f6f4_ts(dcol, acol + kk * 8, smem_desc_sw128(bb + kk * 32), idesc,
+                          (p | kk) != 0);
+        }
+        mma_commit(&empty[s]);
+        mma_commit(&afree[a]);
+        mma_commit(&mdone[d]);
+      }
+      __syncwarp();
+    }
+    if (u > 0) mbar_wait(&mdone[(u - 1) % kNDS], ((u - 1) / kNDS) & 1, err);
+  } else {
+    // ------------------------------------------------------------ fold
+    const int fq = warp & 3;                // TMEM lane quarter
+    const int hc = (warp - kDecW) >> 2;     // token half of the tile
+    const int r = fq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+    int u = 0;
+    bool ok = true;
+    for (int m = 0; m < ntiles && ok; ++m) {
+      const int tile = blockIdx.x + m * gridDim.x;
+      const int rb = tile / TB, tb = tile % TB;
+      const int n = rb * kRowsS + r;
+      const uint16_t* srow = scales + static_cast<size_t>(n < N ? n : 0) * G;
+      float snext = n < N ? __half2float(__ushort_as_half(srow[0])) : 0.f;
+      for (int g = 0; g < G; ++g, ++u) {
+        const int d = u % kNDS;
+        const float sg = 8.0f * snext;  // D holds acc / 8
+        if (g + 1 < G) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
+        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (u / kNDS) & 1, err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dv[64];
+        const uint32_t col = tbase + lane_off + SL::kDCol + d * kTokS + hc * 64;
+        tmem_ld32(col, dv);
+        tmem_ld32(col + 32, dv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dfree[d]);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = fmaf(sg, __uint_as_float(dv[j]), acc[j]);
+      }
+      if (!ok) break;
+      // end of the tile: y[t][n] = xs[t] * acc
+      const int xb = m & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&xsfull[xb], (m >> 1) & 1, err))) break;
+      const float* xst = xs_tile + xb * kTokS + hc * 64;
+      const int t0 = tb * kTokS + hc * 64;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const int t = t0 + j;
+        if (n < N && t < T) y[static_cast<size_t>(t) * N + n] = xst[j] * acc[j];
+        acc[j] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xsfree[xb]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaW) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
 
-size_t s8_smem_bytes() { return S8Layout::kAlloc; }
+size_t s8_smem_bytes() { return SL::kAlloc; }
 
 cudaError_t s8_set_attributes() {
-  return cudaFuncSetAttribute(s8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              S8Layout::kAlloc);
+  return cudaFuncSetAttribute(s8tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SL::kAlloc);
 }
 
-cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmQ, const uint16_t* scales,
-                      const float* x_scale, float* y, int T, int K, int N, int* err,
-                      cudaStream_t stream) {
-  dim3 grid((N + kS8TileN - 1) / kS8TileN, (T + kS8TileT - 1) / kS8TileT);
-  s8_kernel<<<grid, kThreads, S8Layout::kAlloc, stream>>>(*tmW, *tmQ, scales, x_scale, y, T, K, N,
-                                                          err);
+cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
+                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
+                      int num_sms, int* err, cudaStream_t stream) {
+  const long long tiles = static_cast<long long>((N + kRowsS - 1) / kRowsS) *
+                          ((T + kTokS - 1) / kTokS);
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  s8tc_kernel<<<grid, kThreadsS, SL::kAlloc, stream>>>(*tmW, *tmP1, *tmP2, scales, x_scale, y, T,
+                                                       K, N, err);
   return cudaGetLastError();
 }
 
