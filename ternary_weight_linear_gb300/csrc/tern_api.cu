@@ -166,6 +166,21 @@ int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
   return r == CUDA_SUCCESS ? TERN_OK : TERN_ECUDA;
 }
 
+// 2D fp32 tensor map: `inner` elements per row, `outer` rows, row pitch
+// `pitch` bytes (a multiple of 16).
+int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                 uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TERN_OK : TERN_ECUDA;
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // s8 scratch: the two fp8 pieces [T][K] each, then x_scale [T] (rounded up to
@@ -348,8 +363,15 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       rc = make_map_u8(&tmP2, p2, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
                        static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != TERN_OK) return rc;
-      rc = launch_s8(&tmW, &tmP1, &tmP2, scales, xs, y, T, K, N, d->sms, d->err, st) ==
-                   cudaSuccess
+      CUtensorMap tmY;
+      const bool y_tma = (N % 4) == 0;
+      if (y_tma) {
+        rc = make_map_f32(&tmY, y, static_cast<uint64_t>(N), static_cast<uint64_t>(T),
+                          static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);
+        if (rc != TERN_OK) return rc;
+      }
+      rc = launch_s8(&tmW, &tmP1, &tmP2, y_tma ? &tmY : nullptr, scales, xs, y, T, K, N, d->sms,
+                     d->err, st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
       break;

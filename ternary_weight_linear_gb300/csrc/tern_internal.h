@@ -40,14 +40,18 @@ cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales
 // s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.
 constexpr int kS8TileN = 128;
 constexpr int kS8TileT = 128;
+constexpr int kS8FoldWarps = 8;                          // warps folding the accumulators
+constexpr int kS8YBoxT = kS8TileT * 4 / kS8FoldWarps;   // tokens per fold warp's output box
 size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
 // tmW: packed weights, box 32 B x kS8TileN rows, no swizzle.  tmP1 / tmP2:
 // the two fp8 activation pieces [T][K], box 128 B x kS8TileT rows, 128-byte
-// swizzle.  x_scale: [T] floats, readable up to T rounded up to 4.
+// swizzle.  tmY: y as fp32 [T][N], box 32 x kS8YBoxT, or null (then y is stored
+// directly; needed when N % 4 != 0).  x_scale: [T] floats, readable up to T
+// rounded up to 4.
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
-                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
-                      int num_sms, int* err, cudaStream_t stream);
+                      const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
+                      float* y, int T, int K, int N, int num_sms, int* err, cudaStream_t stream);
 
 // Pack and quantise.
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,

@@ -19,12 +19,14 @@
 // canonical K-major SW128 layout of the MMA's B operand).  Warp roles:
 //   warps 0-3   decode the group's weights into an A slot in TMEM
 //               (tcgen05.st, one row per thread);
-//   warp 13     issues 8 MMAs per group (4 per piece, K = 32 each) into a D
-//               slot (128 columns), committing to the slot's barriers;
-//   warps 4-11  fold: read the D slot (each warp 32 rows x 64 tokens), add
+//   kFoldW warps fold: read the D slot (each warp 32 rows x kFC tokens), add
 //               8 s[n][g] * D into register accumulators, and at the end of
-//               the tile write y = xs[t] * acc;
-//   warp 12     producer (TMA) and the tile's x_scale block.
+//               the tile stage y = xs[t] * acc in shared memory and write it
+//               with a TMA store that overlaps the next tile;
+//   one warp    producer (TMA) and the tile's x_scale block;
+//   two warps   issue (one thread each, alternate groups) 8 MMAs per group
+//               (4 per piece, K = 32 each) into a D slot (128 columns),
+//               committing to the stage's and the slot's barriers.
 // Work: persistent CTAs walk the (row block, token tile) tiles with the token
 // tile fastest, so CTAs that run at the same time share the row block's
 // weights in L2, and the pieces of all tokens stay L2-resident.
@@ -40,14 +42,19 @@ namespace {
 
 constexpr int kRowsS = 128;   // weight rows per tile
 constexpr int kTokS = 128;    // tokens per tile
-constexpr int kStagesS = 4;   // stage ring
-constexpr int kNAS = 4;       // A slots (32 TMEM columns = one group of e4m3)
-constexpr int kNDS = 2;       // D slots (128 columns)
+constexpr int kStagesS = 4;   // stage ring (each stage has an A slot of 32 TMEM columns)
+constexpr int kNDS = 3;       // D slots (128 columns)
 constexpr int kDecW = 4;
-constexpr int kFoldW = 8;
+constexpr int kFoldW = kS8FoldWarps;
+constexpr int kFC = kS8YBoxT;  // tokens (D columns) per fold warp
+static_assert(kFoldW % 4 == 0 && kFC % 32 == 0 && kFC * (kFoldW / 4) == kTokS, "fold split");
 constexpr int kProdW = kDecW + kFoldW;
-constexpr int kMmaW = kProdW + 1;
-constexpr int kThreadsS = (kMmaW + 1) * 32;
+constexpr int kMmaW = kProdW + 1;  // first of kMmaWarps issuers
+// The issuing thread runs in step with the tensor pipe (an MMA issues about
+// as fast as it executes), so its barrier waits and commits would leave the
+// pipe idle; two issuers take alternate groups and cover each other's gaps.
+constexpr int kMmaWarps = 2;
+constexpr int kThreadsS = (kMmaW + kMmaWarps) * 32;
 
 struct SL {
   static constexpr int kPB = kTokS * 128;   // one piece block of a group (16 KB)
@@ -55,14 +62,16 @@ struct SL {
   static constexpr int kP1Off = 0;          // 1024-aligned (128-byte swizzle atoms)
   static constexpr int kP2Off = kP1Off + kStagesS * kPB;
   static constexpr int kWOff = kP2Off + kStagesS * kPB;
-  static constexpr int kXsOff = kWOff + kStagesS * kWB;  // x_scale of 2 tiles
+  static constexpr int kYB = kFC * 32 * 4;  // one fold warp's output block (kFC tokens x 32 rows)
+  static constexpr int kYOff = kWOff + kStagesS * kWB;
+  static constexpr int kXsOff = kYOff + kFoldW * kYB;  // x_scale of 2 tiles
   static constexpr int kBarOff = kXsOff + 2 * kTokS * 4;
-  static constexpr int kNumBars = 2 * kStagesS + 2 * kNAS + 2 * kNDS + 4;
+  static constexpr int kNumBars = 3 * kStagesS + 2 * kNDS + 4;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kACol = 0;
-  static constexpr uint32_t kDCol = kNAS * 32;
+  static constexpr uint32_t kDCol = kStagesS * 32;
   static_assert(kDCol + kNDS * kTokS <= 512, "TMEM budget");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
@@ -77,17 +86,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 
 __global__ void __launch_bounds__(kThreadsS, 1)
     s8tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmP1,
-                const __grid_constant__ CUtensorMap tmP2, const uint16_t* __restrict__ scales,
-                const float* __restrict__ x_scale, float* __restrict__ y, int T, int K, int N,
-                int* err) {
+                const __grid_constant__ CUtensorMap tmP2, const __grid_constant__ CUtensorMap tmY,
+                const uint16_t* __restrict__ scales, const float* __restrict__ x_scale,
+                float* __restrict__ y, int T, int K, int N, int y_tma, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
-  uint64_t* empty = full + kStagesS;   // weights decoded and pieces read by the MMAs
+  // empty[s]: the stage's weights are decoded and its A slot and pieces are
+  // read by the MMAs (the A ring is the stage ring, so a stage refilled by the
+  // producer also has a free A slot by the time its copy lands)
+  uint64_t* empty = full + kStagesS;
   uint64_t* afull = empty + kStagesS;  // A slot written
-  uint64_t* afree = afull + kNAS;      // MMAs reading the A slot done
-  uint64_t* mdone = afree + kNAS;      // MMAs writing the D slot done
+  uint64_t* mdone = afull + kStagesS;  // MMAs writing the D slot done
   uint64_t* dfree = mdone + kNDS;      // D slot read back
   uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
   uint64_t* xsfree = xsfull + 2;       // [2] ... and used
@@ -107,10 +118,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     for (int s = 0; s < kStagesS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecW + 1);
-    }
-    for (int a = 0; a < kNAS; ++a) {
-      mbar_init(&afull[a], kDecW);
-      mbar_init(&afree[a], 1);
+      mbar_init(&afull[s], kDecW);
     }
     for (int d = 0; d < kNDS; ++d) {
       mbar_init(&mdone[d], 1);
@@ -124,6 +132,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmP1);
     prefetch_tensormap(&tmP2);
+    if (y_tma) prefetch_tensormap(&tmY);
   }
   if (warp == kMmaW) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -133,51 +142,55 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 
   if (warp == kProdW) {
     // ------------------------------------------------------------ producer
-    int u = 0;
-    bool ok = true;
-    for (int m = 0; m < ntiles && ok; ++m) {
-      const int tile = blockIdx.x + m * gridDim.x;
-      const int rb = tile / TB, tb = tile % TB;
-      // this tile's x_scale block (padded to whole 16-byte chunks: the
-      // workspace rounds the x_scale array up to 256 bytes)
-      const int xb = m & 1;
-      if (m >= 2 && !__all_sync(0xffffffffu, mbar_wait(&xsfree[xb], ((m >> 1) & 1) ^ 1, err))) break;
-      if (lane == 0) {
+    // one thread: copies need no warp, and single-thread waits are cheapest
+    if (lane == 0) {
+      int u = 0, s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int m = 0; m < ntiles && ok; ++m) {
+        const int tile = blockIdx.x + m * gridDim.x;
+        const int rb = tile / TB, tb = tile % TB;
+        // this tile's x_scale block (padded to whole 16-byte chunks: the
+        // workspace rounds the x_scale array up to 256 bytes)
+        const int xb = m & 1;
+        if (m >= 2 && !mbar_wait(&xsfree[xb], ((m >> 1) & 1) ^ 1, err)) break;
         const int cnt = T - tb * kTokS < kTokS ? T - tb * kTokS : kTokS;
         const uint32_t bytes = static_cast<uint32_t>((cnt * 4 + 15) & ~15);
         mbar_arrive_expect_tx(&xsfull[xb], bytes);
         bulk_load(smem + SL::kXsOff + xb * kTokS * 4, x_scale + tb * kTokS, bytes, &xsfull[xb]);
-      }
-      for (int g = 0; g < G; ++g, ++u) {
-        const int s = u % kStagesS;
-        if (u >= kStagesS &&
-            !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((u / kStagesS) & 1) ^ 1, err))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+        for (int g = 0; g < G; ++g, ++u) {
+          if (u >= kStagesS && !mbar_wait(&empty[s], ph ^ 1, err)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&full[s], SL::kWB + 2 * SL::kPB);
           tma_load_2d(smem + SL::kWOff + s * SL::kWB, &tmW, g * 32, rb * kRowsS, &full[s]);
           tma_load_2d(smem + SL::kP1Off + s * SL::kPB, &tmP1, g * 128, tb * kTokS, &full[s]);
           tma_load_2d(smem + SL::kP2Off + s * SL::kPB, &tmP2, g * 128, tb * kTokS, &full[s]);
+          if (++s == kStagesS) {
+            s = 0;
+            ph ^= 1;
+          }
         }
       }
+      // no copy of this CTA may still be in flight when it exits
+      for (int v = (u > kStagesS ? u - kStagesS : 0); v < u; ++v)
+        if (!mbar_wait(&full[v % kStagesS], (v / kStagesS) & 1, err)) break;
+      for (int m = (ntiles > 2 ? ntiles - 2 : 0); m < ntiles; ++m)
+        if (!mbar_wait(&xsfull[m & 1], (m >> 1) & 1, err)) break;
     }
-    // no copy of this CTA may still be in flight when it exits
-    for (int d = (u > kStagesS ? u - kStagesS : 0); d < u; ++d)
-      if (!mbar_wait(&full[d % kStagesS], (d / kStagesS) & 1, err)) break;
-    for (int m = (ntiles > 2 ? ntiles - 2 : 0); m < ntiles; ++m)
-      if (!mbar_wait(&xsfull[m & 1], (m >> 1) & 1, err)) break;
+    __syncwarp();
   } else if (warp < kDecW) {
     // ------------------------------------------------------------ decode
     const int r = warp * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    int s = 0;
+    uint32_t ph = 0;
     for (int u = 0; u < units; ++u) {
-      const int s = u % kStagesS;
-      const int a = u % kNAS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (u / kStagesS) & 1, err))) break;
-      if (u >= kNAS && !__all_sync(0xffffffffu, mbar_wait(&afree[a], ((u / kNAS) & 1) ^ 1, err)))
-        break;
+      // the copy into stage s was issued after the MMAs that last read A
+      // slot s completed (the producer waited on empty[s]), so its landing
+      // also frees the slot
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, err))) break;
       tc_fence_after();
       const uint8_t* wrow = smem + SL::kWOff + s * SL::kWB + r * 32;
       const uint4 c0 = lds_v4(wrow);
@@ -191,61 +204,68 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         av[4 * j + 2] = decode_e4m3<2>(w[j]);
         av[4 * j + 3] = decode_e4m3<3>(w[j]);
       }
-      tmem_st32(tbase + lane_off + SL::kACol + a * 32, av);
+      tmem_st32(tbase + lane_off + SL::kACol + s * 32, av);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&afull[a]);
+        mbar_arrive(&afull[s]);
         mbar_arrive(&empty[s]);
       }
-    }
-  } else if (warp == kMmaW) {
-    // ------------------------------------------------------------ MMA issuer
-    const bool leader = elect_one();
-    constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, kTokS);
-    const uint32_t p1base = smem_addr(smem + SL::kP1Off);
-    const uint32_t p2base = smem_addr(smem + SL::kP2Off);
-    int u = 0;
-    for (; u < units; ++u) {
-      const int s = u % kStagesS;
-      const int a = u % kNAS;
-      const int d = u % kNDS;
-      // the pieces landed (the decode warps saw it too; waiting here orders
-      // the tensor core's reads after the copy for this warp as well)
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (u / kStagesS) & 1, err))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (u / kNAS) & 1, err))) break;
-      if (u >= kNDS && !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((u / kNDS) & 1) ^ 1, err)))
-        break;
-      tc_fence_after();
-      if (leader) {
-        const uint32_t dcol = tbase + SL::kDCol + d * kTokS;
-        const uint32_t acol = tbase + SL::kACol + a * 32;
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          const uint32_t bb = (p ? p2base : p1base) + s * SL::kPB;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8f6f4_ts(dcol, acol + kk * 8, smem_desc_sw128(bb + kk * 32), idesc,
-                          (p | kk) != 0);
-        }
-        mma_commit(&empty[s]);
-        mma_commit(&afree[a]);
-        mma_commit(&mdone[d]);
+      if (++s == kStagesS) {
+        s = 0;
+        ph ^= 1;
       }
-      __syncwarp();
     }
-    if (u > 0) mbar_wait(&mdone[(u - 1) % kNDS], ((u - 1) / kNDS) & 1, err);
+  } else if (warp >= kMmaW) {
+    // ------------------------------------------------------------ MMA issuers
+    // one thread per issuer warp, groups u = w, w + kMmaWarps, ...; no warp
+    // votes, two commits per group
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, kTokS);
+      const uint64_t desc1 = smem_desc_sw128(smem_addr(smem + SL::kP1Off));
+      const uint64_t desc2 = smem_desc_sw128(smem_addr(smem + SL::kP2Off));
+      int u = warp - kMmaW;
+      int last = -1;
+      for (; u < units; u += kMmaWarps) {
+        const int s = u % kStagesS, d = u % kNDS;
+        const uint32_t ph = (u / kStagesS) & 1, dph = (u / kNDS) & 1;
+        if (!mbar_wait(&afull[s], ph, err)) break;
+        // the pieces landed (implied by afull; waited on here as well so the
+        // tensor core's reads are ordered after the copy for this thread)
+        if (!mbar_wait(&full[s], ph, err)) break;
+        if (u >= kNDS && !mbar_wait(&dfree[d], dph ^ 1, err)) break;
+        tc_fence_after();
+        const uint32_t dcol = tbase + SL::kDCol + d * kTokS;
+        const uint32_t acol = tbase + SL::kACol + s * 32;
+        // descriptor start addresses advance in 16-byte units: a stage is
+        // kPB bytes, a K = 32 step 32 bytes inside the swizzle atom
+        const uint64_t b1 = desc1 + static_cast<uint64_t>((s * SL::kPB) >> 4);
+        const uint64_t b2 = desc2 + static_cast<uint64_t>((s * SL::kPB) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8f6f4_ts(dcol, acol + kk * 8, b1 + 2 * kk, idesc, kk != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_f8f6f4_ts(dcol, acol + kk * 8, b2 + 2 * kk, idesc, true);
+        mma_commit(&empty[s]);
+        mma_commit(&mdone[d]);
+        last = u;
+      }
+      // this issuer's MMAs are complete before the CTA tears down
+      if (last >= 0) mbar_wait(&mdone[last % kNDS], (last / kNDS) & 1, err);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ fold
     const int fq = warp & 3;                // TMEM lane quarter
-    const int hc = (warp - kDecW) >> 2;     // token half of the tile
+    const int hc = (warp - kDecW) >> 2;     // token block of the tile
     const int r = fq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
-    float acc[64];
+    float acc[kFC];
 #pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-    int u = 0;
+    for (int j = 0; j < kFC; ++j) acc[j] = 0.f;
+    int d = 0;
+    uint32_t dph = 0;
     bool ok = true;
     for (int m = 0; m < ntiles && ok; ++m) {
       const int tile = blockIdx.x + m * gridDim.x;
@@ -253,41 +273,72 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const int n = rb * kRowsS + r;
       const uint16_t* srow = scales + static_cast<size_t>(n < N ? n : 0) * G;
       float snext = n < N ? __half2float(__ushort_as_half(srow[0])) : 0.f;
-      for (int g = 0; g < G; ++g, ++u) {
-        const int d = u % kNDS;
+      for (int g = 0; g < G; ++g) {
         const float sg = 8.0f * snext;  // D holds acc / 8
         if (g + 1 < G) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (u / kNDS) & 1, err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], dph, err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t dv[64];
-        const uint32_t col = tbase + lane_off + SL::kDCol + d * kTokS + hc * 64;
-        tmem_ld32(col, dv);
-        tmem_ld32(col + 32, dv + 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&dfree[d]);
+        // 32 columns at a time: load, wait, fold (the slot is released after
+        // the last load has completed)
+        const uint32_t col = tbase + lane_off + SL::kDCol + d * kTokS + hc * kFC;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = fmaf(sg, __uint_as_float(dv[j]), acc[j]);
+        for (int c = 0; c < kFC / 32; ++c) {
+          uint32_t dv[32];
+          tmem_ld32(col + 32 * c, dv);
+          tmem_wait_ld();
+          if (c == kFC / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dfree[d]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            acc[32 * c + j] = fmaf(sg, __uint_as_float(dv[j]), acc[32 * c + j]);
+        }
+        if (++d == kNDS) {
+          d = 0;
+          dph ^= 1;
+        }
       }
       if (!ok) break;
       // end of the tile: y[t][n] = xs[t] * acc
       const int xb = m & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&xsfull[xb], (m >> 1) & 1, err))) break;
-      const float* xst = xs_tile + xb * kTokS + hc * 64;
-      const int t0 = tb * kTokS + hc * 64;
+      const float* xst = xs_tile + xb * kTokS + hc * kFC;
+      const int t0 = tb * kTokS + hc * kFC;
+      if (y_tma) {
+        // stage the warp's kFC x 32 block and store it asynchronously: the
+        // next tile's groups overlap the write-back
+        float* stg = reinterpret_cast<float*>(smem + SL::kYOff + (warp - kDecW) * SL::kYB);
+        if (lane == 0) bulk_wait_group_read0();  // the warp's previous block was read out
+        __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int t = t0 + j;
-        if (n < N && t < T) y[static_cast<size_t>(t) * N + n] = xst[j] * acc[j];
-        acc[j] = 0.f;
+        for (int j = 0; j < kFC; ++j) {
+          stg[j * 32 + lane] = xst[j] * acc[j];
+          acc[j] = 0.f;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        // a box that starts inside the tensor (the rest is clipped)
+        if (lane == 0 && rb * kRowsS + fq * 32 < N && t0 < T) {
+          tma_store_2d(&tmY, stg, rb * kRowsS + fq * 32, t0);
+          bulk_commit_group();
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kFC; ++j) {
+          const int t = t0 + j;
+          if (n < N && t < T) y[static_cast<size_t>(t) * N + n] = xst[j] * acc[j];
+          acc[j] = 0.f;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xsfree[xb]);
     }
+    if (lane == 0) bulk_wait_group0();  // output blocks written before the CTA exits
   }
 
   tc_fence_before();
@@ -306,13 +357,16 @@ cudaError_t s8_set_attributes() {
 }
 
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
-                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
-                      int num_sms, int* err, cudaStream_t stream) {
+                      const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
+                      float* y, int T, int K, int N, int num_sms, int* err, cudaStream_t stream) {
   const long long tiles = static_cast<long long>((N + kRowsS - 1) / kRowsS) *
                           ((T + kTokS - 1) / kTokS);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  s8tc_kernel<<<grid, kThreadsS, SL::kAlloc, stream>>>(*tmW, *tmP1, *tmP2, scales, x_scale, y, T,
-                                                       K, N, err);
+  // without a y tensor map (N % 4 != 0: rows not 16-byte strided) the fold
+  // warps store y directly; the map argument is then an unused copy
+  s8tc_kernel<<<grid, kThreadsS, SL::kAlloc, stream>>>(*tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW,
+                                                       scales, x_scale, y, T, K, N,
+                                                       tmY ? 1 : 0, err);
   return cudaGetLastError();
 }
 
