@@ -113,6 +113,27 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, i
   }
 }
 
+// mbar_wait with a non-blocking first probe: an already-complete phase costs
+// one test_wait (a try_wait issued right behind tcgen05 commits is slow to
+// return even then); an open phase is waited on with try_wait, which lets the
+// thread yield instead of flooding the barrier with probes.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, err);
+}
+
+// Warp-wide wait with a single polling lane: lane 0 waits, the result is
+// broadcast, and __syncwarp orders the other lanes' later accesses after
+// lane 0's acquire.  Keeps barrier traffic to one thread per waiting warp.
+// Every lane of the warp must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 // Wait until *ctr >= target (acquire, GPU scope).  Gives up after
 // kWaitLimitNs: ORs kErrTimeout into *err and returns false.
 __device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* ctr,
