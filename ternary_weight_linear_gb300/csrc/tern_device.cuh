@@ -134,6 +134,31 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   return ok != 0;
 }
 
+// Publish / observe a sequence number in shared memory with release /
+// acquire semantics at CTA scope (a hand-off between two threads that needs
+// no mbarrier operation on the observing side).
+__device__ __forceinline__ void seq_publish(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t seq_read(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+// Spin until *p >= target.  Gives up after kWaitLimitNs: ORs kErrTimeout into
+// *err and returns false.
+__device__ __forceinline__ bool seq_wait(const uint32_t* p, uint32_t target, int* err) {
+  if (seq_read(p) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (seq_read(p) >= target) return true;
+    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // Wait until *ctr >= target (acquire, GPU scope).  Gives up after
 // kWaitLimitNs: ORs kErrTimeout into *err and returns false.
 __device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* ctr,

@@ -34,17 +34,17 @@
 //    into their row's running sums with s[n][g] * f[g][token].
 //
 // Pipeline (one CTA per SM, persistent; TMEM 512 columns):
-//   warp 12    producer: one 2D TMA box of packed weights (128 rows x 128 B,
+//   warp 16    producer: one 2D TMA box of packed weights (128 rows x 128 B,
 //              128-byte swizzle) per stage into the weight ring (plus, for
 //              T > 1, a bulk copy of the stage's activation block); the
 //              stage's fp16 scales (cp.async) into a longer scale ring;
-//   warps 15-18 (T = 1) build the resident activation blocks and factors;
+//   warps 19-22 (T = 1) build the resident activation blocks and factors;
 //   warps 0-7  decode (two groups of 32 rows per warp) into A slots;
-//   warps 13-14 issue the MMAs of half-stage 0 / 1 of every stage once its
-//              A slot is full and its D slot has been drained (warp 13 also
+//   warps 17-18 issue the MMAs of half-stage 0 / 1 of every stage once its
+//              A slot is full and its D slot has been drained (warp 17 also
 //              allocates TMEM);
-//   warps 8-11 fold D slots into per-row running sums (one row per thread)
-//              and write y at the end of each row block.
+//   warps 8-15 fold D slots into per-row running sums (two threads per row,
+//              one per half-stage) and write y at the end of each row block.
 //
 // Work split: the (row block, 512-wide k stage) units are cut into equal
 // contiguous ranges, one per CTA, so every SM streams the same bytes.  A row
@@ -81,7 +81,9 @@ namespace {
 
 constexpr int kRows = 128;       // rows per CTA row block (MMA M, TMEM lanes)
 constexpr int kDecWarps = 8;     // two decode threads per row (groups split in halves)
-constexpr int kFoldWarps = 4;    // one fold thread per row
+// Two fold threads per row: fold warp f owns TMEM lane quarter f % 4 and
+// half-stage f / 4 (groups 2 (f / 4), 2 (f / 4) + 1) of every stage.
+constexpr int kFoldWarps = 8;
 constexpr int kProducerWarp = kDecWarps + kFoldWarps;
 // Two MMA-issuing warps: the first issues half-stage 0 of every stage, the
 // second half-stage 1, so a single issuing thread never paces the tensor pipe.
@@ -129,10 +131,11 @@ struct TC {
   static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) f[stage][4]
   static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * 16 : 0);
   static constexpr int kNumBars =
-      2 * kStages + 2 * kSStages + 2 * kNAH + 2 * kNDH + (kInKernelX ? kX1MaxStages : 0);
+      2 * kStages + 2 * kSStages + 2 * kNAH + 2 * kNDH + 8 + (kInKernelX ? kX1MaxStages : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kFirstOff = kTmemSlot + 16;  // fold: parked first row block sums
-  static constexpr int kX1Off = (kFirstOff + TT * kRows * 4 + 127) / 128 * 128;  // (T = 1)
+  static constexpr int kPartOff = kFirstOff + TT * kRows * 4;  // fold: half-stage 1 sums
+  static constexpr int kX1Off = (kPartOff + TT * kRows * 4 + 127) / 128 * 128;  // (T = 1)
   // shared memory for K: fixed part, the T = 1 blocks, alignment slack
   static constexpr int smem_bytes(int KS) {
     return kX1Off + (kInKernelX ? KS * kX1Stage : 0) + 1024;
@@ -259,6 +262,10 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   uint64_t* mdone = afree + NA;   // MMAs writing D slot d completed
   uint64_t* dfree = mdone + ND;   // D slot d read back by the fold warps
   uint64_t* xready = dfree + ND;  // (T = 1) activation block of stage ks built
+  // fold pairs: [quarter] the half-stage-1 warp's row block sums are in
+  // shared memory / have been taken by the half-stage-0 warp
+  uint64_t* pfull = xready + (C::kInKernelX ? kX1MaxStages : 0);
+  uint64_t* pfree = pfull + 4;
   uint8_t* xres = smem + C::kX1Off;                              // (T = 1) blocks
   float* ftab = reinterpret_cast<float*>(smem + C::kFOff);       // (T = 1) f[ks][4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
@@ -270,8 +277,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);  // producer's expect_tx arrival
-      // the decoders (+ both MMA warps' commits when the stage holds activations)
-      mbar_init(&empty[s], C::kInKernelX ? kDecWarps : kDecWarps + kMmaWarps);
+      // the decoders (+ one MMA commit per half-stage when the stage holds
+      // activations)
+      mbar_init(&empty[s], C::kInKernelX ? kDecWarps : kDecWarps + 2);
     }
     for (int s = 0; s < SS; ++s) {
       mbar_init(&sfull[s], 32);
@@ -283,10 +291,14 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
     for (int d = 0; d < ND; ++d) {
       mbar_init(&mdone[d], 1);
-      mbar_init(&dfree[d], kFoldWarps);
+      mbar_init(&dfree[d], kFoldWarps / 2);  // the four warps of its half-stage
     }
     if constexpr (C::kInKernelX)
       for (int k = 0; k < KS; ++k) mbar_init(&xready[k], C::kXWarps);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&pfull[q], 1);
+      mbar_init(&pfree[q], 1);
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -486,7 +498,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // warp-uniform; one elected lane issues.  Half-stage hu = 2 it + hh
     // (groups 2 hh, 2 hh + 1) uses A slot hu % NA and D slot hu % ND and is
     // issued by MMA warp hh.
-    const int hh = warp - kMmaWarp;
+    const int w = warp - kMmaWarp;
     const bool leader = elect_one();
     constexpr uint32_t idesc = idesc_e4m3_f32(kRows, NC);
     // Descriptor of stage 0's B block; a stage / k chunk only moves the start
@@ -495,11 +507,11 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         C::kInKernelX ? smem_desc_kmajor(smem_addr(xres), kX1Lbo, kX1Sbo)
                       : smem_desc_kmajor(smem_addr(smem + C::kXOff), kXLbo, kXSbo);
     constexpr uint32_t kLbo = C::kInKernelX ? kX1Lbo : kXLbo;
-    int it = 0;
-    int ks = ks0;
-    bool ok = true;
-    for (; it < nunits && ok; ++it) {
+    int last = -1;
+    for (int hu = w; hu < 2 * nunits; hu += kMmaWarps) {
+      const int it = hu >> 1, hh = hu & 1;
       const int s = it % S;
+      const int ks = static_cast<int>((ks0 + it) % KS);
       const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
       const uint64_t dstage =
           desc0 + static_cast<uint64_t>(
@@ -507,44 +519,36 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if constexpr (C::kInKernelX) {
         if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
       }
-      {
-        const int hu = 2 * it + hh;
-        const int a = hu % NA;
-        const int d = hu % ND;
-        if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (hu / NA) & 1, err)) ||
-            (hu >= ND &&
-             !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err)))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t dcol = tbase + C::kDCol + d * 2 * NC;
-        const uint32_t acol = tbase + C::kACol + a * 64;
-        if (leader) {
+      const int a = hu % NA;
+      const int d = hu % ND;
+      if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (hu / NA) & 1, err)) ||
+          (hu >= ND &&
+           !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err))))
+        break;
+      tc_fence_after();
+      const uint32_t dcol = tbase + C::kDCol + d * 2 * NC;
+      const uint32_t acol = tbase + C::kACol + a * 64;
+      if (leader) {
 #pragma unroll
-          for (int gg = 0; gg < 2; ++gg) {
-            const int g = 2 * hh + gg;
-            if (g < ng) {
+        for (int gg = 0; gg < 2; ++gg) {
+          const int g = 2 * hh + gg;
+          if (g < ng) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
-                              dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
-                              idesc, kk > 0);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
+                            dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
+                            idesc, kk > 0);
           }
-          if (!C::kInKernelX) mma_commit(&empty[s]);
-          mma_commit(&afree[a]);
-          mma_commit(&mdone[d]);
         }
-        __syncwarp();
+        if (!C::kInKernelX) mma_commit(&empty[s]);
+        mma_commit(&afree[a]);
+        mma_commit(&mdone[d]);
       }
-      if (++ks == KS) ks = 0;
+      __syncwarp();
+      last = hu;
     }
     // Before TMEM is released, this warp's last MMAs must have completed.
-    if (it > 0) {
-      const int hu = 2 * (it - 1) + hh;
-      mbar_wait(&mdone[hu % ND], (hu / ND) & 1, err);
-    }
+    if (last >= 0) mbar_wait(&mdone[last % ND], (last / ND) & 1, err);
   } else if (warp < kDecWarps) {
     // ------------------------------------------------------------ decode
     // Warp w owns TMEM lane quarter q = w % 4 (rows 32 q .. 32 q + 31) and the
@@ -593,10 +597,13 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ fold
-    // Fold warp f owns TMEM lane quarter f (rows 32 f .. 32 f + 31) and all
-    // four groups of every stage: y[t][row] += s[row][g] * f[g][t] *
-    // (D[g][piece 0, t] + D[g][piece 1, t]).
-    const int fq = warp - kDecWarps;  // == warp % 4
+    // Fold warp f owns TMEM lane quarter fq = f % 4 (rows 32 fq .. 32 fq + 31)
+    // and half-stage fh = f / 4 (groups 2 fh, 2 fh + 1) of every stage:
+    // y[t][row] += s[row][g] * f[g][t] * (D[g][piece 0, t] + D[g][piece 1, t]).
+    // At the end of a row block the fh = 1 warp hands its sums to the fh = 0
+    // warp of the same quarter, which writes y.
+    const int fq = (warp - kDecWarps) & 3;  // == warp % 4
+    const int fh = (warp - kDecWarps) >> 2;
     const int r = fq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
     float yacc[TT];
@@ -606,16 +613,18 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // Row blocks split between CTAs are summed with fp32 atomics into y.
     // Every CTA first zeroes the y rows of its split row blocks, then adds to
     // the launch-arrival counter; a CTA adds into y only once the counter
-    // shows that every fold warp of the launch has done its zeroing.  Each
-    // launch adds exactly 1024 in total, so the counter is a multiple of 1024
-    // between launches and needs no reset.
+    // shows that every writing fold warp of the launch has done its zeroing.
+    // Each launch adds exactly 1024 in total, so the counter is a multiple of
+    // 1024 between launches and needs no reset.  (Only the fh = 0 warps write
+    // y, zero and count.)
     auto is_split = [&](int rb) {
       const long long u = static_cast<long long>(rb) * KS;
       return owner_of(u, U, P) != owner_of(u + KS - 1, U, P);
     };
     grid_dependency_wait();  // y and the workspace may be in use by earlier work
     const int rb_last = static_cast<int>((end - 1) / KS);
-    {
+    unsigned long long arrival_target = 0;
+    if (fh == 0) {
       const int zr[2] = {rb0, rb_last};
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -624,16 +633,16 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         if (n < N)
           for (int t = 0; t < Tt; ++t) y[static_cast<size_t>(tok0 + t) * N + n] = 0.f;
       }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        const unsigned long long add =
+            (cta == 0 && fq == 0) ? 1024ull - 4ull * static_cast<unsigned long long>(P) + 1ull
+                                  : 1ull;
+        arrival_target = (atomicAdd(arrivals, add) & ~1023ull) + 1024ull;
+      }
+      arrival_target = __shfl_sync(0xffffffffu, arrival_target, 0);
     }
-    __threadfence();
-    __syncwarp();
-    unsigned long long arrival_target = 0;
-    if (lane == 0) {
-      const unsigned long long add =
-          (cta == 0 && fq == 0) ? 1024ull - 4ull * static_cast<unsigned long long>(P) + 1ull : 1ull;
-      arrival_target = (atomicAdd(arrivals, add) & ~1023ull) + 1024ull;
-    }
-    arrival_target = __shfl_sync(0xffffffffu, arrival_target, 0);
 
     // A split row block's sums are added into y only after the arrival
     // counter shows every CTA has zeroed; so that the fold never stalls on
@@ -641,37 +650,59 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // shared memory and all atomics are issued once this CTA's last unit is
     // folded.
     float* first_part = reinterpret_cast<float*>(smem + C::kFirstOff);  // [TT][128]
+    float* half_part = reinterpret_cast<float*>(smem + C::kPartOff);    // [TT][128]
     bool first_parked = false;
-    auto flush = [&](int rb) {
+    int nflush = 0;
+    // false: a bounded wait gave up (the error word is set)
+    auto flush = [&](int rb) -> bool {
       const int n = rb * kRows + r;
-      if (!is_split(rb)) {
+      if (fh == 1) {
+        // hand the sums over once the previous hand-over has been taken
+        if (nflush > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&pfree[fq], (nflush - 1) & 1, err)))
+          return false;
 #pragma unroll
-        for (int t = 0; t < TT; ++t)
-          if (n < N && t < Tt) y[static_cast<size_t>(tok0 + t) * N + n] = yacc[t];
-      } else if (rb == rb0 && rb != rb_last) {
-#pragma unroll
-        for (int t = 0; t < TT; ++t) first_part[t * kRows + r] = yacc[t];
-        first_parked = true;
+        for (int t = 0; t < TT; ++t) half_part[t * kRows + r] = yacc[t];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[fq]);
       } else {
-        bool fine = true;
-        if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
-        fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
-        if (fine) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pfull[fq], nflush & 1, err))) return false;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) yacc[t] += half_part[t * kRows + r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfree[fq]);
+        if (!is_split(rb)) {
 #pragma unroll
           for (int t = 0; t < TT; ++t)
-            if (n < N && t < Tt) atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n], yacc[t]);
-          if (first_parked) {
-            const int n0 = rb0 * kRows + r;
+            if (n < N && t < Tt) y[static_cast<size_t>(tok0 + t) * N + n] = yacc[t];
+        } else if (rb == rb0 && rb != rb_last) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) first_part[t * kRows + r] = yacc[t];
+          first_parked = true;
+        } else {
+          bool fine = true;
+          if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
+          fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
+          if (fine) {
 #pragma unroll
             for (int t = 0; t < TT; ++t)
-              if (n0 < N && t < Tt)
-                atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0], first_part[t * kRows + r]);
-            first_parked = false;
+              if (n < N && t < Tt) atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n], yacc[t]);
+            if (first_parked) {
+              const int n0 = rb0 * kRows + r;
+#pragma unroll
+              for (int t = 0; t < TT; ++t)
+                if (n0 < N && t < Tt)
+                  atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0],
+                            first_part[t * kRows + r]);
+              first_parked = false;
+            }
           }
         }
       }
+      ++nflush;
 #pragma unroll
       for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
+      return true;
     };
 
     int ks = ks0;
@@ -682,6 +713,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
       const uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
       const uint2 sw = lds_v2(sst + r * 8);
+      const uint32_t s2 = fh ? sw.y : sw.x;  // this half-stage's two fp16 scales
       // f[g][t] at fv[g * FH + t]
       constexpr int FH = C::kInKernelX ? 1 : H;
       const float* fv = C::kInKernelX ? ftab + ks * 4
@@ -689,23 +721,46 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if constexpr (C::kInKernelX) {
         if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
       }
+      const int hu = 2 * j + fh;
+      const int d = hu % ND;
+      if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) break;
+      tc_fence_after();
+      const uint32_t dbase = tbase + lane_off + C::kDCol + d * 2 * NC;
+      // only the accumulator columns that carry tokens are read back:
+      // piece 0 of token t is column t, piece 1 is H + t
+      auto fold_group = [&](int gg, const uint32_t* dv) {
+        const float sg = __half2float(__ushort_as_half(
+            static_cast<unsigned short>(gg ? (s2 >> 16) : (s2 & 0xFFFFu))));
+        const int g = 2 * fh + gg;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int hu = 2 * j + hh;
-        const int d = hu % ND;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) {
-          ok = false;
-          break;
+        for (int t = 0; t < TT; ++t)
+          yacc[t] = fmaf(sg * fv[g * FH + t], __uint_as_float(dv[t]) + __uint_as_float(dv[H + t]),
+                         yacc[t]);
+      };
+      static_assert(NC == 16 || NC == 32, "accumulator width");
+      if constexpr (NC == 32) {
+        // 16 tokens: one group at a time keeps the live registers down
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          uint32_t dv[NC];
+          const bool has = 2 * fh + gg < ng;
+          if (has) {
+            tmem_ld16(dbase + gg * NC, dv);
+            tmem_ld16(dbase + gg * NC + 16, dv + 16);
+          }
+          tmem_wait_ld();
+          if (gg == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dfree[d]);
+          }
+          if (has) fold_group(gg, dv);
         }
-        tc_fence_after();
-        const uint32_t dbase = tbase + lane_off + C::kDCol + d * 2 * NC;
-        // only the accumulator columns that carry tokens are read back:
-        // piece 0 of token t is column t, piece 1 is H + t
+      } else {
         uint32_t dv[2][NC];
 #pragma unroll
         for (int gg = 0; gg < 2; ++gg) {
-          const int g = 2 * hh + gg;
-          if (g < ng) {
+          if (2 * fh + gg < ng) {
             const uint32_t col = dbase + gg * NC;
             if constexpr (TT == 1) {
               tmem_ld1(col, dv[gg][0]);
@@ -714,8 +769,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
               tmem_ld4(col, dv[gg]);
               tmem_ld4(col + H, dv[gg] + H);
             } else {
-              tmem_ld16(col, dv[gg]);
-              if constexpr (NC == 32) tmem_ld16(col + 16, dv[gg] + 16);
+              tmem_ld16(col, dv[gg]);  // 8 tokens: both pieces, columns 0 .. 15
             }
           }
         }
@@ -724,31 +778,19 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&dfree[d]);
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const int g = 2 * hh + gg;
-          if (g < ng) {
-            const uint32_t s2 = hh ? sw.y : sw.x;
-            const float sg = __half2float(__ushort_as_half(
-                static_cast<unsigned short>(gg ? (s2 >> 16) : (s2 & 0xFFFFu))));
-#pragma unroll
-            for (int t = 0; t < TT; ++t)
-              yacc[t] = fmaf(sg * fv[g * FH + t],
-                             __uint_as_float(dv[gg][t]) + __uint_as_float(dv[gg][H + t]),
-                             yacc[t]);
-          }
-        }
+        for (int gg = 0; gg < 2; ++gg)
+          if (2 * fh + gg < ng) fold_group(gg, dv[gg]);
       }
-      if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[ss]);
       if (++ks == KS) {
-        flush(static_cast<int>((begin + j) / KS));
+        ok = flush(static_cast<int>((begin + j) / KS));
         ks = 0;
       }
     }
     // a row block whose last stage lies beyond this CTA's range
-    if (ok && ks != 0) flush(rb_last);
-    if (ok && first_parked) {
+    if (ok && ks != 0) ok = flush(rb_last);
+    if (ok && fh == 0 && first_parked) {
       // the last row block was whole: add the parked first one now
       bool fine = true;
       if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
