@@ -38,6 +38,9 @@ sys.path.insert(0, ROOT)
 
 GU = (5120, 2 * 17408)
 DN = (17408, 5120)
+AI = (5120, 6144)   # attention-like in
+AO = (6144, 5120)   # attention-like out
+STACK_LAYERS = 64
 GROUP = 128
 
 
@@ -60,6 +63,8 @@ def parse_args():
     ap.add_argument("--profile", choices=["gu", "dn", "s8gu", "s8dn"], default=None,
                     help="only call tern_linear on one projection at T=1 (for profilers)")
     ap.add_argument("--profile-calls", type=int, default=3)
+    ap.add_argument("--no-stack", action="store_true",
+                    help="skip the 64-layer whole-stack passes")
     return ap.parse_args()
 
 
@@ -170,6 +175,66 @@ def make_x(torch, T, K, gen, dev):
     ch = torch.randperm(K, generator=gen, device=dev)[: max(1, round(0.01 * K))]
     x[:, ch] *= 20.0
     return x.bfloat16()
+
+
+def run_stack(tl, torch, gen, dev, peaks, stream):
+    """The whole-stack family: STACK_LAYERS resident layers of (gate+up, down,
+    attention-like in and out), one full pass at T = 1, 4 and 2048, each pass
+    captured as a CUDA graph and replayed.  Weights at P(0) = 0.4; the kernels
+    read zeros like any other code, so the rate does not depend on P(0)."""
+    shapes = (GU, DN, AI, AO)
+    layers = [[make_layer(tl, torch, K, N, gen, dev) for (K, N) in shapes]
+              for _ in range(STACK_LAYERS)]
+    wbytes = STACK_LAYERS * sum(weight_bytes(K, N) for K, N in shapes)
+    res = {"layers": STACK_LAYERS,
+           "projections": "gate+up 5120x34816, down 17408x5120, attn-in 5120x6144, attn-out 6144x5120",
+           "weight_bytes": wbytes, "p_zero": 0.4}
+    for T in (1, 4, 2048):
+        xs = {K: make_x(torch, T, K, gen, dev) for K in sorted({k for k, _ in shapes})}
+        ys = {sh: torch.empty(T, sh[1], device=dev) for sh in shapes}
+        ws = torch.zeros(max(tl.tern_linear_workspace_bytes(T, K, N) for K, N in shapes),
+                         dtype=torch.uint8, device=dev)
+        stream.wait_stream(torch.cuda.current_stream())
+
+        def one_pass():
+            for lay in layers:
+                for sh, (Wp, sc) in zip(shapes, lay):
+                    tl.tern_linear(Wp, sc, xs[sh[0]], ys[sh], ws)
+
+        with torch.cuda.stream(stream):
+            one_pass()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                one_pass()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = 20 if T < 2048 else 3
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        if T < 2048:
+            gbs = wbytes / (ms * 1e-3) / 1e9
+            res[f"t{T}"] = {"ms_per_pass": round(ms, 4), "GB/s": round(gbs, 1),
+                            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+        else:
+            ops = 2.0 * T * STACK_LAYERS * sum(K * N for K, N in shapes)
+            tops = ops / (ms * 1e-3) / 1e12
+            res[f"t{T}"] = {"ms_per_pass": round(ms, 3), "TOPS": round(tops, 1),
+                            "frac_of_bf16_peak": round(tops / peaks.get("bf16_tflops", 1900.0), 4)}
+        del g, xs, ys, ws
+    if tl.tern_device_status() != 0:
+        raise RuntimeError("device error word set in the stack passes")
+    del layers
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world, local):
@@ -307,6 +372,9 @@ def run_ours(args, rank, world, local):
                        "unit": "TOPS", "frac": round(s8_tops / peaks.get("bf16_tflops", 1900.0), 4),
                        "traffic": None}}
 
+    # ---- whole-stack family (64 resident layers) at T = 1, 4, 2048
+    stack = run_stack(tl, torch, gen, dev, peaks, stream) if not args.no_stack else None
+
     # ---- end to end through the C ABI with host buffers
     import numpy as np
     xh_gu = x_gu.cpu().pin_memory()
@@ -350,6 +418,7 @@ def run_ours(args, rank, world, local):
         "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": roofline,
         "s8_t2048": s8,
+        "stack_c4": stack,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "path": "pinned host x -> device copy, tern_linear via the C ABI (eager), y -> pinned host"},

@@ -278,6 +278,43 @@ def test_prefill_config_sampled(tl, proj, T):
     assert _check_case(tl, synth.config_prefill(proj, T), full=False) == "s8"
 
 
+@pytest.mark.parametrize("p_zero", synth.STACK_P_ZERO)
+@pytest.mark.parametrize("seed", synth.STACK_SEEDS)
+def test_stack_sweep_sampled(tl, p_zero, seed):
+    """The layer-stack family: every projection of a layer with P(0) in
+    {0.2, 0.4, 0.6} and seeds 1-3, each layer's weights packed once and run at
+    T = 1 (gemv), 4 (small_t) and 2048 (s8), checked on sampled outputs."""
+    import torch
+    for proj in synth.STACK_PROJ:
+        base = synth.case(proj, 1, seed=seed, p_zero=p_zero, outliers=True)
+        K, N = base.K, base.N
+        wp_ref, bad = oracle.pack(base.W)
+        assert bad == 0
+        Wd, sd, _ = to_device(base)
+        Wp = tl.tern_pack(Wd)
+        del Wd
+        assert np.array_equal(packed_to_numpy(Wp), wp_ref), f"{proj}: tern_pack differs"
+        for T, want in ((1, "gemv"), (4, "small_t"), (2048, "s8")):
+            xb = synth.activations(T, K, seed, outlier_frac=0.01 if T != 4 else 0.0)
+            xd = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+            y = tl.tern_linear(Wp, sd, xd)
+            ran = tl.tern_last_rung()
+            torch.cuda.synchronize()
+            assert tl.tern_device_status() == 0
+            assert ran == want
+            y = y.cpu().numpy()
+            ti, ni = sample_indices(T, N, 2048, seed=K + T)
+            what = f"{proj} p0={p_zero} seed={seed} T={T}"
+            if ran == "s8":
+                q_ref, xs_ref = oracle.quant_s8(xb, T, K)
+                y_ref, m, _ = oracle.linear_s8_sampled(wp_ref, base.scales, q_ref, xs_ref, K, N,
+                                                       ti, ni)
+                assert_s8_parity(y[ti, ni], y_ref, m, what)
+            else:
+                y_ref, m = oracle.linear_f64_sampled(wp_ref, base.scales, xb, K, N, ti, ni)
+                assert_bf16_parity(y[ti, ni], y_ref, m, what)
+
+
 # ---------------------------------------------------------------- probe
 
 def test_debug_probe_reports_each_rung(tl):
