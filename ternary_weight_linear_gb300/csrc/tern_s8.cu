@@ -55,6 +55,11 @@ constexpr int kMmaW = kProdW + 1;  // first of kMmaWarps issuers
 // pipe idle; two issuers take alternate groups and cover each other's gaps.
 constexpr int kMmaWarps = 2;
 constexpr int kThreadsS = (kMmaW + kMmaWarps) * 32;
+// An issuer's previous group (u - kMmaWarps) waited for the fold of group
+// u - kMmaWarps - kNDS, so when it checks the D slot for group u the slot's
+// barrier is at most one phase behind, as a parity wait requires, only while
+// kMmaWarps <= kNDS.
+static_assert(kMmaWarps <= kNDS, "issuers may outrun the accumulator ring's parity check");
 
 struct SL {
   static constexpr int kPB = kTokS * 128;   // one piece block of a group (16 KB)
@@ -66,7 +71,7 @@ struct SL {
   static constexpr int kYOff = kWOff + kStagesS * kWB;
   static constexpr int kXsOff = kYOff + kFoldW * kYB;  // x_scale of 2 tiles
   static constexpr int kBarOff = kXsOff + 2 * kTokS * 4;
-  static constexpr int kNumBars = 3 * kStagesS + 2 * kNDS + 4;
+  static constexpr int kNumBars = 3 * kStagesS + 2 * kNDS + 4 + kMmaWarps;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   uint64_t* dfree = mdone + kNDS;      // D slot read back
   uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
   uint64_t* xsfree = xsfull + 2;       // [2] ... and used
+  uint64_t* mfin = xsfree + 2;         // [issuer] all of that issuer's MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
   const float* xs_tile = reinterpret_cast<const float*>(smem + SL::kXsOff);
 
@@ -128,6 +134,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       mbar_init(&xsfull[b], 1);
       mbar_init(&xsfree[b], kFoldW);
     }
+    for (int w = 0; w < kMmaWarps; ++w) mbar_init(&mfin[w], 1);
     fence_mbar_init();
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmP1);
@@ -226,7 +233,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const uint64_t desc1 = smem_desc_sw128(smem_addr(smem + SL::kP1Off));
       const uint64_t desc2 = smem_desc_sw128(smem_addr(smem + SL::kP2Off));
       int u = warp - kMmaW;
-      int last = -1;
       for (; u < units; u += kMmaWarps) {
         const int s = u % kStagesS, d = u % kNDS;
         const uint32_t ph = (u / kStagesS) & 1, dph = (u / kNDS) & 1;
@@ -249,10 +255,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         for (int kk = 0; kk < 4; ++kk) mma_f8f6f4_ts(dcol, acol + kk * 8, b2 + 2 * kk, idesc, true);
         mma_commit(&empty[s]);
         mma_commit(&mdone[d]);
-        last = u;
       }
-      // this issuer's MMAs are complete before the CTA tears down
-      if (last >= 0) mbar_wait(&mdone[last % kNDS], (last / kNDS) & 1, err);
+      // This issuer's MMAs are complete before the CTA tears down.  (Its own
+      // barrier: a D slot's barrier may have moved on by two phases when
+      // another issuer's later group reused the slot.)
+      mma_commit(&mfin[warp - kMmaW]);
+      mbar_wait(&mfin[warp - kMmaW], 0, err);
     }
     __syncwarp();
   } else {

@@ -547,7 +547,10 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       __syncwarp();
       last = hu;
     }
-    // Before TMEM is released, this warp's last MMAs must have completed.
+    // Before TMEM is released, this warp's last MMAs must have completed.  The
+    // D slot's barrier is still at that phase: with two issuers no later
+    // half-stage reuses the slot.
+    static_assert(kMmaWarps == 2 && ND > 2, "the last-slot wait needs two issuers");
     if (last >= 0) mbar_wait(&mdone[last % ND], (last / ND) & 1, err);
   } else if (warp < kDecWarps) {
     // ------------------------------------------------------------ decode
