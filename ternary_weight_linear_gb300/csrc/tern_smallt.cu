@@ -114,8 +114,15 @@ struct TC {
   static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
   // TMEM is used in half-stage slots (256 k: two groups): A slots of 64
   // columns (256 k of e4m3), D slots of 2 x kNC columns (two groups).
-  static constexpr int kNAH = TT <= 8 ? 5 : 4;
+  // Both ring lengths are even: half-stage hu uses slot hu % n, so every
+  // slot only ever holds half-stages of one parity, which one decode half,
+  // one MMA issuer and one fold half own.  A barrier a waiter checks is then
+  // never two phases behind it (with an odd length the slot alternates
+  // between the halves, and an issuer could pass a parity check while the
+  // other decode half was still one phase back).
+  static constexpr int kNAH = 4;
   static constexpr int kNDH = TT <= 8 ? 6 : 4;
+  static_assert(kNAH % 2 == 0 && kNDH % 2 == 0, "slot rings must not mix half-stage parities");
   static constexpr int kStages = TT == 1 ? 8 : TT <= 8 ? 6 : 5;  // weight (+ activation) ring
   // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
   // ring does not wait for the MMAs, so the fold must never wait for scales).
