@@ -161,8 +161,8 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
  * activation blocks) lives in one file-scope device array of
  * TERN_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that loads
  * the library holds it until the process exits.  A call whose workspace does
- * not fit returns TERN_ENOSPACE before any device work: K <= 257536 for
- * T = 1..8 and K <= 128512 for T = 9..16.  The call allocates nothing: no
+ * not fit returns TERN_ENOSPACE before any device work: K <= 257024 for
+ * T = 1..8 and K <= 128000 for T = 9..16.  The call allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
  * Set-up.  The first call on a device (with that device current) looks up the

@@ -10,7 +10,7 @@ namespace tern {
 
 // Small-T rungs (T <= 16): k per pipeline stage.  Token tiles are TT = 1, 4,
 // 8 or 16 tokens.
-constexpr int kSTStageK = 512;  // 128 packed bytes per row
+constexpr int kSTStageK = 1024;  // 256 packed bytes per row: two 128-byte TMA boxes
 // Grid cap of the small-T kernel (one CTA per SM).
 constexpr int kSmallTMaxCtas = 160;
 // Largest K of the one-token kernel (its activation blocks stay in shared

@@ -16,7 +16,7 @@
 //    element within 2^-10 of its group's absmax; smaller ones keep an
 //    absolute error below 2^-10 * 2^-p.  The pieces are the columns of the
 //    MMA's B operand (column piece * H + token) in the tcgen05 K-major
-//    shared-memory layout, one block per 512-wide k stage, with the
+//    shared-memory layout, one block per 1024-wide k stage, with the
 //    per-(group, token) factors f = 2^(3-p).  At T = 1 four warps of the
 //    main kernel build the blocks of every stage the CTA visits once, into
 //    shared memory where they stay (a compact layout: see kX1Lbo); for wider
@@ -39,14 +39,14 @@
 //              T > 1, a bulk copy of the stage's activation block); the
 //              stage's fp16 scales (cp.async) into a longer scale ring;
 //   warps 19-22 (T = 1) build the resident activation blocks and factors;
-//   warps 0-7  decode (two groups of 32 rows per warp) into A slots;
+//   warps 0-7  decode (four groups of 32 rows per warp) into A slots;
 //   warps 17-18 issue the MMAs of half-stage 0 / 1 of every stage once its
 //              A slot is full and its D slot has been drained (warp 17 also
 //              allocates TMEM);
 //   warps 8-15 fold D slots into per-row running sums (two threads per row,
 //              one per half-stage) and write y at the end of each row block.
 //
-// Work split: the (row block, 512-wide k stage) units are cut into equal
+// Work split: the (row block, 1024-wide k stage) units are cut into equal
 // contiguous ranges, one per CTA, so every SM streams the same bytes.  A row
 // block whole inside one CTA is written to y directly.  A row block split
 // between CTAs is summed with fp32 atomics into y: at its start every CTA
@@ -56,9 +56,12 @@
 // since true).  The atomics make the order of those few additions, and so
 // the last bits of split rows, vary from run to run.
 //
-// TMEM is used in half-stage slots: the decode warps of groups 0-1 and of
-// groups 2-3 each fill their own A slot, the MMAs of a half-stage write their
-// own D slot, so decode, MMA and fold can run several half-stages apart.
+// A stage is 1024 k: two 128-byte weight boxes per row, eight groups; a
+// half-stage is one box, four groups.  TMEM is used in half-stage slots: the
+// decode warps of groups 0-3 and of groups 4-7 each fill their own A slot,
+// the MMAs of a half-stage write their own D slot, so decode, MMA and fold
+// can run half-stages apart.  (Doubling the stage from 512 k halved every
+// role's barrier hand-offs per byte, which bound the pipeline.)
 //
 // Calls chain by programmatic dependent launch: every kernel lets the next one
 // launch as soon as all of its CTAs run; the next kernel's CTAs set up, warm
@@ -90,53 +93,57 @@ constexpr int kProducerWarp = kDecWarps + kFoldWarps;
 constexpr int kMmaWarp = kProducerWarp + 1;
 constexpr int kMmaWarps = 2;
 constexpr int kXWarp0 = kMmaWarp + kMmaWarps;  // (T = 1) activation warps, one per group
+constexpr int kGS = kSTStageK / 128;       // 128-wide groups per stage
+constexpr int kGH = kGS / 2;               // groups per half-stage
+constexpr int kWBoxes = kSTStageK / 512;   // 128-byte TMA boxes per stage row
+static_assert(kGH == 4 && kWBoxes * 4 == kGS, "a half-stage is one weight box");
 constexpr uint32_t kXLbo = 128;            // K-direction core-matrix stride in the B block
-constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (512 k per stage)
+constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (one stage of k)
 // T = 1 activation block of one stage: only B columns 0 (h1) and 8 (h2) carry
 // data.  With a 16-byte K-direction stride, column r of a core matrix aliases
 // column 0 of the core matrix r steps further along K, so each piece needs a
-// single 512-byte row (plus 112 bytes of overrun): the other 14 accumulator
-// columns receive shifted dot products that are never read.
+// single row of one byte per k (plus 112 bytes of overrun): the other 14
+// accumulator columns receive shifted dot products that are never read.
 constexpr uint32_t kX1Lbo = 16;
-constexpr uint32_t kX1Sbo = 640;       // h2 row
-constexpr int kX1Stage = 1280;         // bytes per stage (h1 row, h2 row, overrun)
+constexpr uint32_t kX1Sbo = kSTStageK + 128;  // h2 row
+constexpr int kX1Stage = 2 * kX1Sbo;          // bytes per stage (h1 row, h2 row, overruns)
 constexpr int kX1MaxStages = kSmallTT1MaxK / kSTStageK;
 
 template <int TT>
 struct TC {
   static constexpr int kH = TT <= 8 ? 8 : 16;  // B columns per piece
   static constexpr int kNC = 2 * kH;           // MMA N: 16 or 32
-  static constexpr int kXFrag = kNC * kSTStageK;  // B operand of one 512-wide k stage
-  static constexpr int kXF = 4 * kH * 4;          // f[group 4][kH] fp32
+  static constexpr int kXFrag = kNC * kSTStageK;  // B operand of one k stage
+  static constexpr int kXF = kGS * kH * 4;        // f[group][kH] fp32
   static constexpr int kXBytes = kXFrag + kXF;    // one stage block of the prep buffer
   static constexpr bool kInKernelX = TT == 1;     // x blocks built by the main kernel
-  static constexpr int kXWarps = kInKernelX ? 4 : 0;
+  static constexpr int kXWarps = kInKernelX ? 4 : 0;  // two groups of every stage each
   static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
-  // TMEM is used in half-stage slots (256 k: two groups): A slots of 64
-  // columns (256 k of e4m3), D slots of 2 x kNC columns (two groups).
+  // TMEM is used in half-stage slots (kGH groups): A slots of kGH x 32
+  // columns (e4m3), D slots of kGH x kNC columns.
   // Both ring lengths are even: half-stage hu uses slot hu % n, so every
   // slot only ever holds half-stages of one parity, which one decode half,
   // one MMA issuer and one fold half own.  A barrier a waiter checks is then
   // never two phases behind it (with an odd length the slot alternates
   // between the halves, and an issuer could pass a parity check while the
   // other decode half was still one phase back).
-  static constexpr int kNAH = 4;
-  static constexpr int kNDH = TT <= 8 ? 6 : 4;
+  static constexpr int kNAH = 2;
+  static constexpr int kNDH = TT <= 8 ? 4 : 2;
   static_assert(kNAH % 2 == 0 && kNDH % 2 == 0, "slot rings must not mix half-stage parities");
-  static constexpr int kStages = TT == 1 ? 8 : TT <= 8 ? 6 : 5;  // weight (+ activation) ring
+  static constexpr int kStages = TT == 1 ? 4 : 3;  // weight (+ activation) ring
   // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
   // ring does not wait for the MMAs, so the fold must never wait for scales).
-  static constexpr int kLead = kInKernelX ? 4 : 0;
+  static constexpr int kLead = kInKernelX ? 2 : 0;
   // scale (+ factor) ring: held until folded, which trails the weight ring
   // by up to (kNAH + kNDH) / 2 stages
   static constexpr int kSStages = kStages + kLead + (kNAH + kNDH + 1) / 2;
-  static constexpr int kWBytes = kRows * 128;
-  static constexpr int kSBytes = kRows * 8 + (kInKernelX ? 0 : kXF);  // scales [128][4], f
+  static constexpr int kWBytes = kRows * kSTStageK / 4;  // kWBoxes boxes of 128 rows x 128 B
+  static constexpr int kSBytes = kRows * 2 * kGS + (kInKernelX ? 0 : kXF);  // scales [128][kGS], f
   static constexpr int kWOff = 0;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kXOff = kWOff + kStages * kWBytes;  // activation ring (T > 1)
   static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
   static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) f[stage][4]
-  static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * 16 : 0);
+  static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * kGS * 4 : 0);
   static constexpr int kNumBars =
       2 * kStages + 2 * kSStages + 2 * kNAH + 2 * kNDH + 8 + (kInKernelX ? kX1MaxStages : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
@@ -148,10 +155,12 @@ struct TC {
     return kX1Off + (kInKernelX ? KS * kX1Stage : 0) + 1024;
   }
   static constexpr int kAllocMax = smem_bytes(kInKernelX ? kX1MaxStages : 0);
-  static constexpr uint32_t kACol = 0;             // A[kNAH]: 64 columns each
-  static constexpr uint32_t kDCol = kNAH * 64;     // D[kNDH]: 2 x kNC columns each
+  static constexpr uint32_t kASlot = kGH * 32;     // A[kNAH] slots
+  static constexpr uint32_t kDSlot = kGH * kNC;    // D[kNDH] slots
+  static constexpr uint32_t kACol = 0;
+  static constexpr uint32_t kDCol = kNAH * kASlot;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kDCol + kNDH * 2 * kNC <= kTmemCols, "TMEM budget");
+  static_assert(kDCol + kNDH * kDSlot <= kTmemCols, "TMEM budget");
   static_assert(kXFrag % 16 == 0 && kXF % 16 == 0 && kXBytes % 16 == 0, "bulk copy sizes");
   static_assert(kSBytes % 16 == 0 && kBarOff % 8 == 0, "alignment");
   static_assert(kAllocMax <= 227 * 1024, "shared memory");
@@ -198,11 +207,11 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
   using C = TC<TT>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int task = blockIdx.x * 8 + warp;
-  const int groups = 4 * KS;
+  const int groups = kGS * KS;
   if (task >= C::kH * groups) return;
   const int t = task / groups;
   const int gi = task % groups;
-  const int ks = gi >> 2, jg = gi & 3;
+  const int ks = gi / kGS, jg = gi % kGS;
   const int kbase = gi * 128 + 4 * lane;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (t < Tt && kbase < K) {
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   uint64_t* pfull = xready + (C::kInKernelX ? kX1MaxStages : 0);
   uint64_t* pfree = pfull + 4;
   uint8_t* xres = smem + C::kX1Off;                              // (T = 1) blocks
-  float* ftab = reinterpret_cast<float*>(smem + C::kFOff);       // (T = 1) f[ks][4]
+  float* ftab = reinterpret_cast<float*>(smem + C::kFOff);       // (T = 1) f[ks][kGS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       mbar_init(&dfree[d], kFoldWarps / 2);  // the four warps of its half-stage
     }
     if constexpr (C::kInKernelX)
-      for (int k = 0; k < KS; ++k) mbar_init(&xready[k], C::kXWarps);
+      for (int k = 0; k < KS; ++k) mbar_init(&xready[k], kGS);  // one arrival per group
     for (int q = 0; q < 4; ++q) {
       mbar_init(&pfull[q], 1);
       mbar_init(&pfree[q], 1);
@@ -335,7 +344,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     if (lane == 0) {
       int rb = rb0, ks = ks0;
       for (int it = 0; it < nunits && it < S; ++it) {
-        tma_prefetch_2d(&tmW, ks * 128, rb * kRows);
+#pragma unroll
+        for (int b = 0; b < kWBoxes; ++b)
+          tma_prefetch_2d(&tmW, ks * (kSTStageK / 4) + 128 * b, rb * kRows);
         if (++ks == KS) {
           ks = 0;
           ++rb;
@@ -346,8 +357,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (sbytes) bulk_prefetch_l2(scales + static_cast<size_t>(rb0) * kRows * G, sbytes);
     }
     grid_dependency_wait();
-    // Scale stream: unit su's fp16 scales of groups 4 ks .. 4 ks + 3 for rows
-    // lane + 32 i (and, T > 1, its factors f), into scale ring slot su % SS.
+    // Scale stream: unit su's fp16 scales of groups kGS ks .. kGS ks + kGS - 1
+    // for rows lane + 32 i (and, T > 1, its factors f), into scale ring slot
+    // su % SS.
     int su = 0, srb = rb0, sks = ks0;
     auto issue_scales = [&]() -> bool {
       const int ss = su % SS;
@@ -358,19 +370,35 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if constexpr (!C::kInKernelX) {
         if (lane == 0) {
           mbar_expect_tx(&sfull[ss], C::kXF);
-          bulk_load(sst + kRows * 8, xprep + static_cast<size_t>(sks) * C::kXBytes + C::kXFrag,
-                    C::kXF, &sfull[ss]);
+          bulk_load(sst + kRows * 2 * kGS,
+                    xprep + static_cast<size_t>(sks) * C::kXBytes + C::kXFrag, C::kXF,
+                    &sfull[ss]);
         }
       }
-      uint2* sb = reinterpret_cast<uint2*>(sst);
-      const int g0 = sks * 4;
-      if ((G & 3) == 0) {
+      uint4* sb = reinterpret_cast<uint4*>(sst);
+      const int g0 = sks * kGS;
+      if ((G % kGS) == 0) {
+        // whole 16-byte rows of scales
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
           const int n = srb * kRows + r;
           const bool in = n < N;
-          cp_async_8(&sb[r], scales + static_cast<size_t>(in ? n : 0) * G + g0, in ? 8u : 0u);
+          cp_async_16(&sb[r], scales + static_cast<size_t>(in ? n : 0) * G + g0, in ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(&sfull[ss]);
+      } else if ((G & 3) == 0) {
+        // 8-byte halves; the second is past the row end in a short last stage
+        const bool second = g0 + 4 < G;
+#pragma unroll
+        for (int i = 0; i < kRows / 32; ++i) {
+          const int r = lane + 32 * i;
+          const int n = srb * kRows + r;
+          const bool in = n < N;
+          const uint16_t* src = scales + static_cast<size_t>(in ? n : 0) * G + g0;
+          cp_async_8(&sb[r], src, in ? 8u : 0u);
+          cp_async_8(reinterpret_cast<uint8_t*>(&sb[r]) + 8, second ? src + 4 : src,
+                     (in && second) ? 8u : 0u);
         }
         cp_async_mbar_arrive(&sfull[ss]);
       } else {
@@ -378,15 +406,16 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
           const int n = srb * kRows + r;
-          uint2 v = make_uint2(0, 0);
+          uint32_t hv[kGS];
+#pragma unroll
+          for (int j = 0; j < kGS; ++j) hv[j] = 0u;
           if (n < N) {
             const uint16_t* src = scales + static_cast<size_t>(n) * G + g0;
-            uint32_t hv[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) hv[j] = (g0 + j < G) ? src[j] : 0u;
-            v = make_uint2(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16));
+            for (int j = 0; j < kGS; ++j) hv[j] = (g0 + j < G) ? src[j] : 0u;
           }
-          sb[r] = v;
+          sb[r] = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16), hv[4] | (hv[5] << 16),
+                             hv[6] | (hv[7] << 16));
         }
         mbar_arrive(&sfull[ss]);
       }
@@ -405,15 +434,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int s = it % S;
       if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
       if (lane == 0) {
-        if constexpr (C::kInKernelX) {
-          mbar_arrive_expect_tx(&full[s], C::kWBytes);  // activations are resident
-          tma_load_2d(smem + C::kWOff + s * C::kWBytes, &tmW, ks * 128, rb * kRows, &full[s]);
-        } else {
-          mbar_arrive_expect_tx(&full[s], C::kWBytes + C::kXFrag);
-          tma_load_2d(smem + C::kWOff + s * C::kWBytes, &tmW, ks * 128, rb * kRows, &full[s]);
+        // activations are resident at T = 1; for T > 1 the stage's block comes along
+        mbar_arrive_expect_tx(&full[s], C::kWBytes + (C::kInKernelX ? 0 : C::kXFrag));
+#pragma unroll
+        for (int bx = 0; bx < kWBoxes; ++bx)
+          tma_load_2d(smem + C::kWOff + s * C::kWBytes + bx * (kRows * 128), &tmW,
+                      ks * (kSTStageK / 4) + 128 * bx, rb * kRows, &full[s]);
+        if constexpr (!C::kInKernelX)
           bulk_load(smem + C::kXOff + s * C::kXFrag,
                     xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXFrag, &full[s]);
-        }
       }
       if (su < nunits) ok = issue_scales();
       if (++ks == KS) {
@@ -428,31 +457,35 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (!mbar_wait(&sfull[d % SS], (d / SS) & 1, err)) break;
   } else if (warp >= kXWarp0) {
     // ------------------------------------------------------------ activations (T = 1)
-    // Activation warp xw builds group xw of every stage this CTA visits, in
-    // visiting order, once: lane l splits k = 128 xw + 4l .. +3 of the stage.
+    // Activation warp xw builds groups xw and xw + 4 of every stage this CTA
+    // visits, in visiting order, once: lane l splits k = 128 g + 4l .. +3 of
+    // the stage.  Item qi is group xw + 4 (qi & 1) of the (qi >> 1)-th stage.
     if constexpr (C::kInKernelX) {
       const int xw = warp - kXWarp0;
       grid_dependency_wait();
       const uint16_t* xt = x + static_cast<size_t>(tok0) * K;
       const int nq = nunits < KS ? nunits : KS;
-      // loads of the next kXLoads stages stay in flight while one is built
+      const int nitems = 2 * nq;
+      // loads of the next kXLoads items stay in flight while one is built
       constexpr int kXLoads = 8;
       uint2 raw[kXLoads];
-      auto load_stage = [&](int q) -> uint2 {
-        const int ks = (ks0 + q) % KS;
-        const int k = ks * kSTStageK + 128 * xw + 4 * lane;
-        return (q < nq && k < K) ? *reinterpret_cast<const uint2*>(xt + k) : make_uint2(0, 0);
+      auto load_item = [&](int qi) -> uint2 {
+        const int ks = (ks0 + (qi >> 1)) % KS;
+        const int k = ks * kSTStageK + 128 * (xw + 4 * (qi & 1)) + 4 * lane;
+        return (qi < nitems && k < K) ? *reinterpret_cast<const uint2*>(xt + k)
+                                      : make_uint2(0, 0);
       };
 #pragma unroll
-      for (int j = 0; j < kXLoads; ++j) raw[j] = load_stage(j);
-      for (int q0 = 0; q0 < nq; q0 += kXLoads) {
+      for (int j = 0; j < kXLoads; ++j) raw[j] = load_item(j);
+      for (int q0 = 0; q0 < nitems; q0 += kXLoads) {
 #pragma unroll
         for (int j = 0; j < kXLoads; ++j) {
-          const int q = q0 + j;
-          if (q >= nq) break;
-          const int ks = (ks0 + q) % KS;
+          const int qi = q0 + j;
+          if (qi >= nitems) break;
+          const int ks = (ks0 + (qi >> 1)) % KS;
+          const int g = xw + 4 * (qi & 1);
           const uint2 cur = raw[j];
-          raw[j] = load_stage(q + kXLoads);
+          raw[j] = load_item(qi + kXLoads);
           const float v[4] = {__uint_as_float(cur.x << 16), __uint_as_float(cur.x & 0xFFFF0000u),
                               __uint_as_float(cur.y << 16), __uint_as_float(cur.y & 0xFFFF0000u)};
           float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -485,14 +518,14 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
             h1 |= static_cast<uint32_t>(a) << (16 * hf);
             h2 |= static_cast<uint32_t>(c) << (16 * hf);
           }
-          // 16-block 8 xw + l/4, position b = l%4: value i goes to slot 4i + b
-          uint8_t* blk = xres + ks * kX1Stage + (8 * xw + (lane >> 2)) * 16 + (lane & 3);
+          // 16-block 8 g + l/4, position b = l%4: value i goes to slot 4i + b
+          uint8_t* blk = xres + ks * kX1Stage + (8 * g + (lane >> 2)) * 16 + (lane & 3);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             blk[4 * i] = static_cast<uint8_t>(h1 >> (8 * i));
             blk[kX1Sbo + 4 * i] = static_cast<uint8_t>(h2 >> (8 * i));
           }
-          if (lane == 0) ftab[ks * 4 + xw] = f;
+          if (lane == 0) ftab[ks * kGS + g] = f;
           fence_proxy_async_smem();  // the MMA reads the block through the async proxy
           __syncwarp();
           if (lane == 0) mbar_arrive(&xready[ks]);
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int it = hu >> 1, hh = hu & 1;
       const int s = it % S;
       const int ks = static_cast<int>((ks0 + it) % KS);
-      const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
+      const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
       const uint64_t dstage =
           desc0 + static_cast<uint64_t>(
                       (C::kInKernelX ? ks * kX1Stage : s * C::kXFrag) >> 4);
@@ -533,12 +566,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
            !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err))))
         break;
       tc_fence_after();
-      const uint32_t dcol = tbase + C::kDCol + d * 2 * NC;
-      const uint32_t acol = tbase + C::kACol + a * 64;
+      const uint32_t dcol = tbase + C::kDCol + d * C::kDSlot;
+      const uint32_t acol = tbase + C::kACol + a * C::kASlot;
       if (leader) {
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const int g = 2 * hh + gg;
+        for (int gg = 0; gg < kGH; ++gg) {
+          const int g = kGH * hh + gg;
           if (g < ng) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -555,14 +588,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       last = hu;
     }
     // Before TMEM is released, this warp's last MMAs must have completed.  The
-    // D slot's barrier is still at that phase: with two issuers no later
-    // half-stage reuses the slot.
-    static_assert(kMmaWarps == 2 && ND > 2, "the last-slot wait needs two issuers");
+    // D slot's barrier is still at that phase: with two issuers and an even
+    // ring, only this issuer's own (earlier) half-stages use the slot.
+    static_assert(kMmaWarps == 2 && ND % 2 == 0, "the last-slot wait needs two issuers");
     if (last >= 0) mbar_wait(&mdone[last % ND], (last / ND) & 1, err);
   } else if (warp < kDecWarps) {
     // ------------------------------------------------------------ decode
     // Warp w owns TMEM lane quarter q = w % 4 (rows 32 q .. 32 q + 31) and the
-    // two groups 2 h, 2 h + 1 (h = w / 4) of every stage.
+    // four groups 4 h .. 4 h + 3 (h = w / 4, the stage's weight box h) of
+    // every stage.
     const int q = warp & 3;
     const int h = warp >> 2;
     const int r = q * 32 + lane;  // row within the block == TMEM lane
@@ -576,14 +610,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (hu >= NA && !__all_sync(0xffffffffu, mbar_wait(&afree[a], ((hu / NA) & 1) ^ 1, err)))
         break;
       tc_fence_after();
-      const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + r * 128;
-      const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
+      // half-stage h is weight box h: groups kGH h .. kGH h + kGH - 1
+      const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + h * (kRows * 128) + r * 128;
+      const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
 #pragma unroll
-      for (int gg = 0; gg < 2; ++gg) {
-        const int g = 2 * h + gg;
+      for (int gg = 0; gg < kGH; ++gg) {
+        const int g = kGH * h + gg;
         if (g < ng) {
-          const uint4 c0 = lds_v4(wrow + (((2 * g) ^ (r & 7)) << 4));
-          const uint4 c1 = lds_v4(wrow + (((2 * g + 1) ^ (r & 7)) << 4));
+          const uint4 c0 = lds_v4(wrow + (((2 * gg) ^ (r & 7)) << 4));
+          const uint4 c1 = lds_v4(wrow + (((2 * gg + 1) ^ (r & 7)) << 4));
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t av[32];
 #pragma unroll
@@ -593,7 +628,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
             av[4 * j + 2] = decode_e4m3<2>(w[j]);
             av[4 * j + 3] = decode_e4m3<3>(w[j]);
           }
-          tmem_st32(tbase + lane_off + C::kACol + a * 64 + gg * 32, av);
+          tmem_st32(tbase + lane_off + C::kACol + a * C::kASlot + gg * 32, av);
         }
       }
       tmem_wait_st();
@@ -720,14 +755,14 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     for (int j = 0; j < nunits && ok; ++j) {
       const int ss = j % SS;
       if (!__all_sync(0xffffffffu, mbar_wait(&sfull[ss], (j / SS) & 1, err))) break;
-      const int ng = G - 4 * ks < 4 ? G - 4 * ks : 4;
+      const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
       const uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
-      const uint2 sw = lds_v2(sst + r * 8);
-      const uint32_t s2 = fh ? sw.y : sw.x;  // this half-stage's two fp16 scales
+      // this half-stage's kGH fp16 scales
+      const uint2 s4 = lds_v2(sst + r * (2 * kGS) + fh * (2 * kGH));
       // f[g][t] at fv[g * FH + t]
       constexpr int FH = C::kInKernelX ? 1 : H;
-      const float* fv = C::kInKernelX ? ftab + ks * 4
-                                      : reinterpret_cast<const float*>(sst + kRows * 8);
+      const float* fv = C::kInKernelX ? ftab + ks * kGS
+                                      : reinterpret_cast<const float*>(sst + kRows * 2 * kGS);
       if constexpr (C::kInKernelX) {
         if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
       }
@@ -735,31 +770,33 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int d = hu % ND;
       if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) break;
       tc_fence_after();
-      const uint32_t dbase = tbase + lane_off + C::kDCol + d * 2 * NC;
+      const uint32_t dbase = tbase + lane_off + C::kDCol + d * C::kDSlot;
       // only the accumulator columns that carry tokens are read back:
       // piece 0 of token t is column t, piece 1 is H + t
       auto fold_group = [&](int gg, const uint32_t* dv) {
+        const uint32_t sp = gg < 2 ? s4.x : s4.y;
         const float sg = __half2float(__ushort_as_half(
-            static_cast<unsigned short>(gg ? (s2 >> 16) : (s2 & 0xFFFFu))));
-        const int g = 2 * fh + gg;
+            static_cast<unsigned short>((gg & 1) ? (sp >> 16) : (sp & 0xFFFFu))));
+        const int g = kGH * fh + gg;
 #pragma unroll
         for (int t = 0; t < TT; ++t)
           yacc[t] = fmaf(sg * fv[g * FH + t], __uint_as_float(dv[t]) + __uint_as_float(dv[H + t]),
                          yacc[t]);
       };
       static_assert(NC == 16 || NC == 32, "accumulator width");
-      if constexpr (NC == 32) {
-        // 16 tokens: one group at a time keeps the live registers down
+      static_assert(TT == 1 || TT == 4 || TT == 8 || TT == 16, "token tiles");
+      if constexpr (TT >= 8) {
+        // 8 or 16 tokens: one group at a time keeps the live registers down
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
+        for (int gg = 0; gg < kGH; ++gg) {
           uint32_t dv[NC];
-          const bool has = 2 * fh + gg < ng;
+          const bool has = kGH * fh + gg < ng;
           if (has) {
             tmem_ld16(dbase + gg * NC, dv);
-            tmem_ld16(dbase + gg * NC + 16, dv + 16);
+            if constexpr (NC == 32) tmem_ld16(dbase + gg * NC + 16, dv + 16);
           }
           tmem_wait_ld();
-          if (gg == 1) {
+          if (gg == kGH - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&dfree[d]);
@@ -767,19 +804,17 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
           if (has) fold_group(gg, dv);
         }
       } else {
-        uint32_t dv[2][NC];
+        uint32_t dv[kGH][NC];
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          if (2 * fh + gg < ng) {
+        for (int gg = 0; gg < kGH; ++gg) {
+          if (kGH * fh + gg < ng) {
             const uint32_t col = dbase + gg * NC;
             if constexpr (TT == 1) {
               tmem_ld1(col, dv[gg][0]);
               tmem_ld1(col + H, dv[gg][H]);
-            } else if constexpr (TT == 4) {
+            } else {
               tmem_ld4(col, dv[gg]);
               tmem_ld4(col + H, dv[gg] + H);
-            } else {
-              tmem_ld16(col, dv[gg]);  // 8 tokens: both pieces, columns 0 .. 15
             }
           }
         }
@@ -788,8 +823,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&dfree[d]);
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg)
-          if (2 * fh + gg < ng) fold_group(gg, dv[gg]);
+        for (int gg = 0; gg < kGH; ++gg)
+          if (kGH * fh + gg < ng) fold_group(gg, dv[gg]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[ss]);
@@ -855,7 +890,7 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint16_t* scales, const uint
 
   cudaLaunchAttribute attr[1];
   if constexpr (!C::kInKernelX) {
-    const int tasks = C::kH * 4 * KS;
+    const int tasks = C::kH * kGS * KS;
     cudaLaunchConfig_t pc = pdl_config(attr, dim3((tasks + 7) / 8), dim3(256), 0, stream);
     cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, KS);
     if (e != cudaSuccess) return e;

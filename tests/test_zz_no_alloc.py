@@ -38,11 +38,12 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(tl):
     assert _noalloc_raw(tl, 17, 512, 64) == -1
     assert _noalloc_raw(tl, 0, 512, 64) == -1
     # K whose activation blocks exceed the 4 MiB scratch (the largest K that
-    # fits is 257536 for T <= 8 and 128512 for T <= 16)
-    assert _noalloc_raw(tl, 1, 257664, 64) == -3
-    assert _noalloc_raw(tl, 8, 257664, 64) == -3
-    assert _noalloc_raw(tl, 9, 128640, 64) == -3
-    assert _noalloc_raw(tl, 16, 128640, 64) == -3
+    # fits is 257024 for T <= 8 and 128000 for T <= 16)
+    assert _noalloc_raw(tl, 1, 257152, 64) == -3
+    assert _noalloc_raw(tl, 8, 257152, 64) == -3
+    assert _noalloc_raw(tl, 9, 128128, 64) == -3
+    assert _noalloc_raw(tl, 16, 128128, 64) == -3
+    assert _noalloc_raw(tl, 16, 257152, 64) == -3
     assert "workspace" in tl.tern_status_string(-3)
 
 
