@@ -315,6 +315,58 @@ def test_stack_sweep_sampled(tl, p_zero, seed):
                 assert_bf16_parity(y[ti, ni], y_ref, m, what)
 
 
+def test_chained_calls_in_a_cuda_graph(tl):
+    """Back-to-back calls chained by programmatic dependent launch, captured
+    once in a CUDA graph and replayed: every rung, several shapes, one shared
+    workspace.  Each replay must leave the device status clean and every
+    output equal to the oracle's (sampled)."""
+    import torch
+    specs = [("gu", 1, 21), ("dn", 1, 22), ("ai", 4, 23), ("ao", 8, 24), ("ai", 12, 25),
+             ("gu", 1, 26), ("ao", 40, 27), ("dn", 1, 28)]
+    calls = []
+    ws_bytes = 0
+    for proj, T, seed in specs:
+        c = synth.case(proj, T, seed=seed, outliers=(T == 1 or T > 16))
+        W, s, x = to_device(c)
+        Wp = tl.tern_pack(W)
+        del W
+        y = torch.empty(T, c.N, dtype=torch.float32, device="cuda")
+        calls.append((c, Wp, s, x, y))
+        ws_bytes = max(ws_bytes, tl.tern_linear_workspace_bytes(T, c.K, c.N))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        for c, Wp, s, x, y in calls:  # library set-up outside the capture
+            tl.tern_linear(Wp, s, x, y, ws)
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for c, Wp, s, x, y in calls:
+                tl.tern_linear(Wp, s, x, y, ws)
+    for _ in range(5):
+        for _, _, _, _, y in calls:
+            y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert tl.tern_device_status() == 0
+    for c, Wp, s, x, y in calls:
+        yh = y.cpu().numpy()
+        wp_ref, _ = oracle.pack(c.W)
+        ti, ni = sample_indices(c.T, c.N, 1024, seed=c.K + c.T)
+        what = f"{c.name} T={c.T} (graph replay)"
+        if c.T >= 17:
+            q_ref, xs_ref = oracle.quant_s8(c.x, c.T, c.K)
+            y_ref, m, _ = oracle.linear_s8_sampled(wp_ref, c.scales, q_ref, xs_ref, c.K, c.N, ti, ni)
+            assert_s8_parity(yh[ti, ni], y_ref, m, what)
+        else:
+            y_ref, m = oracle.linear_f64_sampled(wp_ref, c.scales, c.x, c.K, c.N, ti, ni)
+            assert_bf16_parity(yh[ti, ni], y_ref, m, what)
+
+
 # ---------------------------------------------------------------- probe
 
 def test_debug_probe_reports_each_rung(tl):
