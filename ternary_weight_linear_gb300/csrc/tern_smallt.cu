@@ -145,7 +145,7 @@ struct TC {
   static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) f[stage][4]
   static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * kGS * 4 : 0);
   static constexpr int kNumBars =
-      2 * kStages + 2 * kSStages + 2 * kNAH + 2 * kNDH + 8 + (kInKernelX ? kX1MaxStages : 0);
+      2 * kStages + 2 * kSStages + 4 * kNAH + 2 * kNDH + 8 + (kInKernelX ? kX1MaxStages : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kFirstOff = kTmemSlot + 16;  // fold: parked first row block sums
   static constexpr int kPartOff = kFirstOff + TT * kRows * 4;  // fold: half-stage 1 sums
@@ -273,9 +273,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   uint64_t* empty = full + S;     // weights decoded and activation block consumed
   uint64_t* sfull = empty + S;    // scales + factors landed
   uint64_t* sempty = sfull + SS;  // ... and folded
-  uint64_t* afull = sempty + SS;  // A slot a written by its four decoders
-  uint64_t* afree = afull + NA;   // MMAs reading A slot a completed
-  uint64_t* mdone = afree + NA;   // MMAs writing D slot d completed
+  // A slots are used in two halves (sub-slots 2 a and 2 a + 1: groups 0-1
+  // and 2-3 of the half-stage), each with its own barriers, so the MMAs on
+  // one half overlap the decoding of the other.
+  uint64_t* afull = sempty + SS;     // A sub-slot written by its four decoders
+  uint64_t* afree = afull + 2 * NA;  // MMAs reading A sub-slot completed
+  uint64_t* mdone = afree + 2 * NA;  // MMAs writing D slot d completed
   uint64_t* dfree = mdone + ND;   // D slot d read back by the fold warps
   uint64_t* xready = dfree + ND;  // (T = 1) activation block of stage ks built
   // fold pairs: [quarter] the half-stage-1 warp's row block sums are in
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       mbar_init(&sfull[s], 32);
       mbar_init(&sempty[s], kFoldWarps);
     }
-    for (int a = 0; a < NA; ++a) {
+    for (int a = 0; a < 2 * NA; ++a) {
       mbar_init(&afull[a], kDecWarps / 2);
       mbar_init(&afree[a], 1);
     }
@@ -561,27 +564,39 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       }
       const int a = hu % NA;
       const int d = hu % ND;
-      if (!__all_sync(0xffffffffu, mbar_wait(&afull[a], (hu / NA) & 1, err)) ||
-          (hu >= ND &&
-           !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err))))
+      if (hu >= ND &&
+          !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err)))
         break;
-      tc_fence_after();
       const uint32_t dcol = tbase + C::kDCol + d * C::kDSlot;
       const uint32_t acol = tbase + C::kACol + a * C::kASlot;
-      if (leader) {
+      bool ok_h = true;
 #pragma unroll
-        for (int gg = 0; gg < kGH; ++gg) {
-          const int g = kGH * hh + gg;
-          if (g < ng) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
-                            dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
-                            idesc, kk > 0);
-          }
+      for (int b = 0; b < 2; ++b) {  // the two A sub-slots of the half-stage
+        if (!__all_sync(0xffffffffu, mbar_wait(&afull[2 * a + b], (hu / NA) & 1, err))) {
+          ok_h = false;
+          break;
         }
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int gs = 0; gs < kGH / 2; ++gs) {
+            const int gg = (kGH / 2) * b + gs;
+            const int g = kGH * hh + gg;
+            if (g < ng) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
+                              dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
+                              idesc, kk > 0);
+            }
+          }
+          mma_commit(&afree[2 * a + b]);
+        }
+        __syncwarp();
+      }
+      if (!ok_h) break;
+      if (leader) {
         if (!C::kInKernelX) mma_commit(&empty[s]);
-        mma_commit(&afree[a]);
         mma_commit(&mdone[d]);
       }
       __syncwarp();
@@ -607,37 +622,44 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int hu = 2 * it + h;  // this warp's half-stage
       const int a = hu % NA;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / S) & 1, err))) break;
-      if (hu >= NA && !__all_sync(0xffffffffu, mbar_wait(&afree[a], ((hu / NA) & 1) ^ 1, err)))
-        break;
-      tc_fence_after();
       // half-stage h is weight box h: groups kGH h .. kGH h + kGH - 1
       const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + h * (kRows * 128) + r * 128;
       const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
+      bool ok_h = true;
 #pragma unroll
-      for (int gg = 0; gg < kGH; ++gg) {
-        const int g = kGH * h + gg;
-        if (g < ng) {
-          const uint4 c0 = lds_v4(wrow + (((2 * gg) ^ (r & 7)) << 4));
-          const uint4 c1 = lds_v4(wrow + (((2 * gg + 1) ^ (r & 7)) << 4));
-          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint32_t av[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            av[4 * j + 0] = decode_e4m3<0>(w[j]);
-            av[4 * j + 1] = decode_e4m3<1>(w[j]);
-            av[4 * j + 2] = decode_e4m3<2>(w[j]);
-            av[4 * j + 3] = decode_e4m3<3>(w[j]);
-          }
-          tmem_st32(tbase + lane_off + C::kACol + a * C::kASlot + gg * 32, av);
+      for (int b = 0; b < 2; ++b) {  // A sub-slot b: groups 2 b, 2 b + 1 of the half-stage
+        if (hu >= NA &&
+            !__all_sync(0xffffffffu, mbar_wait(&afree[2 * a + b], ((hu / NA) & 1) ^ 1, err))) {
+          ok_h = false;
+          break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int gs = 0; gs < kGH / 2; ++gs) {
+          const int gg = (kGH / 2) * b + gs;
+          const int g = kGH * h + gg;
+          if (g < ng) {
+            const uint4 c0 = lds_v4(wrow + (((2 * gg) ^ (r & 7)) << 4));
+            const uint4 c1 = lds_v4(wrow + (((2 * gg + 1) ^ (r & 7)) << 4));
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t av[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              av[4 * j + 0] = decode_e4m3<0>(w[j]);
+              av[4 * j + 1] = decode_e4m3<1>(w[j]);
+              av[4 * j + 2] = decode_e4m3<2>(w[j]);
+              av[4 * j + 3] = decode_e4m3<3>(w[j]);
+            }
+            tmem_st32(tbase + lane_off + C::kACol + a * C::kASlot + gg * 32, av);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[2 * a + b]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&afull[a]);
-        mbar_arrive(&empty[s]);
-      }
+      if (!ok_h) break;
+      if (lane == 0) mbar_arrive(&empty[s]);
       if (++ks == KS) ks = 0;
     }
   } else {
