@@ -9,11 +9,10 @@
  *   T = 9..16    two small-T token tiles per weight    rung "small_t_tiled"
  *   T >= 17      int8 per-token activations ("s8")     rung "s8"
  * The band map, the env override and the per-rung probe follow the rung map
- * and the probe discipline of the "ninfer-perf-tuning" skill page
- * (markdownregistry.com), section 2 ("which rung ran" and its rung-map
- * table); the format follows the "NInfer sm_89 fork" write-up
- * (2kiu.com/news/5424991), section 9 item 2 (ternary codes plus one FP16
- * scale per 128 weights; int8 activations with m16n8k32 int8 MMA for prefill).
+ * and the probe discipline of the "ninfer-perf-tuning" skill page, section 2
+ * ("which rung ran" and its rung-map table); the format follows the "NInfer
+ * sm_89 fork" write-up, section 9 item 2 (ternary codes plus one FP16 scale
+ * per 128 weights; int8 activations with m16n8k32 int8 MMA for prefill).
  *
  * Conventions for every entry point
  *  - All array arguments are DEVICE pointers of the current CUDA device, owned

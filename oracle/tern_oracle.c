@@ -9,7 +9,7 @@
  * What it computes (all citations name a web page and a section on it):
  *
  *  - Ternary weights w in {-1, 0, +1} with one fp16 scale per 128 consecutive
- *    weights along K ("NInfer sm_89 fork" write-up, 2kiu.com/news/5424991,
+ *    weights along K ("NInfer sm_89 fork" write-up,
  *    section 9 "why NInfer is fast", item 2 "ternary weights": codes plus one
  *    FP16 scale per 128 weights).
  *
@@ -31,7 +31,7 @@
  *    acc[t,n,g] = sum_{k in g} q w exactly in integers and
  *    y = xs * sum_g s * acc (fp64 here).  Int8 activations x ternary-as-int8
  *    weights with int32 accumulation is the "s8" prefill rung of the
- *    "ninfer-perf-tuning" skill page (markdownregistry.com), section 2 rung map
+ *    "ninfer-perf-tuning" skill page, section 2 rung map
  *    and section 4 numeric gate; per-token absmax/127 with round-to-nearest-even
  *    is the reading of "quantised per token to int8".
  *

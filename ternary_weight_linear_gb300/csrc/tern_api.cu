@@ -2,8 +2,8 @@
 // dispatcher with its environment override and per-rung debug probe, tensor
 // map set-up, and the launches.
 //
-// Dispatcher: the rung map of the "ninfer-perf-tuning" skill page
-// (markdownregistry.com), section 2 — T = 1 decode entry, T = 2..8 small-T
+// Dispatcher: the rung map of the "ninfer-perf-tuning" skill page,
+// section 2 — T = 1 decode entry, T = 2..8 small-T
 // tile, T = 9..16 tiled small-T, T >= 17 int8 "s8" — with env-overridable
 // thresholds read once per process, and a probe that prints which rung ran
 // (section 2: every reachable branch reports itself), limited by a minimum T
