@@ -34,9 +34,9 @@
 //    into their row's running sums with s[n][g] * f[g][token].
 //
 // Pipeline (one CTA per SM, persistent; TMEM 512 columns):
-//   warp 16    producer: one 2D TMA box of packed weights (128 rows x 128 B,
-//              128-byte swizzle) per stage into the weight ring (plus, for
-//              T > 1, a bulk copy of the stage's activation block); the
+//   warp 16    producer: two 2D TMA boxes of packed weights (128 rows x 128 B
+//              each, 128-byte swizzle) per stage into the weight ring (plus,
+//              for T > 1, a bulk copy of the stage's activation block); the
 //              stage's fp16 scales (cp.async) into a longer scale ring;
 //   warps 19-22 (T = 1) build the resident activation blocks and factors;
 //   warps 0-7  decode (four groups of 32 rows per warp) into A slots;
@@ -60,13 +60,18 @@
 // half-stage is one box, four groups.  TMEM is used in half-stage slots: the
 // decode warps of groups 0-3 and of groups 4-7 each fill their own A slot,
 // the MMAs of a half-stage write their own D slot, so decode, MMA and fold
-// can run half-stages apart.  (Doubling the stage from 512 k halved every
-// role's barrier hand-offs per byte, which bound the pipeline.)
+// can run half-stages apart; each A slot is filled and released in two
+// halves (groups 0-1, 2-3), so a half-stage's MMAs overlap the decoding of
+// its next use.  (Doubling the stage from 512 k halved every role's barrier
+// hand-offs per byte, which bound the pipeline.)
 //
 // Calls chain by programmatic dependent launch: every kernel lets the next one
 // launch as soon as all of its CTAs run; the next kernel's CTAs set up, warm
 // L2 with their first weight tiles and wait for the previous grid before they
 // read anything it may have written (weights, x) or write y / the workspace.
+// Every ring of slots has an even length, so a slot only ever holds
+// half-stages of one parity (one decode half, one MMA issuer, one fold half):
+// a waiter's barrier is then never two phases behind it.
 //
 // The pages' kernel for this band (the "small_t" rung of the
 // "ninfer-perf-tuning" skill page, sections 2 and 6) decodes through a LUT
