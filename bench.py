@@ -77,6 +77,25 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms, world, device):
+    """The job's time for a region that every rank timed on its own GPU: the
+    largest per-rank figure (each replica runs the same work, so the job ends
+    with the slowest one).  world == 1 returns ms unchanged."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Aggregate weight GB/s of world independent replicas, each streaming the
+    same bytes per step, over the job's (slowest rank's) time per step."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -301,14 +320,11 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
-        ms = float(t.item())
     ms_per_step = ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9  # GB/s, whole job
+    value = whole_job_gbs(world, step_bytes, ms_per_step)
 
     # ---- dominant kernel: the gate+up T=1 call, timed back to back
     reps = 200
@@ -396,8 +412,8 @@ def run_ours(args, rank, world, local):
             yh.copy_(y_dn[-1], non_blocking=True)
         ee1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = ee0.elapsed_time(ee1) / e2e_steps
-    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(ee0.elapsed_time(ee1), world, dev) / e2e_steps
+    e2e_val = whole_job_gbs(world, step_bytes, e2e_ms)
     if not np.isfinite(yh.numpy()).all():
         raise RuntimeError("non-finite output")
     if tl.tern_device_status() != 0:
