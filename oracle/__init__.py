@@ -9,9 +9,14 @@ This module compiles it with gcc on first use (or from ``build()``) and exposes
 numpy-friendly wrappers.  See the header of ``tern_oracle.c`` for what each
 function computes and which page section it follows.
 
+Two packed weight formats are understood: the 2-bit code (uint32 words
+[N, K/16]) and the base-3 code, five weights per byte (uint8 [N, K/128*26]).
+The linear definitions take either and pick the format from the dtype.
+
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests in
-``tests/test_oracle_pins.py`` (hand-written packed words, brute force on tiny
-inputs, closed forms, invariants); none is "parity unpinned".
+``tests/test_oracle_pins.py`` (hand-written packed words and bytes, brute force
+on tiny inputs, closed forms, numpy's base conversion, invariants); none is
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -71,6 +76,18 @@ def _load():
         lib.tern_oracle_linear_s8.restype = None
         lib.tern_oracle_linear_s8_sampled.argtypes = [P, P, P, P, i32, i32, P, P, i64, P, P, P]
         lib.tern_oracle_linear_s8_sampled.restype = None
+        lib.tern_oracle_pack_t5.argtypes = [P, i32, i32, P]
+        lib.tern_oracle_pack_t5.restype = i64
+        lib.tern_oracle_unpack_t5.argtypes = [P, i32, i32, P]
+        lib.tern_oracle_unpack_t5.restype = i64
+        lib.tern_oracle_linear_t5_f64.argtypes = [P, P, P, i32, i32, i32, P, P]
+        lib.tern_oracle_linear_t5_f64.restype = None
+        lib.tern_oracle_linear_t5_f64_sampled.argtypes = [P, P, P, i32, i32, P, P, i64, P, P]
+        lib.tern_oracle_linear_t5_f64_sampled.restype = None
+        lib.tern_oracle_linear_t5_s8.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
+        lib.tern_oracle_linear_t5_s8.restype = None
+        lib.tern_oracle_linear_t5_s8_sampled.argtypes = [P, P, P, P, i32, i32, P, P, i64, P, P, P]
+        lib.tern_oracle_linear_t5_s8_sampled.restype = None
         lib.tern_oracle_num_threads.argtypes = []
         lib.tern_oracle_num_threads.restype = i32
         _lib = lib
@@ -91,6 +108,29 @@ def _u16(a: np.ndarray) -> np.ndarray:
         return a.view(np.uint16)
     assert a.dtype == np.uint16, a.dtype
     return a
+
+
+T5_GROUP_BYTES = 26  # ceil(128 / 5) base-3 bytes per 128-weight group
+
+
+def _packed(wp, K: int, N: int):
+    """The packed weights and their format: uint32 words [N, K/16] are the
+    2-bit code ("2bit"), uint8 bytes [N, K/128*26] the base-3 code ("t5")."""
+    wp = np.ascontiguousarray(wp)
+    if wp.dtype == np.uint32:
+        assert wp.size == N * (K // 16), (wp.shape, K, N)
+        return wp, "2bit"
+    assert wp.dtype == np.uint8, wp.dtype
+    assert wp.size == N * (K // 128) * T5_GROUP_BYTES, (wp.shape, K, N)
+    return wp, "t5"
+
+
+def _fn(name: str, fmt: str):
+    """The C entry point of a definition ("linear_f64", "linear_s8_sampled", ...)
+    for a weight format."""
+    if fmt == "t5":
+        name = name.replace("linear_", "linear_t5_", 1)
+    return getattr(_load(), "tern_oracle_" + name)
 
 
 def num_threads() -> int:
@@ -117,22 +157,43 @@ def unpack(wp: np.ndarray, K: int) -> tuple[np.ndarray, int]:
     return W, int(bad)
 
 
+def pack_t5(W: np.ndarray) -> tuple[np.ndarray, int]:
+    """W int8 [N, K] -> (base-3 bytes uint8 [N, K/128*26], count of values not
+    in {-1,0,1}).  Five weights per byte, 26 bytes per 128-weight group."""
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    N, K = W.shape
+    assert K % 128 == 0
+    p = np.empty((N, K // 128 * T5_GROUP_BYTES), dtype=np.uint8)
+    bad = _load().tern_oracle_pack_t5(_ptr(W), K, N, _ptr(p))
+    return p, int(bad)
+
+
+def unpack_t5(p: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    """base-3 bytes [N, K/128*26] -> (W int8 [N, K], count of invalid bytes)."""
+    p = np.ascontiguousarray(p, dtype=np.uint8)
+    N = p.shape[0]
+    assert p.shape[1] == K // 128 * T5_GROUP_BYTES
+    W = np.empty((N, K), dtype=np.int8)
+    bad = _load().tern_oracle_unpack_t5(_ptr(p), K, N, _ptr(W))
+    return W, int(bad)
+
+
 def linear_f64(wp, scales_f16, x_bf16, T: int, K: int, N: int):
     """bf16-rung definition in fp64.  Returns (y [T, N], m [T, N]) where
-    m = sum |s w x| is the tolerance scale."""
-    wp = np.ascontiguousarray(wp, dtype=np.uint32)
+    m = sum |s w x| is the tolerance scale.  wp is either packed format."""
+    wp, fmt = _packed(wp, K, N)
     s = _u16(scales_f16)
     x = _u16(x_bf16)
-    assert wp.size == N * (K // 16) and s.size == N * (K // 128) and x.size == T * K
+    assert s.size == N * (K // 128) and x.size == T * K
     y = np.empty((T, N), dtype=np.float64)
     m = np.empty((T, N), dtype=np.float64)
-    _load().tern_oracle_linear_f64(_ptr(wp), _ptr(s), _ptr(x), T, K, N, _ptr(y), _ptr(m))
+    _fn("linear_f64", fmt)(_ptr(wp), _ptr(s), _ptr(x), T, K, N, _ptr(y), _ptr(m))
     return y, m
 
 
 def linear_f64_sampled(wp, scales_f16, x_bf16, K: int, N: int, t_idx, n_idx):
     """The bf16-rung definition at the listed (t, n) outputs only."""
-    wp = np.ascontiguousarray(wp, dtype=np.uint32)
+    wp, fmt = _packed(wp, K, N)
     s = _u16(scales_f16)
     x = _u16(x_bf16)
     t_idx = np.ascontiguousarray(t_idx, dtype=np.int32)
@@ -140,8 +201,8 @@ def linear_f64_sampled(wp, scales_f16, x_bf16, K: int, N: int, t_idx, n_idx):
     cnt = t_idx.size
     y = np.empty(cnt, dtype=np.float64)
     m = np.empty(cnt, dtype=np.float64)
-    _load().tern_oracle_linear_f64_sampled(_ptr(wp), _ptr(s), _ptr(x), K, N, _ptr(t_idx),
-                                           _ptr(n_idx), cnt, _ptr(y), _ptr(m))
+    _fn("linear_f64_sampled", fmt)(_ptr(wp), _ptr(s), _ptr(x), K, N, _ptr(t_idx),
+                                   _ptr(n_idx), cnt, _ptr(y), _ptr(m))
     return y, m
 
 
@@ -157,7 +218,7 @@ def quant_s8(x_bf16, T: int, K: int):
 
 def linear_s8(wp, scales_f16, q, xs, T: int, K: int, N: int, want_acc: bool = False):
     """s8-rung definition.  Returns (y [T, N] fp64, m [T, N], acc int64 [T, N, G] or None)."""
-    wp = np.ascontiguousarray(wp, dtype=np.uint32)
+    wp, fmt = _packed(wp, K, N)
     s = _u16(scales_f16)
     q = np.ascontiguousarray(q, dtype=np.int8)
     xs = np.ascontiguousarray(xs, dtype=np.float32)
@@ -165,15 +226,15 @@ def linear_s8(wp, scales_f16, q, xs, T: int, K: int, N: int, want_acc: bool = Fa
     y = np.empty((T, N), dtype=np.float64)
     m = np.empty((T, N), dtype=np.float64)
     acc = np.empty((T, N, G), dtype=np.int64) if want_acc else None
-    _load().tern_oracle_linear_s8(_ptr(wp), _ptr(s), _ptr(q), _ptr(xs), T, K, N, _ptr(acc),
-                                  _ptr(y), _ptr(m))
+    _fn("linear_s8", fmt)(_ptr(wp), _ptr(s), _ptr(q), _ptr(xs), T, K, N, _ptr(acc),
+                          _ptr(y), _ptr(m))
     return y, m, acc
 
 
 def linear_s8_sampled(wp, scales_f16, q, xs, K: int, N: int, t_idx, n_idx,
                       want_acc: bool = False):
     """s8-rung definition at the listed (t, n) outputs.  Returns (y, m, acc [cnt, G] or None)."""
-    wp = np.ascontiguousarray(wp, dtype=np.uint32)
+    wp, fmt = _packed(wp, K, N)
     s = _u16(scales_f16)
     q = np.ascontiguousarray(q, dtype=np.int8)
     xs = np.ascontiguousarray(xs, dtype=np.float32)
@@ -184,7 +245,7 @@ def linear_s8_sampled(wp, scales_f16, q, xs, K: int, N: int, t_idx, n_idx,
     y = np.empty(cnt, dtype=np.float64)
     m = np.empty(cnt, dtype=np.float64)
     acc = np.empty((cnt, G), dtype=np.int64) if want_acc else None
-    _load().tern_oracle_linear_s8_sampled(_ptr(wp), _ptr(s), _ptr(q), _ptr(xs), K, N,
-                                          _ptr(t_idx), _ptr(n_idx), cnt, _ptr(acc), _ptr(y),
-                                          _ptr(m))
+    _fn("linear_s8_sampled", fmt)(_ptr(wp), _ptr(s), _ptr(q), _ptr(xs), K, N,
+                                  _ptr(t_idx), _ptr(n_idx), cnt, _ptr(acc), _ptr(y),
+                                  _ptr(m))
     return y, m, acc

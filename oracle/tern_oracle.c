@@ -35,8 +35,26 @@
  *    and section 4 numeric gate; per-token absmax/127 with round-to-nearest-even
  *    is the reading of "quantised per token to int8".
  *
+ *  - base-3 packing, five weights per byte ("NInfer sm_89 fork" write-up,
+ *    section 9, item 2: base-3 codes five to a byte with one FP16 scale per
+ *    128 weights, 1.75 bits per weight on average).  Each 128-weight group of
+ *    a row takes ceil(128/5) = 26 bytes; with its fp16 scale that is 28 bytes
+ *    per 128 weights, exactly the 1.75 bits the page gives.  Byte j of group
+ *    g of row n is P[(n*G + g)*26 + j] and holds the weights
+ *    k = 128g + 5j + i, i = 0..4, as the base-3 number
+ *        byte = sum_i (w_i + 1) * 3^i          (0..242),
+ *    so the first weight is the least significant digit.  The last byte of a
+ *    group holds three weights; its digits 3 and 4 are padding written as
+ *    weight 0 and ignored on reading.  Bytes 243..255 are invalid.  The
+ *    scales stay in their own [N][K/128] fp16 array, as for the 2-bit code.
+ *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - the 2-bit code is sign-magnitude with the bit order above;
+ *  - the base-3 byte is a plain base-3 integer, least significant digit
+ *    first, 26 bytes per group with padding digits for weight 0;
+ *  - an invalid code (the 2-bit pair (0, 1), a base-3 byte above 242) reads
+ *    as weight 0 in every definition here, as the library documents for its
+ *    kernels, and is counted by the unpack functions;
  *  - the quantiser divides by xs = a/127 in IEEE fp32 and clamps to +-127;
  *  - a token whose absmax is 0 gets xs = 0 and q = 0.
  *
@@ -130,65 +148,154 @@ long tern_oracle_unpack(const uint32_t* wp, int K, int N, int8_t* W) {
   return bad;
 }
 
+/* ---- base-3 packing: five weights per byte ------------------------------- */
+
+#define T5_GROUP_BYTES 26 /* ceil(128 / 5) */
+
+/* Weight (n, k) from a base-3 packed matrix; 2 for an invalid byte. */
+static int unpack_one_t5(const uint8_t* p, int K, int n, int k) {
+  int G = K / 128, r = k % 128;
+  unsigned v = p[((size_t)n * G + k / 128) * T5_GROUP_BYTES + r / 5];
+  if (v > 242u) return 2;
+  for (int i = 0; i < r % 5; ++i) v /= 3u;
+  return (int)(v % 3u) - 1;
+}
+
+/* W [N][K] int8 in {-1,0,1} -> base-3 bytes [N][K/128][26].  Values outside
+ * {-1,0,1} are stored as 0 and counted; the count is returned. */
+long tern_oracle_pack_t5(const int8_t* W, int K, int N, uint8_t* p) {
+  long bad = 0;
+  int G = K / 128;
+  for (int n = 0; n < N; ++n)
+    for (int g = 0; g < G; ++g)
+      for (int j = 0; j < T5_GROUP_BYTES; ++j) {
+        unsigned v = 0, place = 1;
+        for (int i = 0; i < 5; ++i, place *= 3u) {
+          int r = 5 * j + i, w = 0;
+          if (r < 128) {
+            w = W[(size_t)n * K + (size_t)g * 128 + r];
+            if (w < -1 || w > 1) {
+              ++bad;
+              w = 0;
+            }
+          }
+          v += (unsigned)(w + 1) * place;
+        }
+        p[((size_t)n * G + g) * T5_GROUP_BYTES + j] = (uint8_t)v;
+      }
+  return bad;
+}
+
+/* base-3 bytes -> W [N][K] int8; the weights of an invalid byte become 0.
+ * Returns the number of invalid bytes. */
+long tern_oracle_unpack_t5(const uint8_t* p, int K, int N, int8_t* W) {
+  long bad = 0;
+  size_t bytes = (size_t)N * (size_t)(K / 128) * T5_GROUP_BYTES;
+  for (size_t b = 0; b < bytes; ++b) bad += p[b] > 242u;
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) {
+      int w = unpack_one_t5(p, K, n, k);
+      W[(size_t)n * K + k] = (int8_t)(w == 2 ? 0 : w);
+    }
+  return bad;
+}
+
+/* ---- the weight as the layer reads it ------------------------------------ */
+
+/* Both packed formats go through one reader type, so each definition below
+ * is written once.  An invalid code reads as 0. */
+typedef int (*weight_reader)(const void* packed, int K, int n, int k);
+
+static int read_2bit(const void* packed, int K, int n, int k) {
+  int w = unpack_one((const uint32_t*)packed, K, n, k);
+  return w == 2 ? 0 : w;
+}
+
+static int read_t5(const void* packed, int K, int n, int k) {
+  int w = unpack_one_t5((const uint8_t*)packed, K, n, k);
+  return w == 2 ? 0 : w;
+}
+
 /* ---- bf16 rungs: plain fp64 definition ----------------------------------- */
 
-/* y[t][n] = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k]   (fp64)
- * m[t][n] = sum_g sum_{k in g} |s[n][g] * w[n][k] * x[t][k]|  (fp64)
- * scales: fp16 bits [N][K/128]; x: bf16 bits [T][K].  m may be NULL.
- * Rows n are independent, so they are split across threads; each output is a
- * single sequential sum in k order. */
-void tern_oracle_linear_f64(const uint32_t* wp, const uint16_t* scales,
-                            const uint16_t* x, int T, int K, int N, double* y,
-                            double* m) {
+/* y = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k] for one output (fp64),
+ * one sequential sum in k order; *m = sum_g sum_{k in g} |s w x|. */
+static double dot_f64(weight_reader rd, const void* packed,
+                      const uint16_t* scales, const uint16_t* x, int K, int t,
+                      int n, double* m) {
   int G = K / 128;
+  double acc = 0.0, mag = 0.0;
+  for (int g = 0; g < G; ++g) {
+    double s = f16_to_f64(scales[(size_t)n * G + g]);
+    double part = 0.0, partm = 0.0;
+    for (int k = g * 128; k < (g + 1) * 128; ++k) {
+      int w = rd(packed, K, n, k);
+      double xv = (double)bf16_to_f32(x[(size_t)t * K + k]);
+      part += (double)w * xv;
+      partm += fabs((double)w * xv);
+    }
+    acc += s * part;
+    mag += fabs(s) * partm;
+  }
+  *m = mag;
+  return acc;
+}
+
+/* y [T][N], m [T][N] (m may be NULL); rows n are split across threads. */
+static void linear_f64(weight_reader rd, const void* packed,
+                       const uint16_t* scales, const uint16_t* x, int T, int K,
+                       int N, double* y, double* m) {
 #pragma omp parallel for schedule(dynamic, 16)
-  for (int n = 0; n < N; ++n) {
+  for (int n = 0; n < N; ++n)
     for (int t = 0; t < T; ++t) {
-      double acc = 0.0, mag = 0.0;
-      for (int g = 0; g < G; ++g) {
-        double s = f16_to_f64(scales[(size_t)n * G + g]);
-        double part = 0.0, partm = 0.0;
-        for (int k = g * 128; k < (g + 1) * 128; ++k) {
-          int w = unpack_one(wp, K, n, k);
-          double xv = (double)bf16_to_f32(x[(size_t)t * K + k]);
-          part += (double)w * xv;
-          partm += fabs((double)w * xv);
-        }
-        acc += s * part;
-        mag += fabs(s) * partm;
-      }
-      y[(size_t)t * N + n] = acc;
+      double mag;
+      y[(size_t)t * N + n] = dot_f64(rd, packed, scales, x, K, t, n, &mag);
       if (m) m[(size_t)t * N + n] = mag;
     }
+}
+
+/* The same for a list of sampled outputs (t_idx[i], n_idx[i]). */
+static void linear_f64_sampled(weight_reader rd, const void* packed,
+                               const uint16_t* scales, const uint16_t* x,
+                               int K, const int* t_idx, const int* n_idx,
+                               long count, double* y, double* m) {
+#pragma omp parallel for schedule(dynamic, 64)
+  for (long i = 0; i < count; ++i) {
+    double mag;
+    y[i] = dot_f64(rd, packed, scales, x, K, t_idx[i], n_idx[i], &mag);
+    if (m) m[i] = mag;
   }
 }
 
-/* Same definition for a list of sampled outputs (t_idx[i], n_idx[i]). */
+/* scales: fp16 bits [N][K/128]; x: bf16 bits [T][K]; 2-bit weights
+ * [N][K/16] u32 or base-3 weights [N][K/128][26] bytes. */
+void tern_oracle_linear_f64(const uint32_t* wp, const uint16_t* scales,
+                            const uint16_t* x, int T, int K, int N, double* y,
+                            double* m) {
+  linear_f64(read_2bit, wp, scales, x, T, K, N, y, m);
+}
+
 void tern_oracle_linear_f64_sampled(const uint32_t* wp, const uint16_t* scales,
                                     const uint16_t* x, int K, int N,
                                     const int* t_idx, const int* n_idx,
                                     long count, double* y, double* m) {
-  int G = K / 128;
-#pragma omp parallel for schedule(dynamic, 64)
-  for (long i = 0; i < count; ++i) {
-    int t = t_idx[i], n = n_idx[i];
-    double acc = 0.0, mag = 0.0;
-    for (int g = 0; g < G; ++g) {
-      double s = f16_to_f64(scales[(size_t)n * G + g]);
-      double part = 0.0, partm = 0.0;
-      for (int k = g * 128; k < (g + 1) * 128; ++k) {
-        int w = unpack_one(wp, K, n, k);
-        double xv = (double)bf16_to_f32(x[(size_t)t * K + k]);
-        part += (double)w * xv;
-        partm += fabs((double)w * xv);
-      }
-      acc += s * part;
-      mag += fabs(s) * partm;
-    }
-    y[i] = acc;
-    if (m) m[i] = mag;
-  }
   (void)N;
+  linear_f64_sampled(read_2bit, wp, scales, x, K, t_idx, n_idx, count, y, m);
+}
+
+void tern_oracle_linear_t5_f64(const uint8_t* p, const uint16_t* scales,
+                               const uint16_t* x, int T, int K, int N,
+                               double* y, double* m) {
+  linear_f64(read_t5, p, scales, x, T, K, N, y, m);
+}
+
+void tern_oracle_linear_t5_f64_sampled(const uint8_t* p,
+                                       const uint16_t* scales,
+                                       const uint16_t* x, int K, int N,
+                                       const int* t_idx, const int* n_idx,
+                                       long count, double* y, double* m) {
+  (void)N;
+  linear_f64_sampled(read_t5, p, scales, x, K, t_idx, n_idx, count, y, m);
 }
 
 /* ---- s8 rung ------------------------------------------------------------- */
@@ -220,58 +327,91 @@ void tern_oracle_quant_s8(const uint16_t* x, int T, int K, int8_t* q,
   }
 }
 
-/* Exact per-group integer accumulators and the fp64 output:
- *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]          (int64, exact)
- *   y[t][n]      = xs[t] * sum_g s[n][g] * acc[t][n][g]    (fp64)
- *   m[t][n]      = xs[t] * sum_g |s[n][g] * acc[t][n][g]|  (tolerance scale)
- * acc and m may be NULL. */
-void tern_oracle_linear_s8(const uint32_t* wp, const uint16_t* scales,
-                           const int8_t* q, const float* xs, int T, int K,
-                           int N, int64_t* acc, double* y, double* m) {
+/* Exact per-group integer accumulators and the fp64 output for one output:
+ *   acc[g] = sum_{k in g} q[t][k] * w[n][k]          (int64, exact)
+ *   y      = xs[t] * sum_g s[n][g] * acc[g]          (fp64)
+ *   *m     = xs[t] * sum_g |s[n][g] * acc[g]|        (tolerance scale)
+ * acc may be NULL. */
+static double dot_s8(weight_reader rd, const void* packed,
+                     const uint16_t* scales, const int8_t* q, const float* xs,
+                     int K, int t, int n, int64_t* acc, double* m) {
+  int G = K / 128;
+  double sum = 0.0, mag = 0.0;
+  for (int g = 0; g < G; ++g) {
+    int64_t a = 0;
+    for (int k = g * 128; k < (g + 1) * 128; ++k)
+      a += (int64_t)q[(size_t)t * K + k] * (int64_t)rd(packed, K, n, k);
+    if (acc) acc[g] = a;
+    double s = f16_to_f64(scales[(size_t)n * G + g]);
+    sum += s * (double)a;
+    mag += fabs(s * (double)a);
+  }
+  *m = fabs((double)xs[t]) * mag;
+  return (double)xs[t] * sum;
+}
+
+/* y [T][N], acc [T][N][G], m [T][N]; acc and m may be NULL. */
+static void linear_s8(weight_reader rd, const void* packed,
+                      const uint16_t* scales, const int8_t* q, const float* xs,
+                      int T, int K, int N, int64_t* acc, double* y, double* m) {
   int G = K / 128;
 #pragma omp parallel for schedule(dynamic, 16)
-  for (int n = 0; n < N; ++n) {
+  for (int n = 0; n < N; ++n)
     for (int t = 0; t < T; ++t) {
-      double sum = 0.0, mag = 0.0;
-      for (int g = 0; g < G; ++g) {
-        int64_t a = 0;
-        for (int k = g * 128; k < (g + 1) * 128; ++k)
-          a += (int64_t)q[(size_t)t * K + k] * (int64_t)unpack_one(wp, K, n, k);
-        if (acc) acc[((size_t)t * N + n) * G + g] = a;
-        double s = f16_to_f64(scales[(size_t)n * G + g]);
-        sum += s * (double)a;
-        mag += fabs(s * (double)a);
-      }
-      y[(size_t)t * N + n] = (double)xs[t] * sum;
-      if (m) m[(size_t)t * N + n] = fabs((double)xs[t]) * mag;
+      double mag;
+      size_t o = (size_t)t * N + n;
+      y[o] = dot_s8(rd, packed, scales, q, xs, K, t, n, acc ? acc + o * G : NULL,
+                    &mag);
+      if (m) m[o] = mag;
     }
+}
+
+/* The same for sampled outputs; acc is [count][G]. */
+static void linear_s8_sampled(weight_reader rd, const void* packed,
+                              const uint16_t* scales, const int8_t* q,
+                              const float* xs, int K, const int* t_idx,
+                              const int* n_idx, long count, int64_t* acc,
+                              double* y, double* m) {
+  int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 64)
+  for (long i = 0; i < count; ++i) {
+    double mag;
+    y[i] = dot_s8(rd, packed, scales, q, xs, K, t_idx[i], n_idx[i],
+                  acc ? acc + (size_t)i * G : NULL, &mag);
+    if (m) m[i] = mag;
   }
 }
 
-/* Same for sampled outputs. */
+void tern_oracle_linear_s8(const uint32_t* wp, const uint16_t* scales,
+                           const int8_t* q, const float* xs, int T, int K,
+                           int N, int64_t* acc, double* y, double* m) {
+  linear_s8(read_2bit, wp, scales, q, xs, T, K, N, acc, y, m);
+}
+
 void tern_oracle_linear_s8_sampled(const uint32_t* wp, const uint16_t* scales,
                                    const int8_t* q, const float* xs, int K,
                                    int N, const int* t_idx, const int* n_idx,
                                    long count, int64_t* acc, double* y,
                                    double* m) {
-  int G = K / 128;
-#pragma omp parallel for schedule(dynamic, 64)
-  for (long i = 0; i < count; ++i) {
-    int t = t_idx[i], n = n_idx[i];
-    double sum = 0.0, mag = 0.0;
-    for (int g = 0; g < G; ++g) {
-      int64_t a = 0;
-      for (int k = g * 128; k < (g + 1) * 128; ++k)
-        a += (int64_t)q[(size_t)t * K + k] * (int64_t)unpack_one(wp, K, n, k);
-      if (acc) acc[(size_t)i * G + g] = a;
-      double s = f16_to_f64(scales[(size_t)n * G + g]);
-      sum += s * (double)a;
-      mag += fabs(s * (double)a);
-    }
-    y[i] = (double)xs[t] * sum;
-    if (m) m[i] = fabs((double)xs[t]) * mag;
-  }
   (void)N;
+  linear_s8_sampled(read_2bit, wp, scales, q, xs, K, t_idx, n_idx, count, acc,
+                    y, m);
+}
+
+void tern_oracle_linear_t5_s8(const uint8_t* p, const uint16_t* scales,
+                              const int8_t* q, const float* xs, int T, int K,
+                              int N, int64_t* acc, double* y, double* m) {
+  linear_s8(read_t5, p, scales, q, xs, T, K, N, acc, y, m);
+}
+
+void tern_oracle_linear_t5_s8_sampled(const uint8_t* p, const uint16_t* scales,
+                                      const int8_t* q, const float* xs, int K,
+                                      int N, const int* t_idx,
+                                      const int* n_idx, long count,
+                                      int64_t* acc, double* y, double* m) {
+  (void)N;
+  linear_s8_sampled(read_t5, p, scales, q, xs, K, t_idx, n_idx, count, acc, y,
+                    m);
 }
 
 int tern_oracle_num_threads(void) {

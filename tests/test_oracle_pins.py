@@ -287,6 +287,198 @@ def test_linear_s8_sampled_matches_full():
     assert np.array_equal(accs, acc[ti, ni])
 
 
+# ---------------------------------------------------------------- invalid codes
+
+def _brute_s8(W, s, q, xs):
+    """y = xs * sum_g s * sum_{k in g} q w with exact rationals; the integer
+    accumulators acc[t, n, g] beside it."""
+    N, K = W.shape
+    T, G = q.shape[0], K // 128
+    y = np.zeros((T, N))
+    acc = np.zeros((T, N, G), dtype=np.int64)
+    for t in range(T):
+        for n in range(N):
+            tot = Fraction(0)
+            for g in range(G):
+                a = sum(int(q[t, k]) * int(W[n, k]) for k in range(g * 128, (g + 1) * 128))
+                acc[t, n, g] = a
+                tot += Fraction(float(s[n, g])) * a
+            y[t, n] = float(Fraction(float(xs[t])) * tot)
+    return y, acc
+
+
+def test_invalid_2bit_pairs_read_as_zero_in_both_rungs():
+    # The library documents that its kernels read the invalid pair
+    # (nz = 0, neg = 1) as weight 0; the oracle's definitions must too.
+    T, K, N = 2, 256, 3
+    W = synth.ternary_weights(N, K, 0.2, seed=61)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=62)
+    x = synth.activations(T, K, seed=63)
+    wp, _ = oracle.pack(W)
+    # turn three nonzero weights into the invalid pair: keep only the
+    # negative bit (nonzero bit at P[i] = {0,1,4,5}[k%4], negative bit 2 above)
+    Wz = W.copy()
+    for n, start in [(0, 5), (1, 130), (2, 200)]:
+        k = start + int(np.flatnonzero(W[n, start:])[0])  # first nonzero weight from start
+        p = 8 * ((k % 16) // 4) + [0, 1, 4, 5][k % 4]
+        wp[n, k // 16] = (int(wp[n, k // 16]) & ~(1 << p)) | (1 << (p + 2))
+        Wz[n, k] = 0
+    back, bad = oracle.unpack(wp, K)
+    assert bad == 3 and np.array_equal(back, Wz)
+    y, _ = oracle.linear_f64(wp, s, x, T, K, N)
+    np.testing.assert_allclose(y, _brute_linear(Wz, s, x), rtol=1e-12, atol=1e-15)
+    q, xs = oracle.quant_s8(x, T, K)
+    y8, _, acc = oracle.linear_s8(wp, s, q, xs, T, K, N, want_acc=True)
+    yb, accb = _brute_s8(Wz, s, q, xs)
+    assert np.array_equal(acc, accb)
+    np.testing.assert_allclose(y8, yb, rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------- base-3 packing
+
+def _t5_digits(v):
+    """The five base-3 digits of v, least significant first, from numpy's
+    own base conversion."""
+    return [int(d) for d in reversed(np.base_repr(v, 3).zfill(5))]
+
+
+def test_t5_golden_bytes():
+    for name, ws, byte in _read_fixture("t5_bytes.txt"):
+        w5 = [int(v) for v in ws.split(",")]
+        W = np.zeros((1, 128), dtype=np.int8)
+        W[0, 10:15] = w5  # byte 2 of the group holds weights 10..14
+        p, bad = oracle.pack_t5(W)
+        assert bad == 0 and p.shape == (1, 26)
+        assert int(p[0, 2]) == int(byte), name
+        assert all(int(b) == 121 for j, b in enumerate(p[0]) if j != 2), name
+        back, bad2 = oracle.unpack_t5(p, 128)
+        assert bad2 == 0 and np.array_equal(back, W), name
+
+
+def test_t5_closed_form_groups_and_padding():
+    # A group of 128 equal weights: 25 full bytes and a last byte holding
+    # three weights plus two padding digits written as weight 0 (digit 1).
+    for w, full, last in [(0, 121, 1 + 3 + 9 + 27 + 81),
+                          (-1, 0, 27 + 81),
+                          (1, 242, 2 + 6 + 18 + 27 + 81)]:
+        W = np.full((2, 256), w, dtype=np.int8)
+        p, _ = oracle.pack_t5(W)
+        rows = p.reshape(2, 2, 26)
+        assert np.all(rows[:, :, :25] == full), w
+        assert np.all(rows[:, :, 25] == last), w
+    # storage: 26 bytes and one fp16 scale per 128 weights = 1.75 bits per
+    # weight, the average the page gives for this format
+    assert (26 + 2) * 8 / 128 == 1.75
+
+
+def test_t5_unpack_every_byte_value_against_base_repr():
+    K = 256
+    for v in range(256):
+        p = np.full((1, 2 * 26), 121, dtype=np.uint8)  # all weights 0
+        p[0, 26 + 7] = v                               # group 1, byte 7: k = 163..167
+        W, bad = oracle.unpack_t5(p, K)
+        expect = np.zeros((1, K), dtype=np.int8)
+        if v <= 242:
+            expect[0, 163:168] = [d - 1 for d in _t5_digits(v)]
+            assert bad == 0, v
+        else:
+            assert bad == 1, v                         # invalid byte: weights read 0
+        assert np.array_equal(W, expect), v
+
+
+def test_t5_last_byte_ignores_padding_digits():
+    # digits 3 and 4 of byte 25 lie past the group: any value there leaves
+    # the group's weights unchanged
+    W = synth.ternary_weights(1, 128, 0.4, seed=64)
+    p, _ = oracle.pack_t5(W)
+    low = int(p[0, 25]) % 27
+    for pad in range(9):
+        q = p.copy()
+        q[0, 25] = low + 27 * pad
+        back, bad = oracle.unpack_t5(q, 128)
+        assert bad == 0 and np.array_equal(back, W), pad
+
+
+def test_t5_pack_counts_invalid_values():
+    W = np.zeros((1, 128), dtype=np.int8)
+    W[0, 0] = 3
+    W[0, 127] = -2
+    p, bad = oracle.pack_t5(W)
+    assert bad == 2 and np.all(p == 121)  # stored as weight 0
+
+
+def test_t5_round_trip_and_agreement_with_2bit_code():
+    N, K = 9, 640
+    W = synth.ternary_weights(N, K, 0.4, seed=65)
+    p, bad = oracle.pack_t5(W)
+    assert bad == 0 and p.shape == (N, 5 * 26)
+    back, bad2 = oracle.unpack_t5(p, K)
+    assert bad2 == 0 and np.array_equal(back, W)
+    wp, _ = oracle.pack(W)
+    back2, _ = oracle.unpack(wp, K)
+    assert np.array_equal(back, back2)
+
+
+@pytest.mark.parametrize("T,K,N", [(1, 128, 3), (3, 384, 4)])
+def test_t5_linear_f64_brute_force_and_equal_to_2bit(T, K, N):
+    W = synth.ternary_weights(N, K, 0.4, seed=66 + T)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=67)
+    x = synth.activations(T, K, seed=68, outlier_frac=0.02)
+    p, _ = oracle.pack_t5(W)
+    y, m = oracle.linear_f64(p, s, x, T, K, N)
+    np.testing.assert_allclose(y, _brute_linear(W, s, x), rtol=1e-12, atol=1e-15)
+    # the same weights in the 2-bit code give the same sums in the same order
+    wp, _ = oracle.pack(W)
+    y2, m2 = oracle.linear_f64(wp, s, x, T, K, N)
+    assert np.array_equal(y, y2) and np.array_equal(m, m2)
+    ti = np.array([T - 1, 0], dtype=np.int32)
+    ni = np.array([0, N - 1], dtype=np.int32)
+    ys, ms = oracle.linear_f64_sampled(p, s, x, K, N, ti, ni)
+    assert np.array_equal(ys, y[ti, ni]) and np.array_equal(ms, m[ti, ni])
+
+
+def test_t5_linear_s8_brute_force_and_equal_to_2bit():
+    T, K, N = 3, 256, 5
+    W = synth.ternary_weights(N, K, 0.4, seed=69)
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=70)
+    x = synth.activations(T, K, seed=71, outlier_frac=0.01)
+    p, _ = oracle.pack_t5(W)
+    q, xs = oracle.quant_s8(x, T, K)
+    y, m, acc = oracle.linear_s8(p, s, q, xs, T, K, N, want_acc=True)
+    yb, accb = _brute_s8(W, s, q, xs)
+    assert np.array_equal(acc, accb)
+    np.testing.assert_allclose(y, yb, rtol=1e-12, atol=1e-300)
+    wp, _ = oracle.pack(W)
+    y2, m2, acc2 = oracle.linear_s8(wp, s, q, xs, T, K, N, want_acc=True)
+    assert np.array_equal(y, y2) and np.array_equal(m, m2) and np.array_equal(acc, acc2)
+    ti = np.array([2, 0], dtype=np.int32)
+    ni = np.array([4, 1], dtype=np.int32)
+    ys, ms, accs = oracle.linear_s8_sampled(p, s, q, xs, K, N, ti, ni, want_acc=True)
+    assert np.array_equal(ys, y[ti, ni]) and np.array_equal(accs, acc[ti, ni])
+
+
+def test_t5_invalid_bytes_read_as_zero_in_both_rungs():
+    T, K, N = 2, 256, 2
+    W = synth.ternary_weights(N, K, 0.2, seed=72)
+    s = synth.scales_uniform(N, K, 0.01, 0.05, seed=73)
+    x = synth.activations(T, K, seed=74)
+    p, _ = oracle.pack_t5(W)
+    Wz = W.copy()
+    p[0, 3] = 243          # group 0, byte 3: k = 15..19
+    p[1, 26 + 25] = 255    # group 1, last byte: k = 253..255
+    Wz[0, 15:20] = 0
+    Wz[1, 253:256] = 0
+    back, bad = oracle.unpack_t5(p, K)
+    assert bad == 2 and np.array_equal(back, Wz)
+    y, _ = oracle.linear_f64(p, s, x, T, K, N)
+    np.testing.assert_allclose(y, _brute_linear(Wz, s, x), rtol=1e-12, atol=1e-15)
+    q, xs = oracle.quant_s8(x, T, K)
+    y8, _, acc = oracle.linear_s8(p, s, q, xs, T, K, N, want_acc=True)
+    yb, accb = _brute_s8(Wz, s, q, xs)
+    assert np.array_equal(acc, accb)
+    np.testing.assert_allclose(y8, yb, rtol=1e-12, atol=1e-300)
+
+
 # ---------------------------------------------------------------- generators
 
 def test_synth_distributions():
