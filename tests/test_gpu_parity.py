@@ -102,6 +102,46 @@ def test_pack_bit_exact_and_bad_count(tl):
     assert np.array_equal(packed_to_numpy(Wp), ref)
 
 
+@pytest.mark.parametrize("rung,T", [("gemv", 1), ("small_t", 5), ("small_t_tiled", 13), ("s8", 37)])
+def test_invalid_pairs_decode_as_zero(tl, rung, T):
+    """The header documents that the linear kernels read the invalid pair
+    (nz = 0, neg = 1) as weight 0; so does the oracle.  A quarter of the
+    nonzero weights are turned into that pair in the packed words."""
+    import torch
+    K, N = 1280, 300
+    case = synth.case("invalid", T, K=K, N=N, seed=81)
+    wp, _ = oracle.pack(case.W)
+    rng = np.random.default_rng(82)
+    nz = np.argwhere(case.W != 0)
+    pick = nz[rng.choice(len(nz), size=len(nz) // 4, replace=False)]
+    bit = 8 * ((pick[:, 1] % 16) // 4) + np.array([0, 1, 4, 5])[pick[:, 1] % 4]
+    words = wp[pick[:, 0], pick[:, 1] // 16]
+    np.bitwise_and.at(wp, (pick[:, 0], pick[:, 1] // 16),
+                      ~(np.uint32(1) << bit.astype(np.uint32)))
+    np.bitwise_or.at(wp, (pick[:, 0], pick[:, 1] // 16),
+                     np.uint32(1) << (bit + 2).astype(np.uint32))
+    assert not np.array_equal(wp[pick[:, 0], pick[:, 1] // 16], words)
+    Wz, bad = oracle.unpack(wp, K)
+    assert bad == len(pick)
+    assert np.array_equal(Wz, np.where(np.isin(np.arange(N * K).reshape(N, K),
+                                                pick[:, 0] * K + pick[:, 1]), 0, case.W))
+    _, s, x = to_device(case)
+    Wp = torch.from_numpy(wp.view(np.int32)).cuda()
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, s, x)
+        assert tl.tern_last_rung() == rung
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    y = y.cpu().numpy()
+    if rung == "s8":
+        q_ref, xs_ref = oracle.quant_s8(case.x, T, K)
+        y_ref, m, _ = oracle.linear_s8(wp, case.scales, q_ref, xs_ref, T, K, N)
+        assert_s8_parity(y, y_ref, m, f"invalid pairs rung={rung}")
+    else:
+        y_ref, m = oracle.linear_f64(wp, case.scales, case.x, T, K, N)
+        assert_bf16_parity(y, y_ref, m, f"invalid pairs rung={rung}")
+
+
 @pytest.mark.parametrize("T,K", [(1, 128), (17, 5120), (508, 6144), (3, 16)])
 def test_quant_s8_bit_exact(tl, T, K):
     import torch
