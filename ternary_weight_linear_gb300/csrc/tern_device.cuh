@@ -86,79 +86,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
-// Non-blocking probe of a phase (mbarrier.test_wait never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait that spins on test_wait: for a thread whose reaction time to the
-// phase completing matters more than the issue slots it spends polling.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_test_wait(bar, parity)) return true;
-  unsigned long long t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
-// mbar_wait with a non-blocking first probe: an already-complete phase costs
-// one test_wait (a try_wait issued right behind tcgen05 commits is slow to
-// return even then); an open phase is waited on with try_wait, which lets the
-// thread yield instead of flooding the barrier with probes.
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait(bar, parity, err);
-}
-
-// Warp-wide wait with a single polling lane: lane 0 waits, the result is
-// broadcast, and __syncwarp orders the other lanes' later accesses after
-// lane 0's acquire.  Keeps barrier traffic to one thread per waiting warp.
-// Every lane of the warp must call it.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-
-// Publish / observe a sequence number in shared memory with release /
-// acquire semantics at CTA scope (a hand-off between two threads that needs
-// no mbarrier operation on the observing side).
-__device__ __forceinline__ void seq_publish(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t seq_read(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-  return v;
-}
-// Spin until *p >= target.  Gives up after kWaitLimitNs: ORs kErrTimeout into
-// *err and returns false.
-__device__ __forceinline__ bool seq_wait(const uint32_t* p, uint32_t target, int* err) {
-  if (seq_read(p) >= target) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (seq_read(p) >= target) return true;
-    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
 // Wait until *ctr >= target (acquire, GPU scope).  Gives up after
 // kWaitLimitNs: ORs kErrTimeout into *err and returns false.
 __device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* ctr,
@@ -303,44 +230,6 @@ __device__ __forceinline__ uint32_t decode_e4m3(uint32_t v) {
   return (v << kShift) & 0xA0A0A0A0u;
 }
 
-// Same decode with the left shift done as an integer multiply by mul = 2^shift
-// held in a register the compiler cannot fold (mul[I] = 32, 16, 2, 1): the
-// multiply issues on the FMA pipe and the AND on the ALU pipe, so a stream of
-// decodes uses both pipes instead of two ALU slots per result.
-__device__ __forceinline__ uint32_t decode_e4m3_mul(uint32_t v, uint32_t mul) {
-  uint32_t p;
-  asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(p) : "r"(v), "r"(mul));
-  return p & 0xA0A0A0A0u;
-}
-
-// e4m3-decoded weights -> int8 w in natural byte order: for a packed word v,
-// out[b] holds w[4b .. 4b+3] (byte i of out[b] = w[4b + i]).
-// 4x4 byte transpose: out[b] byte i = in[i] byte b.
-__device__ __forceinline__ void transpose_bytes_4x4(const uint32_t in[4], uint32_t out[4]) {
-  const uint32_t a01 = __byte_perm(in[0], in[1], 0x5140);  // i0b0 i1b0 i0b1 i1b1
-  const uint32_t a23 = __byte_perm(in[2], in[3], 0x5140);
-  const uint32_t b01 = __byte_perm(in[0], in[1], 0x7362);  // i0b2 i1b2 i0b3 i1b3
-  const uint32_t b23 = __byte_perm(in[2], in[3], 0x7362);
-  out[0] = __byte_perm(a01, a23, 0x5410);
-  out[1] = __byte_perm(a01, a23, 0x7632);
-  out[2] = __byte_perm(b01, b23, 0x5410);
-  out[3] = __byte_perm(b01, b23, 0x7632);
-}
-
-__device__ __forceinline__ void decode_word_s8(uint32_t v, uint32_t out[4]) {
-  uint32_t t[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t r = i == 0 ? decode_e4m3<0>(v)
-                     : i == 1 ? decode_e4m3<1>(v)
-                     : i == 2 ? decode_e4m3<2>(v) : decode_e4m3<3>(v);
-    const uint32_t nz = (r >> 5) & 0x01010101u;
-    const uint32_t ng = (r >> 7) & nz;
-    t[i] = nz | (ng * 0xFEu);  // byte: 0, +1 (0x01) or -1 (0xFF); no carries
-  }
-  transpose_bytes_4x4(t, out);
-}
-
 // One lane of the (fully converged) warp is elected; returns true there.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
@@ -348,11 +237,6 @@ __device__ __forceinline__ bool elect_one() {
       "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(pred));
   return pred != 0;
-}
-
-// Named barrier over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -424,13 +308,6 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t r[4]) {
                : "r"(taddr)
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t r[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
-}
 // D[tmem] (+)= A[tmem] x B[smem desc]; kind::f8f6f4, cta_group::1.
 __device__ __forceinline__ void mma_f8f6f4_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,
                                               uint32_t idesc, bool accumulate) {
@@ -459,44 +336,4 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
-
-// ---------------------------------------------------------------- MMA
-__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_e4m3_16832(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_s8_16832(int d[4], const uint32_t a[4], uint32_t b0,
-                                             uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// Exact int -> float for |i| < 2^22 via the 1.5 * 2^23 bias.
-__device__ __forceinline__ float int_to_float_exact(int i) {
-  return __int_as_float(i + 0x4B400000) - 12582912.0f;
-}
-
 }  // namespace tern
