@@ -88,6 +88,10 @@ def _load():
         lib.tern_oracle_linear_t5_s8.restype = None
         lib.tern_oracle_linear_t5_s8_sampled.argtypes = [P, P, P, P, i32, i32, P, P, i64, P, P, P]
         lib.tern_oracle_linear_t5_s8_sampled.restype = None
+        lib.tern_oracle_f64_to_bf16.argtypes = [P, i64, P]
+        lib.tern_oracle_f64_to_bf16.restype = None
+        lib.tern_oracle_rotate.argtypes = [P, i32, i32, i32, P, P]
+        lib.tern_oracle_rotate.restype = None
         lib.tern_oracle_num_threads.argtypes = []
         lib.tern_oracle_num_threads.restype = i32
         _lib = lib
@@ -249,3 +253,22 @@ def linear_s8_sampled(wp, scales_f16, q, xs, K: int, N: int, t_idx, n_idx,
                                   _ptr(t_idx), _ptr(n_idx), cnt, _ptr(acc), _ptr(y),
                                   _ptr(m))
     return y, m, acc
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """fp64 values -> bf16 bits (uint16), round to nearest even in one step."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().tern_oracle_f64_to_bf16(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def rotate(x_bf16, T: int, K: int, block: int = 1024):
+    """Blockwise Hadamard rotation of bf16 activations [T, K]: returns
+    (exact fp64 [T, K], bf16 bits [T, K]).  block is a power of two dividing K."""
+    x = _u16(x_bf16)
+    assert x.size == T * K and block > 0 and block & (block - 1) == 0 and K % block == 0
+    exact = np.empty((T, K), dtype=np.float64)
+    xr = np.empty((T, K), dtype=np.uint16)
+    _load().tern_oracle_rotate(_ptr(x), T, K, block, _ptr(exact), _ptr(xr))
+    return exact, xr

@@ -48,10 +48,22 @@
  *    weight 0 and ignored on reading.  Bytes 243..255 are invalid.  The
  *    scales stay in their own [N][K/128] fp16 array, as for the 2-bit code.
  *
+ *  - Hadamard rotation of the activations in 1024-wide blocks, applied before
+ *    the layer ("NInfer sm_89 fork" write-up, section 9, item 2: the original
+ *    model's Hadamard rotation is fused into the activation quantisation; the
+ *    "ninfer-perf-tuning" skill page, section 6 budget table: the rotation
+ *    works on (1024-block, token) pairs of bf16 activations):
+ *        xr[t][bB + i] = B^(-1/2) * sum_j (-1)^popcount(i & j) x[t][bB + j]
+ *    in fp64 (exact for B = 1024, whose scale is 1/32, while the inputs' bits
+ *    span under 43 binary places), then rounded once to bf16, nearest-even.
+ *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - the 2-bit code is sign-magnitude with the bit order above;
  *  - the base-3 byte is a plain base-3 integer, least significant digit
  *    first, 26 bytes per group with padding digits for weight 0;
+ *  - the rotation matrix is the Sylvester (natural-order) Hadamard matrix,
+ *    orthonormalised by B^(-1/2); its output is rounded to bf16 once, and the
+ *    layer then runs on the rounded values exactly as without rotation;
  *  - an invalid code (the 2-bit pair (0, 1), a base-3 byte above 242) reads
  *    as weight 0 in every definition here, as the library documents for its
  *    kernels, and is counted by the unpack functions;
@@ -412,6 +424,69 @@ void tern_oracle_linear_t5_s8_sampled(const uint8_t* p, const uint16_t* scales,
   (void)N;
   linear_s8_sampled(read_t5, p, scales, q, xs, K, t_idx, n_idx, count, acc, y,
                     m);
+}
+
+/* ---- Hadamard rotation of the activations --------------------------------- */
+
+/* fp64 -> bf16 bits, round to nearest, ties to even, in one step from the
+ * double (no intermediate fp32).  From the format: sign, 8 exponent bits
+ * (bias 127), 7 fraction bits; normal values have 8 significant bits, values
+ * below 2^-126 are subnormal with quantum 2^-133; magnitudes that round to
+ * 2^128 or above become infinity. */
+static uint16_t f64_to_bf16(double d) {
+  if (isnan(d)) return 0x7FC0;
+  uint16_t sign = signbit(d) ? 0x8000 : 0;
+  double a = fabs(d);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a = m 2^e, 0.5 <= m < 1: the leading bit is worth 2^(e-1) */
+  int q = e - 8; /* quantum of an 8-significant-bit value */
+  if (q < -133) q = -133;
+  double r = rint(ldexp(a, -q)); /* integer multiple of the quantum, RNE */
+  double v = ldexp(r, q);
+  if (v >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+  float f = (float)v; /* exact: v is a bf16 value */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+void tern_oracle_f64_to_bf16(const double* v, long n, uint16_t* out) {
+  for (long i = 0; i < n; ++i) out[i] = f64_to_bf16(v[i]);
+}
+
+/* Popcount parity of i & j: the sign of entry (i, j) of the Sylvester
+ * Hadamard matrix is (-1)^parity. */
+static int hadamard_sign(int i, int j) {
+  unsigned v = (unsigned)(i & j);
+  int p = 0;
+  while (v) {
+    p ^= 1;
+    v &= v - 1u;
+  }
+  return p ? -1 : 1;
+}
+
+/* x: bf16 bits [T][K]; B: block width, a power of two dividing K.
+ *   exact[t][k] = B^(-1/2) * sum over the block of k of sign * x   (fp64)
+ *   xr[t][k]    = bf16 of exact[t][k]
+ * Either output may be NULL.  The sum over j runs in j order. */
+void tern_oracle_rotate(const uint16_t* x, int T, int K, int B, double* exact,
+                        uint16_t* xr) {
+  double norm = 1.0 / sqrt((double)B);
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int b = 0; b < K / B; ++b)
+      for (int i = 0; i < B; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < B; ++j)
+          acc += (double)hadamard_sign(i, j) *
+                 (double)bf16_to_f32(x[(size_t)t * K + (size_t)b * B + j]);
+        double v = acc * norm;
+        size_t o = (size_t)t * K + (size_t)b * B + i;
+        if (exact) exact[o] = v;
+        if (xr) xr[o] = f64_to_bf16(v);
+      }
 }
 
 int tern_oracle_num_threads(void) {

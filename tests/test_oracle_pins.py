@@ -479,6 +479,93 @@ def test_t5_invalid_bytes_read_as_zero_in_both_rungs():
     np.testing.assert_allclose(y8, yb, rtol=1e-12, atol=1e-300)
 
 
+# ---------------------------------------------------------------- rotation
+
+def test_f64_to_bf16_golden():
+    for name, val, bits in _read_fixture("bf16_round.txt"):
+        got = oracle.f64_to_bf16(np.array([float.fromhex(val)]))
+        assert int(got[0]) == int(bits, 16), name
+
+
+def _bf16_neighbours(d):
+    """The two bf16 values around a positive normal double d, by exact
+    rational arithmetic: the grid step is 2^(e-8) for d in [2^(e-1), 2^e)."""
+    m, e = math.frexp(d)
+    step = Fraction(2) ** (e - 8)
+    lo = (Fraction(d) // step) * step
+    return lo, lo + step, step
+
+
+def test_f64_to_bf16_random_against_exact_rationals():
+    rng = np.random.default_rng(91)
+    v = rng.standard_normal(4000) * np.exp2(rng.integers(-60, 60, size=4000))
+    got = synth.bf16_bits_to_f32(oracle.f64_to_bf16(v)).astype(np.float64)
+    for d, g in zip(v, got):
+        a = abs(float(d))
+        lo, hi, step = _bf16_neighbours(a)
+        dl, dh = Fraction(a) - lo, hi - Fraction(a)
+        if dl < dh:
+            want = lo
+        elif dh < dl:
+            want = hi
+        else:  # tie: the neighbour whose last fraction bit is 0
+            want = lo if (lo / step) % 2 == 0 else hi
+        assert Fraction(abs(float(g))) == want and np.sign(g) == np.sign(d), (d, g)
+
+
+@pytest.mark.parametrize("B", [2, 16, 64, 1024])
+def test_rotate_matches_scipy_hadamard(B):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    T, K = 3, 2048
+    x = synth.activations(T, K, seed=92, outlier_frac=0.01)
+    exact, xr = oracle.rotate(x, T, K, block=B)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    H = scipy_linalg.hadamard(B).astype(np.float64) / math.sqrt(B)
+    ref = (xf.reshape(T, K // B, B) @ H.T).reshape(T, K)
+    np.testing.assert_allclose(exact, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(xr, oracle.f64_to_bf16(exact))
+
+
+def test_rotate_closed_forms():
+    B, K = 1024, 2048
+    # one-hot input e_j in block 1: the output is column j of H / 32, exactly
+    for j in (0, 1, 5, 513, 1023):
+        xb = np.zeros((1, K), dtype=np.float32)
+        xb[0, B + j] = 1.0
+        exact, _ = oracle.rotate(_bf16_bits_exact(xb), 1, K)
+        signs = np.array([(-1) ** bin(i & j).count("1") for i in range(B)], dtype=np.float64)
+        assert not exact[0, :B].any()
+        assert np.array_equal(exact[0, B:], signs / 32.0), j
+    # a constant block of ones sums to 1024/32 = 32 in output 0 and cancels elsewhere
+    xb = np.zeros((1, K), dtype=np.float32)
+    xb[0, :B] = 1.0
+    exact, xr = oracle.rotate(_bf16_bits_exact(xb), 1, K)
+    assert exact[0, 0] == 32.0 and not exact[0, 1:].any()
+    assert int(xr[0, 0]) == 0x4200  # 32.0 in bf16
+
+
+def test_rotate_is_orthonormal_and_blockwise():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    T, K, B = 2, 3072, 1024
+    x = synth.activations(T, K, seed=93, outlier_frac=0.02)
+    exact, _ = oracle.rotate(x, T, K)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    # Parseval: the norm of each block is kept
+    np.testing.assert_allclose((exact.reshape(T, 3, B) ** 2).sum(-1),
+                               (xf.reshape(T, 3, B) ** 2).sum(-1), rtol=1e-12)
+    # rotating back with H / 32 returns the input
+    H = scipy_linalg.hadamard(B).astype(np.float64) / 32.0
+    back = (exact.reshape(T, 3, B) @ H.T).reshape(T, K)
+    np.testing.assert_allclose(back, xf, rtol=0, atol=1e-12)
+    # a change inside block 1 leaves blocks 0 and 2 bit-identical
+    x2 = x.copy()
+    x2[:, B + 7] ^= 0x0040
+    exact2, _ = oracle.rotate(x2, T, K)
+    assert np.array_equal(exact2[:, :B], exact[:, :B])
+    assert np.array_equal(exact2[:, 2 * B:], exact[:, 2 * B:])
+    assert not np.array_equal(exact2[:, B:2 * B], exact[:, B:2 * B])
+
+
 # ---------------------------------------------------------------- generators
 
 def test_synth_distributions():
