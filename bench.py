@@ -65,6 +65,8 @@ def parse_args():
     ap.add_argument("--profile-calls", type=int, default=3)
     ap.add_argument("--no-stack", action="store_true",
                     help="skip the 64-layer whole-stack passes")
+    ap.add_argument("--formats", action="store_true",
+                    help="only time the base-3 weight repack and the Hadamard rotation")
     return ap.parse_args()
 
 
@@ -547,9 +549,76 @@ def run_profile(args):
         sys.exit(1)
 
 
+def run_formats(args):
+    """Time tern_repack_t5 (gate+up stored as base-3 bytes) and tern_rotate_bf16
+    (T = 2048 x 17408 prefill activations, and a decode-sized T = 4 x 5120
+    call) with CUDA events.  Several input copies, each launch on the next, so
+    that the big launches read from HBM, not L2.  Prints one JSON line."""
+    import torch
+    import ternary_weight_linear_gb300 as tl
+
+    tl.build()
+    tl.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321)
+
+    def timed_us(fn, reps):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us": round(us, 3), "bytes": nbytes, "GB/s": round(gbs, 1),
+                "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+
+    out = {}
+    K, N = GU
+    copies = 4  # 4 x (36 MB in + 45 MB out)
+    P = [torch.randint(0, 243, (N, K // 128 * 26), dtype=torch.uint8, device=dev, generator=gen)
+         for _ in range(copies)]
+    Wp = [torch.empty((N, K // 16), dtype=torch.int32, device=dev) for _ in range(copies)]
+    us = timed_us(lambda i: tl.tern_repack_t5(P[i % copies], K, Wp[i % copies]), 40)
+    out["repack_t5_gate_up"] = entry(us, N * K // 128 * 26 + N * K // 4)
+    del P, Wp
+
+    T, Kr = 2048, DN[0]
+    copies = 3  # 3 x (71 MB in + 71 MB out)
+    xs = [torch.randn(T, Kr, device=dev, generator=gen).to(torch.bfloat16) for _ in range(copies)]
+    ys = [torch.empty_like(xs[0]) for _ in range(copies)]
+    us = timed_us(lambda i: tl.tern_rotate_bf16(xs[i % copies], ys[i % copies]), 40)
+    out["rotate_bf16_t2048_k17408"] = entry(us, 2 * T * Kr * 2)
+    del xs, ys
+
+    x4 = torch.randn(4, GU[0], device=dev, generator=gen).to(torch.bfloat16)
+    y4 = torch.empty_like(x4)
+    us = timed_us(lambda i: tl.tern_rotate_bf16(x4, y4), 200)
+    out["rotate_bf16_t4_k5120"] = {"us": round(us, 3),
+                                   "note": "eager calls from Python back to back: host-bound, "
+                                           "an upper bound on the kernel's time"}
+    status = tl.tern_device_status()
+    print(json.dumps({"formats": out, "peak_hbm_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind,
+                      "status": status}), flush=True)
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.formats:
+        run_formats(args)
+        return
     if args.profile:
         run_profile(args)
         return

@@ -95,6 +95,44 @@ int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count,
 int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T,
                       int K, void* stream);
 
+/* Convert base-3 packed weights (five per byte) to the 2-bit layout above.
+ *   Pt5      device uint8 [N][K/128][26], read-only.  Each 128-weight group
+ *            takes 26 bytes; byte j of a group holds the group's weights
+ *            5j .. 5j+4 as the base-3 number sum_i (w_i + 1) * 3^i, the first
+ *            weight least significant.  The last byte holds three weights;
+ *            its two upper digits are padding and are ignored.  Bytes above
+ *            242 are invalid: their weights are written as 0.
+ *   Wpacked  device uint32 [N][K/16], written
+ *   K, N     K > 0 and K % 128 == 0; N > 0
+ *   bad_count optional device int32; if not NULL, the number of invalid bytes
+ *            is ADDED to *bad_count.
+ * The scales keep their [N][K/128] fp16 array.  This is a one-time,
+ * memory-bound conversion for weights stored in the base-3 format; the
+ * linear kernels read the 2-bit layout.
+ * Format: "NInfer sm_89 fork" write-up, section 9 item 2 (base-3 codes,
+ * five weights per byte, one FP16 scale per 128 weights, 1.75 bits per
+ * weight: 26 bytes + 2 bytes of scale per 128 weights). */
+int tern_repack_t5(const uint8_t* Pt5, uint32_t* Wpacked, int K, int N,
+                   int* bad_count, void* stream);
+
+/* Blockwise Hadamard rotation of bf16 activations:
+ *   xr[t][1024 b + i] = bf16( 1/32 * sum_j (-1)^popcount(i & j) x[t][1024 b + j] )
+ * for each 1024-wide block b of each token t (the orthonormal Sylvester
+ * Hadamard matrix of order 1024), computed in fp32 and rounded to bf16 with
+ * round-to-nearest-even.  The result differs from the exact rotation rounded
+ * to bf16 by at most half a bf16 step plus the fp32 sum error bound
+ * 10 * 2^-24 * sum_j |x[t][1024 b + j]| / 32.
+ *   x        device bf16 [T][K], read-only
+ *   xr       device bf16 [T][K], written; may be x itself (in place),
+ *            otherwise it must not overlap x
+ *   T > 0, K > 0, K % 1024 == 0.
+ * Source: the Hadamard rotation that the "NInfer sm_89 fork" write-up
+ * (section 9 item 2) fuses into the activation quantisation, over the
+ * (1024-block, token) pairs of the "ninfer-perf-tuning" skill page's
+ * section 6 budget table. */
+int tern_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
+                     void* stream);
+
 /* Bytes of the synchronisation area at the start of every workspace. */
 #define TERN_SYNC_BYTES 4096u
 

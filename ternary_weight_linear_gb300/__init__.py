@@ -22,7 +22,8 @@ __all__ = [
     "tern_pack", "tern_quant_act_s8", "tern_linear", "tern_linear_workspace_bytes",
     "tern_select_rung", "tern_rung_name", "tern_last_rung", "tern_last_rung_id",
     "tern_reload_env", "tern_device_status", "tern_status_string", "TernError", "load",
-    "tern_linear_small_t_noalloc", "RUNGS", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES", "SYNC_BYTES",
+    "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16", "RUNGS",
+    "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES", "SYNC_BYTES", "T5_GROUP_BYTES", "ROTATION_BLOCK",
 ]
 
 RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8"}
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "tern_pack", "tern_quant_act_s8", "tern_linear_workspace_bytes", "tern_linear",
     "tern_select_rung", "tern_rung_name", "tern_last_rung_id", "tern_last_rung",
     "tern_status_string", "tern_reload_env", "tern_device_status",
-    "tern_linear_small_t_noalloc",
+    "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16",
 )
 
 # Size of the library's fixed scratch for tern_linear_small_t_noalloc.
@@ -40,6 +41,10 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 # Leading bytes of every workspace owned by the library (TERN_SYNC_BYTES):
 # zero before first use, then left alone.
 SYNC_BYTES = 4096
+# Base-3 bytes per 128-weight group (five weights per byte, rounded up).
+T5_GROUP_BYTES = 26
+# Width of the Hadamard rotation's blocks along K.
+ROTATION_BLOCK = 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -87,6 +92,10 @@ def load() -> ctypes.CDLL:
         lib.tern_device_status.restype = I
         lib.tern_linear_small_t_noalloc.argtypes = [P, P, P, P, I, I, I, P]
         lib.tern_linear_small_t_noalloc.restype = I
+        lib.tern_repack_t5.argtypes = [P, P, I, I, P, P]
+        lib.tern_repack_t5.restype = I
+        lib.tern_rotate_bf16.argtypes = [P, P, I, I, P]
+        lib.tern_rotate_bf16.restype = I
         _lib = lib
         return lib
 
@@ -140,6 +149,31 @@ def tern_pack(W: torch.Tensor, Wpacked: torch.Tensor | None = None,
     pb = _dev(bad_count, "bad_count", torch.int32) if bad_count is not None else None
     _check("tern_pack", load().tern_pack(pw, pp, K, N, pb, _stream(stream)))
     return Wpacked
+
+
+def tern_repack_t5(Pt5: torch.Tensor, K: int, Wpacked: torch.Tensor | None = None,
+                   bad_count: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """base-3 packed weights uint8 [N, K/128*26] (five weights per byte) ->
+    packed int32 [N, K/16] (uint32 bit patterns of the 2-bit layout)."""
+    N = Pt5.shape[0]
+    if Wpacked is None:
+        Wpacked = torch.empty((N, K // 16), dtype=torch.int32, device=Pt5.device)
+    pp = _dev(Pt5, "Pt5", torch.uint8, (N, K // 128 * T5_GROUP_BYTES))
+    pw = _dev(Wpacked, "Wpacked", torch.int32, (N, K // 16))
+    pb = _dev(bad_count, "bad_count", torch.int32) if bad_count is not None else None
+    _check("tern_repack_t5", load().tern_repack_t5(pp, pw, int(K), N, pb, _stream(stream)))
+    return Wpacked
+
+
+def tern_rotate_bf16(x: torch.Tensor, xr: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Blockwise (1024) Hadamard rotation of bf16 activations [T, K]; xr may be x."""
+    T, K = x.shape
+    if xr is None:
+        xr = torch.empty_like(x)
+    _check("tern_rotate_bf16", load().tern_rotate_bf16(
+        _dev(x, "x", torch.bfloat16), _dev(xr, "xr", torch.bfloat16, (T, K)), T, K,
+        _stream(stream)))
+    return xr
 
 
 def tern_quant_act_s8(x: torch.Tensor, q: torch.Tensor | None = None,

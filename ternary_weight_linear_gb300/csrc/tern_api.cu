@@ -310,6 +310,34 @@ int tern_pack(const int8_t* W, uint32_t* Wpacked, int K, int N, int* bad_count, 
              : TERN_ECUDA;
 }
 
+int tern_repack_t5(const uint8_t* Pt5, uint32_t* Wpacked, int K, int N, int* bad_count,
+                   void* stream) {
+  if (!Pt5 || !Wpacked || K <= 0 || N <= 0 || (K % 128) != 0) return TERN_EINVAL;
+  if (!aligned16(Pt5) || !aligned16(Wpacked)) return TERN_EALIGN;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  return launch_repack_t5(Pt5, Wpacked, K, N, bad_count, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TERN_OK
+             : TERN_ECUDA;
+}
+
+int tern_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K, void* stream) {
+  if (!x || !xr || T <= 0 || K <= 0 || (K % kRotBlock) != 0) return TERN_EINVAL;
+  if (!aligned16(x) || !aligned16(xr)) return TERN_EALIGN;
+  // in place, or no overlap at all
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(xr);
+  const uintptr_t bytes = static_cast<uintptr_t>(T) * static_cast<uintptr_t>(K) * 2u;
+  if (a != b && a < b + bytes && b < a + bytes) return TERN_EINVAL;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  return launch_rotate_bf16(x, xr, T, K, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TERN_OK
+             : TERN_ECUDA;
+}
+
 int tern_quant_act_s8(const uint16_t* x, int8_t* q, float* x_scale, int T, int K, void* stream) {
   if (!x || !q || !x_scale || T <= 0 || K <= 0 || (K % 16) != 0) return TERN_EINVAL;
   if (!aligned16(x) || !aligned16(q) || !aligned16(x_scale)) return TERN_EALIGN;

@@ -62,4 +62,12 @@ cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int 
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
                                 int K, cudaStream_t stream);
 
+// Base-3 packed weights (26 bytes per 128-weight group) -> 2-bit codes.
+cudaError_t launch_repack_t5(const uint8_t* P, uint32_t* Wp, int K, int N, int* bad,
+                             cudaStream_t stream);
+// Blockwise (1024) Hadamard rotation of bf16 activations; xr may equal x.
+constexpr int kRotBlock = 1024;
+cudaError_t launch_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
+                               cudaStream_t stream);
+
 }  // namespace tern

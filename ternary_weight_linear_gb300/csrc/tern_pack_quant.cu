@@ -1,6 +1,8 @@
 // tern_pack: int8 ternary weights -> 2-bit sign-magnitude codes.
+// tern_repack_t5: base-3 packed weights (five per byte) -> the same codes.
 // tern_quant_act_s8: per-token absmax/127 int8 quantisation of bf16 rows.
 // The s8 rung's own input: the same codes split into two exact fp8 pieces.
+// tern_rotate_bf16: blockwise Hadamard rotation of bf16 activations.
 #include "tern_device.cuh"
 #include "tern_internal.h"
 
@@ -155,6 +157,132 @@ __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t*
   }
 }
 
+// ---------------------------------------------------------------- base-3 repack
+// Base-3 layout: 26 bytes per 128-weight group, [N][K/128][26].  Byte j holds
+// the group's weights 5j .. 5j+4 as sum_i (w_i + 1) 3^i, the first weight
+// least significant; the last byte's digits 3 and 4 lie past the group.
+// Bytes above 242 are invalid and give five zero weights.
+constexpr int kT5GroupBytes = 26;
+constexpr int kRepackThreads = 256;  // one 128-weight group per thread
+
+// Each CTA stages the bytes of its kRepackThreads groups in shared memory
+// with 16-byte loads (the block's first byte sits at a multiple of
+// 256 * 26 = 6656 = 16 * 416 bytes), then each thread decodes one group into
+// the eight 2-bit words of that group and stores them as two 16-byte vectors.
+__global__ void __launch_bounds__(kRepackThreads) repack_t5_kernel(
+    const uint8_t* __restrict__ P, uint32_t* __restrict__ Wp, long long groups,
+    int* __restrict__ bad_count) {
+  __shared__ __align__(16) uint8_t stage[kRepackThreads * kT5GroupBytes];
+  const long long g0 = static_cast<long long>(blockIdx.x) * kRepackThreads;
+  const long long left = groups - g0;
+  const int here = left < kRepackThreads ? static_cast<int>(left) : kRepackThreads;
+  const int bytes = here * kT5GroupBytes;
+  const uint8_t* src = P + g0 * kT5GroupBytes;
+  for (int c = threadIdx.x; c < bytes / 16; c += kRepackThreads)
+    reinterpret_cast<uint4*>(stage)[c] = ldg_nc_v4(src + 16 * c);
+  for (int b = (bytes / 16) * 16 + threadIdx.x; b < bytes; b += kRepackThreads) stage[b] = src[b];
+  __syncthreads();
+
+  int bad = 0;
+  if (static_cast<int>(threadIdx.x) < here) {
+    const uint8_t* gb = stage + threadIdx.x * kT5GroupBytes;
+    uint32_t word[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < kT5GroupBytes; ++j) {
+      uint32_t v = gb[j];
+      if (v > 242u) {
+        ++bad;
+        v = 121u;  // digits 1,1,1,1,1: five zero weights
+      }
+#pragma unroll
+      for (int i = 0; i < 5; ++i) {
+        const int r = 5 * j + i;  // weight index in the group (compile-time)
+        const uint32_t d = v % 3u;
+        v /= 3u;
+        if (r < 128) {
+          // 2-bit code of w = d - 1: nonzero bit at P[r % 4] = {0, 1, 4, 5}
+          // of byte (r % 16) / 4 of word r / 16, negative bit two above
+          const int p = 8 * ((r % 16) / 4) + ((r % 4) < 2 ? (r % 4) : (r % 4) + 2);
+          word[r / 16] |= (static_cast<uint32_t>(d != 1u) << p) |
+                          (static_cast<uint32_t>(d == 0u) << (p + 2));
+        }
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(Wp + (g0 + threadIdx.x) * 8);
+    dst[0] = make_uint4(word[0], word[1], word[2], word[3]);
+    dst[1] = make_uint4(word[4], word[5], word[6], word[7]);
+  }
+  if (bad_count) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if ((threadIdx.x & 31) == 0 && bad) atomicAdd(bad_count, bad);
+  }
+}
+
+// ---------------------------------------------------------------- rotation
+// One warp per (token, 1024-block): lane l holds elements 32 l .. 32 l + 31 of
+// the block.  Index bits 0-4 are transformed inside the thread, bits 5-9
+// across lanes with shuffles; each butterfly (a, b) -> (a + b, a - b) in fp32
+// gives the natural-order (Sylvester) Hadamard transform.  Then * 1/32 (exact)
+// and one rounding to bf16, nearest-even.  Plain loads and stores: the block
+// is read whole before it is written, so xr may be x.
+constexpr int kRotWarps = 8;
+
+__global__ void __launch_bounds__(kRotWarps * 32) rotate_bf16_kernel(const uint16_t* x,
+                                                                    uint16_t* xr,
+                                                                    long long pairs) {
+  const long long w = static_cast<long long>(blockIdx.x) * kRotWarps + (threadIdx.x >> 5);
+  if (w >= pairs) return;  // whole warps leave together
+  const int lane = threadIdx.x & 31;
+  // x is [T][K] with K a multiple of 1024, so pair w starts at element 1024 w
+  const size_t base = static_cast<size_t>(w) * kRotBlock + static_cast<size_t>(lane) * 32;
+  const uint4* src = reinterpret_cast<const uint4*>(x + base);
+  float v[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 q = src[c];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * c + 2 * e] = __uint_as_float(u[e] << 16);
+      v[8 * c + 2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    const bool upper = (lane & h) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], h);
+      v[i] = upper ? o - v[i] : v[i] + o;
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(xr + base);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t u[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[8 * c + 2 * e] * 0.03125f));
+      const uint32_t hi =
+          __bfloat16_as_ushort(__float2bfloat16_rn(v[8 * c + 2 * e + 1] * 0.03125f));
+      u[e] = lo | (hi << 16);
+    }
+    dst[c] = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,
@@ -165,6 +293,23 @@ cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, i
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   pack_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(W, Wp, words, bad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_t5(const uint8_t* P, uint32_t* Wp, int K, int N, int* bad,
+                             cudaStream_t stream) {
+  const long long groups = static_cast<long long>(N) * (K / 128);
+  const long long blocks = (groups + kRepackThreads - 1) / kRepackThreads;
+  repack_t5_kernel<<<static_cast<unsigned>(blocks), kRepackThreads, 0, stream>>>(P, Wp, groups,
+                                                                                  bad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
+                               cudaStream_t stream) {
+  const long long pairs = static_cast<long long>(T) * (K / kRotBlock);
+  const long long blocks = (pairs + kRotWarps - 1) / kRotWarps;
+  rotate_bf16_kernel<<<static_cast<unsigned>(blocks), kRotWarps * 32, 0, stream>>>(x, xr, pairs);
   return cudaGetLastError();
 }
 

@@ -115,6 +115,14 @@ def test_invalid_arguments_are_rejected_before_device_work():
     assert lib.tern_linear(p + 2, p, p, p, 1, 128, 8, None, 0, None) == -2
     assert lib.tern_pack(p, p + 4, 16, 4, None, None) == -2
     assert lib.tern_quant_act_s8(p, p, p + 8, 1, 16, None) == -2
+    # base-3 repack: K % 128, null, misaligned
+    assert lib.tern_repack_t5(p, p, 64, 4, None, None) == -1
+    assert lib.tern_repack_t5(None, p, 128, 4, None, None) == -1
+    assert lib.tern_repack_t5(p + 2, p, 128, 4, None, None) == -2
+    # rotation: K % 1024, partial overlap of x and xr, misaligned
+    assert lib.tern_rotate_bf16(p, 1 << 20, 1, 512, None) == -1
+    assert lib.tern_rotate_bf16(p, p + 1024, 2, 1024, None) == -1
+    assert lib.tern_rotate_bf16(p, (1 << 20) + 8, 1, 1024, None) == -2
 
 
 def test_no_gpu_gives_enodev():
