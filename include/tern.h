@@ -220,6 +220,18 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
                                 const uint16_t* x, float* y, int T, int K, int N,
                                 void* stream);
 
+/* Diagnostic of the failure path.  Launches one small kernel whose bounded
+ * wait can never be satisfied, using the same wait code as the layer's
+ * kernels:
+ *   which = 0  an mbarrier phase that nothing completes
+ *   which = 1  a device counter that nothing raises
+ * After the wait limit (2 s) the kernel records the timeout in the device
+ * error word and returns: nothing faults or hangs, and the context stays
+ * usable.  tern_device_status() on the same stream then returns
+ * TERN_ETIMEOUT and clears the word.  which outside {0, 1}: TERN_EINVAL.
+ * For tests and health checks only; never needed on the layer's path. */
+int tern_selftest_wait_timeout(int which, void* stream);
+
 /* Rung the dispatcher picks for T (after env overrides).  Host-only. */
 int tern_select_rung(int T);
 

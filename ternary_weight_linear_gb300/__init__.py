@@ -22,7 +22,8 @@ __all__ = [
     "tern_pack", "tern_quant_act_s8", "tern_linear", "tern_linear_workspace_bytes",
     "tern_select_rung", "tern_rung_name", "tern_last_rung", "tern_last_rung_id",
     "tern_reload_env", "tern_device_status", "tern_status_string", "TernError", "load",
-    "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16", "RUNGS",
+    "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16",
+    "tern_selftest_wait_timeout", "RUNGS",
     "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES", "SYNC_BYTES", "T5_GROUP_BYTES", "ROTATION_BLOCK",
 ]
 
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "tern_select_rung", "tern_rung_name", "tern_last_rung_id", "tern_last_rung",
     "tern_status_string", "tern_reload_env", "tern_device_status",
     "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16",
+    "tern_selftest_wait_timeout",
 )
 
 # Size of the library's fixed scratch for tern_linear_small_t_noalloc.
@@ -96,6 +98,8 @@ def load() -> ctypes.CDLL:
         lib.tern_repack_t5.restype = I
         lib.tern_rotate_bf16.argtypes = [P, P, I, I, P]
         lib.tern_rotate_bf16.restype = I
+        lib.tern_selftest_wait_timeout.argtypes = [I, P]
+        lib.tern_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -264,6 +268,14 @@ def tern_last_rung_id() -> int:
 
 def tern_reload_env() -> None:
     load().tern_reload_env()
+
+
+def tern_selftest_wait_timeout(which: int, stream=None) -> None:
+    """Launch the failure-path diagnostic: a kernel whose bounded wait (0: an
+    mbarrier, 1: a device counter) runs out after 2 s and records the timeout;
+    tern_device_status then returns TERN_ETIMEOUT (-6)."""
+    _check("tern_selftest_wait_timeout",
+           load().tern_selftest_wait_timeout(int(which), _stream(stream)))
 
 
 def tern_device_status(stream=None) -> int:

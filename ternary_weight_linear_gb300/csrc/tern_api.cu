@@ -441,6 +441,17 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   return rc;
 }
 
+int tern_selftest_wait_timeout(int which, void* stream) {
+  if (which != 0 && which != 1) return TERN_EINVAL;
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != TERN_OK) return rc;
+  return launch_wait_timeout_probe(which, d->err, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TERN_OK
+             : TERN_ECUDA;
+}
+
 int tern_device_status(void* stream) {
   DevState* d = nullptr;
   int rc = device_state(&d);

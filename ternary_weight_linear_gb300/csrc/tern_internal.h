@@ -70,4 +70,9 @@ constexpr int kRotBlock = 1024;
 cudaError_t launch_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
                                cudaStream_t stream);
 
+// Diagnostic: one kernel whose bounded wait runs out (which = 0: an mbarrier
+// phase nobody completes; 1: a device counter nobody raises) and records the
+// timeout in *err.
+cudaError_t launch_wait_timeout_probe(int which, int* err, cudaStream_t stream);
+
 }  // namespace tern

@@ -123,6 +123,9 @@ def test_invalid_arguments_are_rejected_before_device_work():
     assert lib.tern_rotate_bf16(p, 1 << 20, 1, 512, None) == -1
     assert lib.tern_rotate_bf16(p, p + 1024, 2, 1024, None) == -1
     assert lib.tern_rotate_bf16(p, (1 << 20) + 8, 1, 1024, None) == -2
+    # failure-path diagnostic: only which = 0 or 1
+    assert lib.tern_selftest_wait_timeout(2, None) == -1
+    assert lib.tern_selftest_wait_timeout(-1, None) == -1
 
 
 def test_no_gpu_gives_enodev():
