@@ -6,6 +6,7 @@ TERN_ETIMEOUT from tern_device_status.  Here a diagnostic kernel runs the same
 wait code on a condition nothing ever meets (an mbarrier phase nobody
 completes, a device counter nobody raises).  The status must come back, be
 cleared by the read, and the context must still run the layer correctly.
+The file runs after the parity tests (its name sorts last).
 """
 import time
 
