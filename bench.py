@@ -67,6 +67,8 @@ def parse_args():
                     help="skip the 64-layer whole-stack passes")
     ap.add_argument("--formats", action="store_true",
                     help="only time the base-3 weight repack and the Hadamard rotation")
+    ap.add_argument("--sweep", action="store_true",
+                    help="only time every projection at every token count of the configs")
     return ap.parse_args()
 
 
@@ -613,9 +615,86 @@ def run_formats(args):
         sys.exit(1)
 
 
+SWEEP_T = (1, 2, 3, 4, 8, 9, 12, 16, 17, 508, 2048)
+L2_BYTES = 129 * 2 ** 20
+
+
+def run_sweep(args):
+    """Per-call time of the four projections at every token count of the
+    configs: T = 1..16 on the bandwidth rungs, T = 17, 508 and 2048 on s8.
+    Each (projection, T) is timed over enough distinct weight copies to exceed
+    4x L2, all calls captured in one CUDA graph that is replayed between CUDA
+    events.  Prints one JSON line."""
+    import torch
+    import ternary_weight_linear_gb300 as tl
+
+    tl.build()
+    tl.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(99)
+    rows = []
+    for name, (K, N) in (("gate_up", GU), ("down", DN), ("attn_in", AI), ("attn_out", AO)):
+        copies = -(-4 * L2_BYTES // weight_bytes(K, N))
+        layers = [make_layer(tl, torch, K, N, gen, dev) for _ in range(copies)]
+        for T in SWEEP_T:
+            x = make_x(torch, T, K, gen, dev)
+            ys = [torch.empty(T, N, device=dev) for _ in range(copies)]
+            ws = torch.zeros(tl.tern_linear_workspace_bytes(T, K, N), dtype=torch.uint8,
+                             device=dev)
+            stream = torch.cuda.Stream(device=dev)
+            stream.wait_stream(torch.cuda.current_stream())
+
+            def calls():
+                for (w, sc), y in zip(layers, ys):
+                    tl.tern_linear(w, sc, x, y, ws)
+
+            with torch.cuda.stream(stream):
+                calls()  # library set-up outside capture
+            torch.cuda.synchronize()
+            rung = tl.tern_last_rung()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    calls()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = 10
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+            gbs = algorithmic_bytes(T, K, N) / (us * 1e-6) / 1e9
+            tops = 2.0 * T * K * N / (us * 1e-6) / 1e12
+            rows.append({"proj": name, "K": K, "N": N, "T": T, "rung": rung, "copies": copies,
+                         "us_per_call": round(us, 3), "GB/s": round(gbs, 1),
+                         "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                         "int8_TOPS" if rung == "s8" else "TOPS": round(tops, 1),
+                         "frac_of_bf16_peak": round(tops / peaks["bf16_tflops"], 4)})
+            del g, x, ys, ws
+        del layers
+        torch.cuda.empty_cache()
+    status = tl.tern_device_status()
+    print(json.dumps({"sweep": rows, "peak_hbm_gbs": peaks["hbm_gbs"],
+                      "peak_bf16_tflops": peaks["bf16_tflops"], "peak_kind": peak_kind,
+                      "status": status}), flush=True)
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.formats:
         run_formats(args)
         return
