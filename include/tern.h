@@ -119,9 +119,11 @@ int tern_repack_t5(const uint8_t* Pt5, uint32_t* Wpacked, int K, int N,
  *   xr[t][1024 b + i] = bf16( 1/32 * sum_j (-1)^popcount(i & j) x[t][1024 b + j] )
  * for each 1024-wide block b of each token t (the orthonormal Sylvester
  * Hadamard matrix of order 1024), computed in fp32 and rounded to bf16 with
- * round-to-nearest-even.  The result differs from the exact rotation rounded
- * to bf16 by at most half a bf16 step plus the fp32 sum error bound
- * 10 * 2^-24 * sum_j |x[t][1024 b + j]| / 32.
+ * round-to-nearest-even.  Each output differs from the exact rotation by at
+ * most half a bf16 step plus the fp32 sum error bound
+ * 10 * 2^-24 * sum_j |x[t][1024 b + j]| / 32, so it is the exact value's own
+ * bf16 rounding except where that value lies within the sum bound of a
+ * rounding boundary.
  *   x        device bf16 [T][K], read-only
  *   xr       device bf16 [T][K], written; may be x itself (in place),
  *            otherwise it must not overlap x
