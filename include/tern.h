@@ -140,18 +140,26 @@ int tern_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
 
 /* Bytes of device workspace tern_linear needs for (T, K, N); the value covers
  * every rung: the synchronisation area, then for the s8 rung the int8 codes
- * split into two fp8 pieces (2 T K bytes) and the token scales, or the
- * activation blocks of the small-T rungs.
+ * split into two fp8 pieces (2 T K bytes) and the token scales, or for the
+ * small-T rungs the partial row sums of row blocks that two or more CTAs
+ * share and the activation blocks built per call.
  * Host-only; 0 for T < 1 or K < 1. */
 size_t tern_linear_workspace_bytes(int T, int K, int N);
 
 /* y = x W^T with group scales:
  *   y[t][n] = sum_g s[n][g] * sum_{k in g} w[n][k] * x[t][k]
- * on the bf16-activation rungs (T <= 16; |y - y_exact| within
- * 1e-3 * sum|s w x| + 1e-6), and on the s8 rung (T >= 17)
+ * on the bf16-activation rungs (T <= 16), and on the s8 rung (T >= 17)
  *   q, xs = tern_quant_act_s8(x)
  *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]   (exact integers)
  *   y[t][n]      = xs[t] * sum_g s[n][g] * acc[t][n][g]   (fp32).
+ * Precision of the bf16 rungs, for every finite input: every product
+ * s * w * x is formed exactly (each bf16 x is cut into three fp8 e5m2 pieces
+ * at a power-of-two scale per token and 128-group, exact for the elements
+ * within 21 binades of the group's largest; the rest are multiplied exactly
+ * on the CUDA cores), and only the fp32 sums round, far inside
+ * |y - y_exact| <= 1e-3 * sum|s w x| + 1e-6.  Groups whose values span more
+ * than 21 binades cost extra time (their leftovers are read twice).
+ * Results are bit-for-bit reproducible from call to call on every rung.
  *   Wpacked  device uint32 [N][K/16] (layout above), read-only
  *   scales   device fp16 [N][K/128], read-only
  *   x        device bf16 [T][K], read-only
@@ -160,20 +168,26 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  *   workspace, workspace_bytes: device scratch of at least
  *            tern_linear_workspace_bytes(T, K, N) bytes, 16-byte aligned
  *            (TERN_ENOSPACE if smaller).  Its first TERN_SYNC_BYTES bytes are
- *            a synchronisation area (a counter the CTAs of a launch use to
- *            order their updates of rows they share) owned by the library:
- *            zero it once before the workspace's first use (e.g. with
- *            cudaMemset), then leave it alone; every call that completes
- *            without a device-side error leaves it valid for the next.
- *            After TERN_ETIMEOUT from tern_device_status, zero it again.  The
- *            rest of the workspace is scratch whose contents on entry are
- *            ignored.  The workspace must not be used by anything else (nor
- *            by another tern_linear call) until the call's work on `stream`
- *            has finished.
+ *            a synchronisation area (ticket counters with which the CTAs of a
+ *            launch agree which of them adds up the rows they share; no CTA
+ *            ever waits for another) owned by the library: zero it once
+ *            before the workspace's first use (e.g. with cudaMemset), then
+ *            leave it alone; every call that completes without a device-side
+ *            error leaves it zeroed again.  After TERN_ETIMEOUT from
+ *            tern_device_status, zero it again.  The rest of the workspace is
+ *            scratch whose contents on entry are ignored.  The workspace must
+ *            not be used by anything else (nor by another tern_linear call)
+ *            until the call's work on `stream` has finished.
  * The small-T kernels use programmatic dependent launch: a kernel may start
- * (and warm L2 with its weights) while the previous kernel on the stream
- * finishes, but reads x / weights and writes y / the workspace only after it
- * has completed.
+ * while the previous kernel on the stream finishes, and it then already
+ * reads Wpacked and scales (never x) before that kernel has completed.  So
+ * Wpacked and scales must not be written by a kernel that launches its
+ * dependents early and may still be running; a kernel launched without
+ * programmatic dependent launch (any other library's kernel, and this
+ * library's tern_pack and tern_repack_t5) has completed before the next
+ * kernel starts.
+ * x, y and the workspace are touched only after the previous kernel has
+ * completed.
  * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
  * Every rung is correct for every T. */
 int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
@@ -181,7 +195,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of the fixed device scratch tern_linear_small_t_noalloc uses. */
-#define TERN_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define TERN_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* tern_linear for T = 1..16 without a caller workspace and without allocating.
  *
@@ -198,11 +212,12 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
  *
  * Scratch.  The call's workspace (the synchronisation area, partial sums and
  * activation blocks) lives in one file-scope device array of
- * TERN_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; every GPU that loads
+ * TERN_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library; every GPU that loads
  * the library holds it until the process exits.  A call whose workspace does
- * not fit returns TERN_ENOSPACE before any device work: K <= 257024 for
- * T = 1..8 and K <= 128000 for T = 9..16.  The call allocates nothing: no
- * cudaMalloc, no cudaFree, no allocating library routine.
+ * not fit returns TERN_ENOSPACE before any device work: K <= 479232 for
+ * T = 1..4, K <= 219136 for T = 5..8 and K <= 118784 for T = 9..16.  The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
  *
  * Set-up.  The first call on a device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress and performs the library's
@@ -226,7 +241,8 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
  * wait can never be satisfied, using the same wait code as the layer's
  * kernels:
  *   which = 0  an mbarrier phase that nothing completes
- *   which = 1  a device counter that nothing raises
+ *   which = 1  a device counter that nothing raises (a wait in global
+ *              memory, the form a wait on another CTA would take)
  * After the wait limit (2 s) the kernel records the timeout in the device
  * error word and returns: nothing faults or hangs, and the context stays
  * usable.  tern_device_status() on the same stream then returns

@@ -39,7 +39,7 @@ EXPORTED_SYMBOLS = (
 )
 
 # Size of the library's fixed scratch for tern_linear_small_t_noalloc.
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 8 << 20
 # Leading bytes of every workspace owned by the library (TERN_SYNC_BYTES):
 # zero before first use, then left alone.
 SYNC_BYTES = 4096

@@ -189,10 +189,10 @@ size_t s8_workspace_bytes(int T, int K) {
   return 2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
 }
 
-// Token tile for a rung, the tokens left and K: (TT, tokens in this launch).
-void small_t_tile(int rung, int left, int K, int* tt, int* take) {
+// Token tile for a rung, the tokens left, K and N: (TT, tokens in this launch).
+void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* take) {
   if (rung == TERN_RUNG_GEMV) {
-    *tt = K <= kSmallTT1MaxK ? 1 : 4;
+    *tt = smallt_gemv_tile(K, N, num_sms);
     *take = 1;
   } else if (rung == TERN_RUNG_SMALL_T) {
     *take = left < 8 ? left : 8;
@@ -206,24 +206,33 @@ void small_t_tile(int rung, int left, int K, int* tt, int* take) {
 // ws: workspace whose first kSyncBytes are the zeroed sync area.
 int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
                 float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st) {
-  CUtensorMap maps[17];
-  bool have[17] = {};
+  CUtensorMap tmW;
+  int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
+                       static_cast<uint64_t>(K) / 4, 128, smallt_rows(1),
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TERN_OK) return rc;
   for (int tok0 = 0; tok0 < T;) {
     int tt = 0, take = 0;
-    small_t_tile(rung, T - tok0, K, &tt, &take);
-    if (!have[tt]) {
-      int rc = make_map_u8(&maps[tt], Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
-                           static_cast<uint64_t>(K) / 4, 128, smallt_rows(tt),
-                           CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc != TERN_OK) return rc;
-      have[tt] = true;
-    }
-    if (launch_smallt(tt, &maps[tt], s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
+    small_t_tile(rung, T - tok0, K, N, d->sms, &tt, &take);
+    if (launch_smallt(tt, &tmW, Wp, s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
                       tok0, take, d->sms, d->err, st) != cudaSuccess)
       return TERN_ECUDA;
     tok0 += take;
   }
   return TERN_OK;
+}
+
+// Scratch of tern_linear_small_t_noalloc for T tokens and K, for any (N,
+// device): at T = 1 the call may run on the one-token or the four-token tile.
+size_t noalloc_need(int T, int K) {
+  size_t w;
+  if (T == 1) {
+    const size_t a = smallt_work_bytes(1, K), b = smallt_work_bytes(4, K);
+    w = a > b ? a : b;
+  } else {
+    w = smallt_work_bytes(T <= 4 ? 4 : (T <= 8 ? 8 : 16), K);
+  }
+  return kSyncBytes + w;
 }
 
 // Device address of g_noalloc_scratch on the current device, looked up once
@@ -423,9 +432,7 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   if (!aligned16(Wpacked) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
     return TERN_EALIGN;
   const int rung = T == 1 ? TERN_RUNG_GEMV : T <= 8 ? TERN_RUNG_SMALL_T : TERN_RUNG_SMALL_T_TILED;
-  int tt = 0, take = 0;
-  small_t_tile(rung, T, K, &tt, &take);
-  if (kSyncBytes + smallt_work_bytes(tt, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
+  if (noalloc_need(T, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;

@@ -13,29 +13,37 @@ namespace tern {
 constexpr int kSTStageK = 1024;  // 256 packed bytes per row: two 128-byte TMA boxes
 // Grid cap of the small-T kernel (one CTA per SM).
 constexpr int kSmallTMaxCtas = 160;
-// Largest K of the one-token kernel (its activation blocks stay in shared
-// memory); a one-token call with larger K runs on the four-token tile.
-constexpr int kSmallTT1MaxK = 24576;
+// Most activation blocks the one-token kernel keeps resident in shared memory
+// (one per distinct k stage a CTA visits); a one-token call that needs more
+// runs on the four-token tile.
+constexpr int kSmallTX1MaxSlots = 16;
 
 // Workspace layout shared by all rungs: a synchronisation area of kSyncBytes
-// that must hold zeros when a call starts (the small-T kernels leave it zeroed
-// again), followed by the rung's scratch.
+// (the small-T kernels' ticket counters, one int per CTA, which must hold
+// zeros when a call starts; every call leaves them zeroed again), followed by
+// the rung's scratch.
 constexpr size_t kSyncBytes = 4096;
-static_assert(kSmallTMaxCtas * 4 * sizeof(int) <= kSyncBytes, "sync area");
+static_assert(kSmallTMaxCtas * sizeof(int) <= kSyncBytes, "sync area");
 
-// Partial-sum scratch of a TT tile: [kSmallTMaxCtas][2][TT][128] fp32.
+// Partial row sums of a TT tile's row blocks split between CTAs:
+// [kSmallTMaxCtas][2][TT][128] fp32.
 size_t smallt_partials_bytes(int tt);
-// Scratch after the sync area for a TT tile and K: partial sums, then (TT > 1)
-// the activation blocks built by the prep kernel.
+// Scratch after the sync area for a TT tile and K: the partial sums, then
+// (TT > 1) the activation blocks built by the prep kernel.
 size_t smallt_work_bytes(int tt, int K);
 // Rows per CTA row block (the TMA box height).
 int smallt_rows(int tt);
+// Token tile of a T = 1 call: 1 when the one-token kernel's resident
+// activation blocks fit for (K, N) on num_sms SMs, else 4.
+int smallt_gemv_tile(int K, int N, int num_sms);
 cudaError_t smallt_set_attributes();
 // Launch the small-T kernel(s) for tokens [tok0, tok0 + Tt) with Tt <= tt.
-// sync: the zeroed sync area; work: smallt_work_bytes(tt, K) bytes.
-cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales,
-                          const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
-                          int tok0, int Tt, int num_sms, int* err, cudaStream_t stream);
+// tmW: Wp's tensor map; sync: the zeroed sync area; work:
+// smallt_work_bytes(tt, K) bytes.
+cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
+                          const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int* err,
+                          cudaStream_t stream);
 
 // s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.
 constexpr int kS8TileN = 128;

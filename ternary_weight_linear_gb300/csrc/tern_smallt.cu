@@ -8,36 +8,47 @@
 // fp32 lane-ops per weight at full HBM rate; a CUDA-core or mma.sync GEMV
 // spends more than that on decode and fragment traffic alone).
 //
-// 1. Activation split.  Per token and per 128-wide group, x is scaled by a
-//    power of two 2^p so that the group's absmax lies in [128, 256), then
-//    split exactly into two fp8 e4m3 pieces x 2^p = h1 + h2
-//    (h1 = RN_e4m3(x 2^p), h2 = RN_e4m3(x 2^p - h1)).  A bf16 value has 8
-//    significant bits and each piece holds 4, so the split is exact for every
-//    element within 2^-10 of its group's absmax; smaller ones keep an
-//    absolute error below 2^-10 * 2^-p.  The pieces are the columns of the
-//    MMA's B operand (column piece * H + token) in the tcgen05 K-major
-//    shared-memory layout, one block per 1024-wide k stage, with the
-//    per-(group, token) factors f = 2^(3-p).  At T = 1 four warps of the
-//    main kernel build the blocks of every stage the CTA visits once, into
-//    shared memory where they stay (a compact layout: see kX1Lbo); for wider
-//    token tiles a prep kernel builds all blocks once per call and the main
-//    kernel copies each stage's block in with its weights.
+// 1. Activation pieces.  Per token and per 128-wide group, x is scaled by a
+//    power of two 2^p so that the group's absmax m lies in [2^14, 2^15), and
+//    split into three fp8 e5m2 pieces
+//        v = x 2^p,  h1 = RN(v),  h2 = RN(v - h1),  h3 = RN(v - h1 - h2).
+//    A bf16 value has 8 significant bits and an e5m2 value 3, and each
+//    rounding leaves a remainder at most half a step of the piece it rounds
+//    to; so for every element whose exponent is at least that of m minus 21
+//    (its scaled value at least 2^-7, its last bit at least 2^-14)
+//    h1 + h2 + h3 == v exactly, and every nonzero piece is a normal e5m2.
+//    Smaller nonzero elements ("leftovers", |x| < 2^-21 of m's binade) get no
+//    pieces; the group's factor is stored negated, and the fold adds their
+//    products exactly on the CUDA cores (leftover_dot), reading the group's
+//    packed weights and x again.  With bf16 activations this happens only in
+//    groups whose values span more than 21 binades.  The pieces are the
+//    columns of the MMA's B operand in the tcgen05 K-major shared-memory
+//    layout, one block per 1024-wide k stage, with the per-(group, token)
+//    factors f = 2^(3-p).  At T = 1 four warps of the main kernel build the
+//    blocks of every stage the CTA visits once, into shared memory where they
+//    stay (a compact layout: see kX1Lbo); for wider token tiles a prep kernel
+//    builds all blocks once per call and the main kernel copies each stage's
+//    block in with its weights.
 // 2. Weights as fp8, decoded into tensor memory.  The packed code puts each
 //    weight's nonzero bit and sign bit at the 2^-3 exponent bit and the sign
 //    bit of an e4m3 byte once shifted, so one shift and one AND turn a packed
 //    word into four exact e4m3 values w/8.  Decode threads own rows of the
 //    CTA's 128-row block (one TMEM lane each) and store decoded row chunks
 //    with tcgen05.st into the A operand in TMEM.
-// 3. One thread issues tcgen05.mma kind::f8f6f4 (A in TMEM, B in shared
-//    memory, fp32 accumulator in TMEM), one 128 x N x 128 accumulator per
-//    128-wide group; fold threads read it back with tcgen05.ld and fold it
-//    into their row's running sums with s[n][g] * f[g][token].
+// 3. tcgen05.mma kind::f8f6f4 (A e4m3 in TMEM, B e5m2 in shared memory, fp32
+//    accumulator in TMEM): every product w/8 * piece is exact.  Fold threads
+//    read the accumulators back with tcgen05.ld and fold the pieces' sums
+//    into their row's running sums with s[n][g] * f[g][token].  The only
+//    roundings are the fp32 sums.
 //
 // Pipeline (one CTA per SM, persistent; TMEM 512 columns):
 //   warp 16    producer: two 2D TMA boxes of packed weights (128 rows x 128 B
 //              each, 128-byte swizzle) per stage into the weight ring (plus,
 //              for T > 1, a bulk copy of the stage's activation block); the
-//              stage's fp16 scales (cp.async) into a longer scale ring;
+//              stage's fp16 scales (cp.async) into a longer scale ring.  The
+//              weights and scales of the first stages are requested before
+//              the previous kernel on the stream has finished (they are not
+//              written by it); activations only after.
 //   warps 19-22 (T = 1) build the resident activation blocks and factors;
 //   warps 0-7  decode (four groups of 32 rows per warp) into A slots;
 //   warps 17-18 issue the MMAs of half-stage 0 / 1 of every stage once its
@@ -49,12 +60,11 @@
 // Work split: the (row block, 1024-wide k stage) units are cut into equal
 // contiguous ranges, one per CTA, so every SM streams the same bytes.  A row
 // block whole inside one CTA is written to y directly.  A row block split
-// between CTAs is summed with fp32 atomics into y: at its start every CTA
-// zeroes the y rows of its split row blocks and counts itself in the
-// workspace's arrival counter, and it adds into y only once the counter
-// shows that all CTAs of the launch have zeroed (by then, in practice, long
-// since true).  The atomics make the order of those few additions, and so
-// the last bits of split rows, vary from run to run.
+// between CTAs is reduced without waiting on other CTAs: each CTA writes its
+// partial row sums to the workspace and takes a ticket; the CTA that arrives
+// last adds every partial in CTA order and writes y.  The result does not
+// depend on which CTA finishes last, so every output is reproducible bit for
+// bit, and no CTA ever waits for another to be scheduled.
 //
 // A stage is 1024 k: two 128-byte weight boxes per row, eight groups; a
 // half-stage is one box, four groups.  TMEM is used in half-stage slots: the
@@ -62,16 +72,15 @@
 // the MMAs of a half-stage write their own D slot, so decode, MMA and fold
 // can run half-stages apart; each A slot is filled and released in two
 // halves (groups 0-1, 2-3), so a half-stage's MMAs overlap the decoding of
-// its next use.  (Doubling the stage from 512 k halved every role's barrier
-// hand-offs per byte, which bound the pipeline.)
+// its next use.
 //
 // Calls chain by programmatic dependent launch: every kernel lets the next one
-// launch as soon as all of its CTAs run; the next kernel's CTAs set up, warm
-// L2 with their first weight tiles and wait for the previous grid before they
-// read anything it may have written (weights, x) or write y / the workspace.
-// Every ring of slots has an even length, so a slot only ever holds
-// half-stages of one parity (one decode half, one MMA issuer, one fold half):
-// a waiter's barrier is then never two phases behind it.
+// launch as soon as all of its CTAs run; the next kernel's CTAs set up, load
+// their first weight stages and wait for the previous grid before they read
+// anything it may have written (x) or write y / the workspace.  Every ring of
+// slots has an even length, so a slot only ever holds half-stages of one
+// parity (one decode half, one MMA issuer, one fold half): a waiter's barrier
+// is then never two phases behind it.
 //
 // The pages' kernel for this band (the "small_t" rung of the
 // "ninfer-perf-tuning" skill page, sections 2 and 6) decodes through a LUT
@@ -90,39 +99,54 @@ namespace {
 constexpr int kRows = 128;       // rows per CTA row block (MMA M, TMEM lanes)
 constexpr int kDecWarps = 8;     // two decode threads per row (groups split in halves)
 // Two fold threads per row: fold warp f owns TMEM lane quarter f % 4 and
-// half-stage f / 4 (groups 2 (f / 4), 2 (f / 4) + 1) of every stage.
+// half-stage f / 4 (groups 4 (f / 4) .. 4 (f / 4) + 3) of every stage.
 constexpr int kFoldWarps = 8;
 constexpr int kProducerWarp = kDecWarps + kFoldWarps;
 // Two MMA-issuing warps: the first issues half-stage 0 of every stage, the
 // second half-stage 1, so a single issuing thread never paces the tensor pipe.
 constexpr int kMmaWarp = kProducerWarp + 1;
 constexpr int kMmaWarps = 2;
-constexpr int kXWarp0 = kMmaWarp + kMmaWarps;  // (T = 1) activation warps, one per group
+constexpr int kXWarp0 = kMmaWarp + kMmaWarps;  // activation warps (T = 1) / split-row warp
 constexpr int kGS = kSTStageK / 128;       // 128-wide groups per stage
 constexpr int kGH = kGS / 2;               // groups per half-stage
 constexpr int kWBoxes = kSTStageK / 512;   // 128-byte TMA boxes per stage row
 static_assert(kGH == 4 && kWBoxes * 4 == kGS, "a half-stage is one weight box");
 constexpr uint32_t kXLbo = 128;            // K-direction core-matrix stride in the B block
-constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (one stage of k)
-// T = 1 activation block of one stage: only B columns 0 (h1) and 8 (h2) carry
-// data.  With a 16-byte K-direction stride, column r of a core matrix aliases
-// column 0 of the core matrix r steps further along K, so each piece needs a
-// single row of one byte per k (plus 112 bytes of overrun): the other 14
-// accumulator columns receive shifted dot products that are never read.
-constexpr uint32_t kX1Lbo = 16;
-constexpr uint32_t kX1Sbo = kSTStageK + 128;  // h2 row
-constexpr int kX1Stage = 2 * kX1Sbo;          // bytes per stage (h1 row, h2 row, overruns)
-constexpr int kX1MaxStages = kSmallTT1MaxK / kSTStageK;
+constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (8 columns of one stage)
+// T = 1 activation block of one stage, for an N = 16 MMA.  With a 32-byte
+// K-direction core-matrix stride, columns 0 and 1 of each 8-column group are
+// two interleaved byte rows and column c + 2 aliases column c one core
+// matrix further along K; so three pieces need only the clean columns 0, 1
+// (first group: h1, h2) and 8 (second group: h3), one byte per k each (plus
+// an overrun that the never-read columns 2-7 / 9-15 reach).
+constexpr uint32_t kX1Lbo = 32;
+constexpr uint32_t kX1Sbo = kSTStageK / 16 * 32 + 128;  // second 8-column group
+constexpr int kX1Stage = 2 * kX1Sbo;                    // bytes per stage block
+static_assert(kX1Sbo >= kSTStageK / 16 * 32 + 7 * 16, "the junk columns' overrun stays inside");
 
 template <int TT>
 struct TC {
-  static constexpr int kH = TT <= 8 ? 8 : 16;  // B columns per piece
-  static constexpr int kNC = 2 * kH;           // MMA N: 16 or 32
-  static constexpr int kXFrag = kNC * kSTStageK;  // B operand of one k stage
-  static constexpr int kXF = kGS * kH * 4;        // f[group][kH] fp32
-  static constexpr int kXBytes = kXFrag + kXF;    // one stage block of the prep buffer
-  static constexpr bool kInKernelX = TT == 1;     // x blocks built by the main kernel
-  static constexpr int kXWarps = kInKernelX ? 4 : 0;  // two groups of every stage each
+  // Token slots of the B operand and MMA N (= accumulator columns per group).
+  //   TT = 1:  compact block, pieces in columns 0, 1, 8; N = 16.
+  //   TT = 4:  piece j of token t in column 4 j + t (12 of 16); N = 16.
+  //   TT = 8:  pieces 0, 1 in columns 8 j + t (N = 16); piece 2 in a block of
+  //            its own (columns 0-7, 8-15 zero) whose N = 16 MMA accumulates
+  //            onto the same accumulator columns as piece 0.
+  //   TT = 16: pieces 0, 1 in columns 16 j + t (N = 32); piece 2 as for 8.
+  static constexpr int kH = TT;
+  static constexpr int kNC = TT <= 8 ? 16 : 32;
+  static constexpr bool kH3 = TT >= 8;
+  static constexpr int kP1 = TT == 1 ? 1 : (TT == 4 ? 4 : TT);  // piece 1's column offset
+  static constexpr int kP2 = TT == 1 ? 8 : 8;                    // piece 2's (TT <= 4)
+  static constexpr int kXMain = kNC * kSTStageK;                 // main B block of a stage
+  static constexpr int kXFrag = kXMain + (kH3 ? 16 * kSTStageK : 0);  // + piece-2 block
+  // per (group, token): the factor f, then the leftovers' sum of |x| L
+  static constexpr int kXF = 2 * kGS * kH * 4;                   // f[group][kH], L[group][kH]
+  static constexpr int kXBytes = kXFrag + kXF;                   // one stage of the prep buffer
+  static constexpr bool kInKernelX = TT == 1;                    // x blocks built by the main kernel
+  // (T = 1) activation warps, two groups of every stage each; the first of
+  // them (the only one for T > 1) then sums the CTA's split row blocks
+  static constexpr int kXWarps = kInKernelX ? 4 : 1;
   static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
   // TMEM is used in half-stage slots (kGH groups): A slots of kGH x 32
   // columns (e4m3), D slots of kGH x kNC columns.
@@ -135,7 +159,7 @@ struct TC {
   static constexpr int kNAH = 2;
   static constexpr int kNDH = TT <= 8 ? 4 : 2;
   static_assert(kNAH % 2 == 0 && kNDH % 2 == 0, "slot rings must not mix half-stage parities");
-  static constexpr int kStages = TT == 1 ? 4 : 3;  // weight (+ activation) ring
+  static constexpr int kStages = TT == 1 ? 4 : (TT == 16 ? 2 : 3);  // weight (+ activation) ring
   // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
   // ring does not wait for the MMAs, so the fold must never wait for scales).
   static constexpr int kLead = kInKernelX ? 2 : 0;
@@ -143,23 +167,22 @@ struct TC {
   // by up to (kNAH + kNDH) / 2 stages
   static constexpr int kSStages = kStages + kLead + (kNAH + kNDH + 1) / 2;
   static constexpr int kWBytes = kRows * kSTStageK / 4;  // kWBoxes boxes of 128 rows x 128 B
-  static constexpr int kSBytes = kRows * 2 * kGS + (kInKernelX ? 0 : kXF);  // scales [128][kGS], f
+  static constexpr int kSBytes = kRows * 2 * kGS + (kInKernelX ? 0 : kXF);  // scales [128][kGS], f, L
   static constexpr int kWOff = 0;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kXOff = kWOff + kStages * kWBytes;  // activation ring (T > 1)
   static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
-  static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) f[stage][4]
-  static constexpr int kBarOff = kFOff + (kInKernelX ? kX1MaxStages * kGS * 4 : 0);
-  static constexpr int kNumBars =
-      2 * kStages + 2 * kSStages + 4 * kNAH + 2 * kNDH + 8 + (kInKernelX ? kX1MaxStages : 0);
+  static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) (f, L)[slot][kGS]
+  static constexpr int kBarOff = kFOff + (kInKernelX ? kSmallTX1MaxSlots * kGS * 8 : 0);
+  static constexpr int kNumBars = 2 * kStages + 2 * kSStages + 4 * kNAH + 2 * kNDH + 8 + 2 +
+                                  (kInKernelX ? kSmallTX1MaxSlots : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
-  static constexpr int kFirstOff = kTmemSlot + 16;  // fold: parked first row block sums
-  static constexpr int kPartOff = kFirstOff + TT * kRows * 4;  // fold: half-stage 1 sums
+  static constexpr int kPartOff = kTmemSlot + 16;  // fold: half-stage 1 sums [TT][128]
   static constexpr int kX1Off = (kPartOff + TT * kRows * 4 + 127) / 128 * 128;  // (T = 1)
-  // shared memory for K: fixed part, the T = 1 blocks, alignment slack
-  static constexpr int smem_bytes(int KS) {
-    return kX1Off + (kInKernelX ? KS * kX1Stage : 0) + 1024;
+  // shared memory for nslots resident T = 1 blocks: fixed part, blocks, alignment slack
+  static constexpr int smem_bytes(int nslots) {
+    return kX1Off + (kInKernelX ? nslots * kX1Stage : 0) + 1024;
   }
-  static constexpr int kAllocMax = smem_bytes(kInKernelX ? kX1MaxStages : 0);
+  static constexpr int kAllocMax = smem_bytes(kInKernelX ? kSmallTX1MaxSlots : 0);
   static constexpr uint32_t kASlot = kGH * 32;     // A[kNAH] slots
   static constexpr uint32_t kDSlot = kGH * kNC;    // D[kNDH] slots
   static constexpr uint32_t kACol = 0;
@@ -171,25 +194,125 @@ struct TC {
   static_assert(kAllocMax <= 227 * 1024, "shared memory");
 };
 
-// x 2^p -> (h1, h2), two e4m3 pieces with h1 + h2 == x 2^p for |x 2^p| < 256
-// (up to the e4m3 resolution of the remainder, see above).
-__device__ __forceinline__ void split_e4m3(float xs, uint8_t& h1, uint8_t& h2) {
-  const __nv_fp8_storage_t a = __nv_cvt_float_to_fp8(xs, __NV_SATFINITE, __NV_E4M3);
-  const float af = __half2float(__half(__nv_cvt_fp8_to_halfraw(a, __NV_E4M3)));
-  h1 = a;
-  h2 = __nv_cvt_float_to_fp8(xs - af, __NV_SATFINITE, __NV_E4M3);
+// Instruction descriptor for kind::f8f6f4 with A e4m3 and B e5m2, fp32
+// accumulator, both operands K-major.
+constexpr uint32_t idesc_e4m3_e5m2_f32(int M, int N) {
+  return idesc_e4m3_f32(M, N) | (1u << 10);  // B type field (bits 10-12): e5m2
 }
 
-// Power-of-two exponent p with m 2^p in [128, 256), and f = 2^(3-p); 0 / 0 for m = 0.
-__device__ __forceinline__ void group_exponent(float m, int& p, float& f) {
-  p = 0;
-  f = 0.f;
-  if (m > 0.f) {
-    int e;
-    (void)frexpf(m, &e);  // m = fr * 2^e, fr in [0.5, 1)
-    p = 8 - e;
-    f = ldexpf(1.0f, 3 - p);
+// Scales of a group with absmax m > 0 (finite): el = floor(log2 m); the
+// pieces are cut from v = x 2^p with p = 14 - el, applied as two normal
+// powers of two sc1 * sc2 (p may exceed the fp32 exponent range of one
+// factor); the fold factor is f = 2^(3 - p) = 2^(el - 11) (w enters the MMA
+// as w/8).
+__device__ __forceinline__ void piece_band(float m, float& sc1, float& sc2, float& f) {
+  const uint32_t mb = __float_as_uint(m);
+  const int el = (mb >> 23) ? static_cast<int>(mb >> 23) - 127 : (31 - __clz(mb)) - 149;
+  const int p = 14 - el;               // in [-113, 147]
+  const int p1 = p >> 1, p2 = p - p1;  // each in [-57, 74]
+  sc1 = __uint_as_float(static_cast<uint32_t>(p1 + 127) << 23);
+  sc2 = __uint_as_float(static_cast<uint32_t>(p2 + 127) << 23);
+  f = el - 11 >= -126 ? __uint_as_float(static_cast<uint32_t>(el - 11 + 127) << 23)
+                      : ldexpf(1.0f, el - 11);  // a subnormal power of two, still exact
+}
+
+// Below this magnitude an element of the group is a leftover (2^(el - 21));
+// computed the same way from |f| by the prep and by the fold.
+__device__ __forceinline__ float leftover_limit(float f_abs) { return f_abs * 0x1p-10f; }
+
+__device__ __forceinline__ float2 e5m2x2_to_float2(__nv_fp8x2_storage_t a) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E5M2);
+  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+}
+
+// Three e5m2 pieces of two scaled values (low byte: v.x, high byte: v.y).
+__device__ __forceinline__ void split3_e5m2(float2 v, uint32_t& h1, uint32_t& h2, uint32_t& h3) {
+  const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E5M2);
+  const float2 af = e5m2x2_to_float2(a);
+  const float2 r1 = make_float2(v.x - af.x, v.y - af.y);
+  const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(r1, __NV_SATFINITE, __NV_E5M2);
+  const float2 bf = e5m2x2_to_float2(b);
+  const float2 r2 = make_float2(r1.x - bf.x, r1.y - bf.y);
+  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(r2, __NV_SATFINITE, __NV_E5M2);
+  h1 = a;
+  h2 = b;
+  h3 = c;
+}
+
+// Pieces of one lane's four consecutive elements of a group (bf16 bits in
+// raw), given the group's absmax m (already reduced over the warp).  Byte i of
+// h1/h2/h3 is element i's piece; returns f, negated when some element of the
+// group (any lane) is a leftover, and in lsum the sum of the leftovers' |x|
+// over the group (0 without leftovers).  Must be called by the whole warp.
+__device__ __forceinline__ float group_pieces(uint2 raw, float m, uint32_t& h1, uint32_t& h2,
+                                              uint32_t& h3, float& lsum) {
+  const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+  h1 = h2 = h3 = 0u;
+  lsum = 0.f;
+  if (m == 0.f) return 0.f;  // warp-uniform
+  float sc1, sc2, f;
+  piece_band(m, sc1, sc2, f);
+  const float tau = leftover_limit(f);
+  bool left = false;
+  float s[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool lo = v[i] != 0.f && fabsf(v[i]) < tau;
+    left |= lo;
+    lsum += lo ? fabsf(v[i]) : 0.f;
+    s[i] = lo ? 0.f : (v[i] * sc1) * sc2;
   }
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t a, b, c;
+    split3_e5m2(make_float2(s[2 * hf], s[2 * hf + 1]), a, b, c);
+    h1 |= a << (16 * hf);
+    h2 |= b << (16 * hf);
+    h3 |= c << (16 * hf);
+  }
+  if (!__any_sync(0xffffffffu, left)) {
+    lsum = 0.f;
+    return f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  return -f;
+}
+
+// The exact part of one group's dot product that the pieces leave out: the sum
+// of w[n][k] * x[k] over the group's elements with 0 < |x| < tau, in fp32
+// (every product is exact).  wp: packed weights, row n, group grp; xg: the
+// group's 128 bf16 values.  Kept out of line: only groups whose values span
+// more than 21 binades call it.
+__device__ __noinline__ float leftover_dot(const uint32_t* __restrict__ wp,
+                                           const uint16_t* __restrict__ xg, int K, int n, int grp,
+                                           float tau) {
+  const uint4* wq = reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 4) + grp * 8);
+  const uint4 wa = ldg_nc_v4(wq), wb = ldg_nc_v4(wq + 1);
+  uint4 xq[16];  // all loads in flight at once
+#pragma unroll
+  for (int i = 0; i < 16; ++i) xq[i] = ldg_nc_v4(xg + 8 * i);
+  const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // word j: k = 16 j .. 16 j + 15 of the group
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 xv = xq[2 * j + c];
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int kw = 8 * c + e;  // weight kw of the word: byte kw / 4, position kw % 4
+        const int bit = 8 * (kw >> 2) + ((kw & 3) < 2 ? (kw & 3) : (kw & 3) + 2);
+        const float xf = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
+        const bool nz = (w[j] >> bit) & 1u;
+        const bool neg = (w[j] >> (bit + 2)) & 1u;
+        if (nz && xf != 0.f && fabsf(xf) < tau) acc += neg ? -xf : xf;
+      }
+    }
+  }
+  return acc;
 }
 
 // CTA owning unit u when U units are cut into P equal contiguous ranges
@@ -218,47 +341,107 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
   const int gi = task % groups;
   const int ks = gi / kGS, jg = gi % kGS;
   const int kbase = gi * 128 + 4 * lane;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  if (t < Tt && kbase < K) {
-    const uint2 raw =
-        *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
-    v[0] = __uint_as_float(raw.x << 16);
-    v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(raw.y << 16);
-    v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-  }
+  uint2 raw = make_uint2(0u, 0u);
+  if (t < Tt && kbase < K)
+    raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
+  const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
   float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  int p;
-  float f;
-  group_exponent(m, p, f);
+  uint32_t hp[3];
+  float lsum;
+  const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
   uint8_t* st = out + static_cast<size_t>(ks) * C::kXBytes;
+  auto put = [&](uint8_t* blk, int n, int slot, uint8_t b) {
+    blk[(n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15)] = b;
+  };
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint8_t hp[2];
-    split_e4m3(ldexpf(v[i], p), hp[0], hp[1]);
     // k = 4 lane + i: 16-block lane/4, position b = lane%4, i -> slot 4i + b
     const int slot = 128 * jg + 16 * (lane >> 2) + 4 * i + (lane & 3);
-#pragma unroll
-    for (int piece = 0; piece < 2; ++piece) {
-      const int n = piece * C::kH + t;
-      const int off = (n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15);
-      st[off] = hp[piece];
+    const uint8_t b0 = static_cast<uint8_t>(hp[0] >> (8 * i));
+    const uint8_t b1 = static_cast<uint8_t>(hp[1] >> (8 * i));
+    const uint8_t b2 = static_cast<uint8_t>(hp[2] >> (8 * i));
+    put(st, t, slot, b0);
+    put(st, C::kP1 + t, slot, b1);
+    if constexpr (C::kH3) {
+      put(st + C::kXMain, t, slot, b2);
+      if constexpr (TT == 8) put(st + C::kXMain, 8 + t, slot, 0);  // the block's idle columns
+    } else {
+      put(st, C::kP2 + t, slot, b2);
     }
   }
-  if (lane == 0) reinterpret_cast<float*>(st + C::kXFrag)[jg * C::kH + t] = f;
+  if (lane == 0) {
+    float* fl = reinterpret_cast<float*>(st + C::kXFrag);
+    fl[jg * C::kH + t] = f;
+    fl[(kGS + jg) * C::kH + t] = lsum;
+  }
 }
 
 // ------------------------------------------------------------------ main
-// x: bf16 activations (read at T = 1); xprep: prep blocks (T > 1).
-// arrivals: the workspace's launch-arrival counter (see the fold warps).
+// The units of one CTA in visiting order.  The CTA's contiguous range of
+// units is visited in order, except that when its last row block is shared
+// with the next CTA, that row block's units (its first `head` stages) come
+// first: then both of the CTA's shared row blocks are finished early, and
+// their sums are combined while the rest of the range streams.
+struct Visit {
+  int KS;      // k stages per row block
+  int rb0;     // row block of the range's first unit, and its stage
+  int ks0;
+  int rbh;     // the last row block, visited first when head > 0
+  int head;    // units of rbh visited first (0: plain order)
+  int nunits;  // units in the range
+};
+
+// (row block, stage) of the unit at visit position v, stepped incrementally.
+struct Cursor {
+  int rb, ks, v;
+  __device__ __forceinline__ void start(const Visit& s) {
+    v = 0;
+    rb = s.head ? s.rbh : s.rb0;
+    ks = s.head ? 0 : s.ks0;
+  }
+  __device__ __forceinline__ void next(const Visit& s) {
+    if (++v == s.head) {
+      rb = s.rb0;
+      ks = s.ks0;
+    } else if (++ks == s.KS) {
+      ks = 0;
+      ++rb;
+    }
+  }
+  // this CTA's last unit of row block rb
+  __device__ __forceinline__ bool ends_row_block(const Visit& s) const {
+    return v == s.nunits - 1 || v == s.head - 1 || (v >= s.head && ks == s.KS - 1);
+  }
+};
+
+// (T = 1) The CTA visits min(nunits, KS) distinct stages, a cyclic run from
+// ks0; stage ks keeps its activation block in slot (ks - ks0) mod KS.
+__device__ __forceinline__ int stage_slot(const Visit& s, int ks) {
+  return ks >= s.ks0 ? ks - s.ks0 : ks + s.KS - s.ks0;
+}
+// The i-th distinct stage in visiting order: the head's stages 0 .. head-1,
+// then the rest of the cyclic run from ks0 without them.
+__device__ __forceinline__ int new_stage(const Visit& s, int i) {
+  if (i < s.head) return i;
+  const int j = i - s.head;
+  if (s.ks0 >= s.head) return j < s.KS - s.ks0 ? s.ks0 + j : s.head + j - (s.KS - s.ks0);
+  return s.head + j;
+}
+
+// wp: the packed weights (read again only for leftovers); x: bf16 activations
+// (read at T = 1, and for leftovers); xprep: prep blocks (T > 1).
+// tickets / partials: the workspace's ticket counters (one per CTA) and
+// partial row sums of split row blocks.  nslots: T = 1 resident blocks.
 template <int TT>
 __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
-    smallt_kernel(const __grid_constant__ CUtensorMap tmW, const uint16_t* __restrict__ scales,
-                  const uint16_t* __restrict__ x, const uint8_t* __restrict__ xprep,
-                  float* __restrict__ y, unsigned long long* __restrict__ arrivals, int K, int N,
-                  int tok0, int Tt, int KS, long long U, int* err) {
+    smallt_kernel(const __grid_constant__ CUtensorMap tmW, const uint32_t* __restrict__ wp,
+                  const uint16_t* __restrict__ scales, const uint16_t* __restrict__ x,
+                  const uint8_t* __restrict__ xprep, float* __restrict__ y,
+                  int* __restrict__ tickets, float* __restrict__ partials, int K, int N, int tok0,
+                  int Tt, int KS, int nslots, long long U, int* err) {
   using C = TC<TT>;
   constexpr int S = C::kStages;
   constexpr int SS = C::kSStages;
@@ -285,13 +468,16 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   uint64_t* afree = afull + 2 * NA;  // MMAs reading A sub-slot completed
   uint64_t* mdone = afree + 2 * NA;  // MMAs writing D slot d completed
   uint64_t* dfree = mdone + ND;   // D slot d read back by the fold warps
-  uint64_t* xready = dfree + ND;  // (T = 1) activation block of stage ks built
   // fold pairs: [quarter] the half-stage-1 warp's row block sums are in
   // shared memory / have been taken by the half-stage-0 warp
-  uint64_t* pfull = xready + (C::kInKernelX ? kX1MaxStages : 0);
+  uint64_t* pfull = dfree + ND;
   uint64_t* pfree = pfull + 4;
+  // [i] the four writing fold warps have published their partial sums of the
+  // CTA's i-th split row block
+  uint64_t* pub = pfree + 4;
+  uint64_t* xready = pub + 2;  // (T = 1) activation block of slot q built
   uint8_t* xres = smem + C::kX1Off;                              // (T = 1) blocks
-  float* ftab = reinterpret_cast<float*>(smem + C::kFOff);       // (T = 1) f[ks][kGS]
+  float2* ftab = reinterpret_cast<float2*>(smem + C::kFOff);     // (T = 1) (f, L)[slot][kGS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -317,12 +503,13 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       mbar_init(&mdone[d], 1);
       mbar_init(&dfree[d], kFoldWarps / 2);  // the four warps of its half-stage
     }
-    if constexpr (C::kInKernelX)
-      for (int k = 0; k < KS; ++k) mbar_init(&xready[k], kGS);  // one arrival per group
     for (int q = 0; q < 4; ++q) {
       mbar_init(&pfull[q], 1);
       mbar_init(&pfree[q], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&pub[i], 4);  // the four half-stage-0 fold warps
+    if constexpr (C::kInKernelX)
+      for (int q = 0; q < nslots; ++q) mbar_init(&xready[q], kGS);  // one arrival per group
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -336,39 +523,44 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   const int cta = blockIdx.x;
   const long long begin = U * cta / P;
   const long long end = U * (cta + 1) / P;
-  const int nunits = static_cast<int>(end - begin);
-  // first unit's (row block, k stage); later ones advance incrementally
-  const int rb0 = static_cast<int>(begin / KS);
-  const int ks0 = static_cast<int>(begin - static_cast<long long>(rb0) * KS);
-  // Every role but the producer (which first warms L2) waits for the previous
-  // grid here, so that no bounded wait below starts its clock while a slow
-  // predecessor is still running.
+  Visit vs;
+  vs.KS = KS;
+  vs.nunits = static_cast<int>(end - begin);
+  vs.rb0 = static_cast<int>(begin / KS);
+  vs.ks0 = static_cast<int>(begin - static_cast<long long>(vs.rb0) * KS);
+  vs.rbh = static_cast<int>((end - 1) / KS);
+  {
+    const int ke = static_cast<int>(end - static_cast<long long>(vs.rbh) * KS);
+    vs.head = (vs.rbh != vs.rb0 && ke < KS) ? ke : 0;  // the last row block is shared
+  }
+  const int nunits = vs.nunits;
+  const int rb0 = vs.rb0, ks0 = vs.ks0;
+  auto is_split = [&](int rb) {
+    const long long u = static_cast<long long>(rb) * KS;
+    return owner_of(u, U, P) != owner_of(u + KS - 1, U, P);
+  };
+  // The CTA's split row blocks in the order the fold finishes them: the head
+  // (the last row block), then the first row block (when shared).
+  int sp[2];
+  int nsp = 0;
+  if (vs.head) sp[nsp++] = vs.rbh;
+  if (is_split(rb0)) sp[nsp++] = rb0;  // (with head == 0 the last row block is not shared)
+
+  // Every role but the producer (which first requests the weights of its
+  // first stages) waits for the previous grid here, so that no bounded wait
+  // below starts its clock while a slow predecessor is still running.
   if (warp != kProducerWarp) grid_dependency_wait();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Warm L2 with the first stages' weights and the first row block's
-    // scales while the previous grid finishes; load only after it has.
-    if (lane == 0) {
-      int rb = rb0, ks = ks0;
-      for (int it = 0; it < nunits && it < S; ++it) {
-#pragma unroll
-        for (int b = 0; b < kWBoxes; ++b)
-          tma_prefetch_2d(&tmW, ks * (kSTStageK / 4) + 128 * b, rb * kRows);
-        if (++ks == KS) {
-          ks = 0;
-          ++rb;
-        }
-      }
-      const int rows = N - rb0 * kRows < kRows ? N - rb0 * kRows : kRows;
-      const uint32_t sbytes = (static_cast<uint32_t>(rows) * G * 2) & ~15u;
-      if (sbytes) bulk_prefetch_l2(scales + static_cast<size_t>(rb0) * kRows * G, sbytes);
-    }
-    grid_dependency_wait();
     // Scale stream: unit su's fp16 scales of groups kGS ks .. kGS ks + kGS - 1
-    // for rows lane + 32 i (and, T > 1, its factors f), into scale ring slot
-    // su % SS.
-    int su = 0, srb = rb0, sks = ks0;
+    // for rows lane + 32 i, into scale ring slot su % SS; for T > 1 the
+    // unit's factors f and leftover sums L come with them (expected here,
+    // copied by issue_f once the previous grid, which may have written them,
+    // has finished).
+    int su = 0;
+    Cursor cs;
+    cs.start(vs);
     auto issue_scales = [&]() -> bool {
       const int ss = su % SS;
       if (su >= SS &&
@@ -376,21 +568,17 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         return false;
       uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
       if constexpr (!C::kInKernelX) {
-        if (lane == 0) {
-          mbar_expect_tx(&sfull[ss], C::kXF);
-          bulk_load(sst + kRows * 2 * kGS,
-                    xprep + static_cast<size_t>(sks) * C::kXBytes + C::kXFrag, C::kXF,
-                    &sfull[ss]);
-        }
+        if (lane == 0) mbar_expect_tx(&sfull[ss], C::kXF);
+        __syncwarp();
       }
       uint4* sb = reinterpret_cast<uint4*>(sst);
-      const int g0 = sks * kGS;
+      const int g0 = cs.ks * kGS;
       if ((G % kGS) == 0) {
         // whole 16-byte rows of scales
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
-          const int n = srb * kRows + r;
+          const int n = cs.rb * kRows + r;
           const bool in = n < N;
           cp_async_16(&sb[r], scales + static_cast<size_t>(in ? n : 0) * G + g0, in ? 16u : 0u);
         }
@@ -401,7 +589,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
-          const int n = srb * kRows + r;
+          const int n = cs.rb * kRows + r;
           const bool in = n < N;
           const uint16_t* src = scales + static_cast<size_t>(in ? n : 0) * G + g0;
           cp_async_8(&sb[r], src, in ? 8u : 0u);
@@ -413,7 +601,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kRows / 32; ++i) {
           const int r = lane + 32 * i;
-          const int n = srb * kRows + r;
+          const int n = cs.rb * kRows + r;
           uint32_t hv[kGS];
 #pragma unroll
           for (int j = 0; j < kGS; ++j) hv[j] = 0u;
@@ -428,35 +616,85 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         mbar_arrive(&sfull[ss]);
       }
       ++su;
-      if (++sks == KS) {
-        sks = 0;
-        ++srb;
-      }
+      cs.next(vs);
       return true;
     };
-    bool ok = true;
-    while (ok && su < nunits && su < C::kLead) ok = issue_scales();
-    int it = 0;
-    int rb = rb0, ks = ks0;
-    for (; it < nunits && ok; ++it) {
+    // (T > 1) the factors of scale unit fu, whose stage is fks
+    auto issue_f = [&](int fu, int fks) {
+      if constexpr (!C::kInKernelX) {
+        if (lane == 0)
+          bulk_load(smem + C::kSOff + (fu % SS) * C::kSBytes + kRows * 2 * kGS,
+                    xprep + static_cast<size_t>(fks) * C::kXBytes + C::kXFrag, C::kXF,
+                    &sfull[fu % SS]);
+      }
+    };
+    // weights of unit it (stage ks of row block rb) into ring slot it % S; the
+    // barrier also expects the stage's activation block (T > 1)
+    auto issue_weights = [&](int it, int rb, int ks) {
       const int s = it % S;
-      if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
       if (lane == 0) {
-        // activations are resident at T = 1; for T > 1 the stage's block comes along
         mbar_arrive_expect_tx(&full[s], C::kWBytes + (C::kInKernelX ? 0 : C::kXFrag));
 #pragma unroll
         for (int bx = 0; bx < kWBoxes; ++bx)
           tma_load_2d(smem + C::kWOff + s * C::kWBytes + bx * (kRows * 128), &tmW,
                       ks * (kSTStageK / 4) + 128 * bx, rb * kRows, &full[s]);
-        if constexpr (!C::kInKernelX)
-          bulk_load(smem + C::kXOff + s * C::kXFrag,
-                    xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXFrag, &full[s]);
       }
+    };
+    auto issue_x = [&](int it, int ks) {
+      if constexpr (!C::kInKernelX) {
+        if (lane == 0)
+          bulk_load(smem + C::kXOff + (it % S) * C::kXFrag,
+                    xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXFrag, &full[it % S]);
+      }
+    };
+    auto prefetch_unit = [&](int rb, int ks) {
+      if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < kWBoxes; ++b)
+          tma_prefetch_2d(&tmW, ks * (kSTStageK / 4) + 128 * b, rb * kRows);
+      }
+    };
+    // Weights and scales are not written by the previous kernels of the
+    // stream's chain, so the first stages are requested before its end.
+    bool ok = true;
+    const int first = nunits < S ? nunits : S;
+    while (ok && su < nunits && su < C::kLead) ok = issue_scales();
+    int it = 0;
+    Cursor cw;
+    cw.start(vs);
+    for (; it < first && ok; ++it) {
+      issue_weights(it, cw.rb, cw.ks);
       if (su < nunits) ok = issue_scales();
-      if (++ks == KS) {
-        ks = 0;
-        ++rb;
+      cw.next(vs);
+    }
+    const int su_early = su;
+    // L2 prefetch of the next S units: with it, twice the ring's bytes are on
+    // their way from DRAM while the ring waits for the decoders.
+    Cursor cp = cw;
+    for (; cp.v < nunits && cp.v < it + S; cp.next(vs)) prefetch_unit(cp.rb, cp.ks);
+    grid_dependency_wait();
+    if constexpr (!C::kInKernelX) {
+      Cursor ce;
+      ce.start(vs);
+      for (int j = 0; j < su_early; ++j, ce.next(vs)) {
+        if (j < it) issue_x(j, ce.ks);
+        issue_f(j, ce.ks);
       }
+    }
+    for (; it < nunits && ok; ++it) {
+      const int s = it % S;
+      if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
+      issue_weights(it, cw.rb, cw.ks);
+      issue_x(it, cw.ks);
+      if (cp.v < nunits) prefetch_unit(cp.rb, cp.ks);
+      if (su < nunits) {
+        const int fks = cs.ks;
+        const int fu = su;
+        ok = issue_scales();
+        if (ok) issue_f(fu, fks);
+      }
+      cw.next(vs);
+      cp.next(vs);
     }
     // Stay until this CTA's copies have landed (bounded).
     for (int d = (it > S ? it - S : 0); d < it; ++d)
@@ -465,12 +703,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (!mbar_wait(&sfull[d % SS], (d / SS) & 1, err)) break;
   } else if (warp >= kXWarp0) {
     // ------------------------------------------------------------ activations (T = 1)
-    // Activation warp xw builds groups xw and xw + 4 of every stage this CTA
-    // visits, in visiting order, once: lane l splits k = 128 g + 4l .. +3 of
-    // the stage.  Item qi is group xw + 4 (qi & 1) of the (qi >> 1)-th stage.
+    // Activation warp xw builds groups xw and xw + 4 of every distinct stage
+    // the CTA visits, in visiting order, once: lane l splits k = 128 g + 4l ..
+    // +3 of the stage.  Item qi is group xw + 4 (qi & 1) of the (qi >> 1)-th
+    // distinct stage.
     if constexpr (C::kInKernelX) {
       const int xw = warp - kXWarp0;
-      grid_dependency_wait();
       const uint16_t* xt = x + static_cast<size_t>(tok0) * K;
       const int nq = nunits < KS ? nunits : KS;
       const int nitems = 2 * nq;
@@ -478,10 +716,10 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       constexpr int kXLoads = 8;
       uint2 raw[kXLoads];
       auto load_item = [&](int qi) -> uint2 {
-        const int ks = (ks0 + (qi >> 1)) % KS;
+        if (qi >= nitems) return make_uint2(0, 0);
+        const int ks = new_stage(vs, qi >> 1);
         const int k = ks * kSTStageK + 128 * (xw + 4 * (qi & 1)) + 4 * lane;
-        return (qi < nitems && k < K) ? *reinterpret_cast<const uint2*>(xt + k)
-                                      : make_uint2(0, 0);
+        return k < K ? *reinterpret_cast<const uint2*>(xt + k) : make_uint2(0, 0);
       };
 #pragma unroll
       for (int j = 0; j < kXLoads; ++j) raw[j] = load_item(j);
@@ -490,53 +728,94 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         for (int j = 0; j < kXLoads; ++j) {
           const int qi = q0 + j;
           if (qi >= nitems) break;
-          const int ks = (ks0 + (qi >> 1)) % KS;
+          const int q = stage_slot(vs, new_stage(vs, qi >> 1));
           const int g = xw + 4 * (qi & 1);
           const uint2 cur = raw[j];
           raw[j] = load_item(qi + kXLoads);
-          const float v[4] = {__uint_as_float(cur.x << 16), __uint_as_float(cur.x & 0xFFFF0000u),
-                              __uint_as_float(cur.y << 16), __uint_as_float(cur.y & 0xFFFF0000u)};
-          float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+          float m = fmaxf(fmaxf(fabsf(__uint_as_float(cur.x << 16)),
+                                fabsf(__uint_as_float(cur.x & 0xFFFF0000u))),
+                          fmaxf(fabsf(__uint_as_float(cur.y << 16)),
+                                fabsf(__uint_as_float(cur.y & 0xFFFF0000u))));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          // floor(log2 m) from the bits; p = 7 - that puts m 2^p in [128, 256)
-          float sc1 = 0.f, sc2 = 0.f, f = 0.f;
-          if (m > 0.f) {
-            const uint32_t mb = __float_as_uint(m);
-            const int el =
-                (mb >> 23) ? static_cast<int>(mb >> 23) - 127 : (31 - __clz(mb)) - 149;
-            const int p = 7 - el;                // in [-120, 156]
-            const int p1 = p >> 1, p2 = p - p1;  // each in [-60, 78]
-            sc1 = __uint_as_float(static_cast<uint32_t>(p1 + 127) << 23);
-            sc2 = __uint_as_float(static_cast<uint32_t>(p2 + 127) << 23);
-            // f = 2^(3-p) = 2^(el-4): a normal power of two unless el is tiny
-            f = el - 4 >= -126 ? __uint_as_float(static_cast<uint32_t>(el - 4 + 127) << 23)
-                               : ldexpf(1.0f, el - 4);
-          }
-          uint32_t h1 = 0, h2 = 0;  // byte i: piece of k = 4l + i
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const float2 xs = make_float2((v[2 * hf] * sc1) * sc2, (v[2 * hf + 1] * sc1) * sc2);
-            const __nv_fp8x2_storage_t a =
-                __nv_cvt_float2_to_fp8x2(xs, __NV_SATFINITE, __NV_E4M3);
-            const __half2_raw ar = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
-            const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&ar));
-            const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
-                make_float2(xs.x - af.x, xs.y - af.y), __NV_SATFINITE, __NV_E4M3);
-            h1 |= static_cast<uint32_t>(a) << (16 * hf);
-            h2 |= static_cast<uint32_t>(c) << (16 * hf);
-          }
-          // 16-block 8 g + l/4, position b = l%4: value i goes to slot 4i + b
-          uint8_t* blk = xres + ks * kX1Stage + (8 * g + (lane >> 2)) * 16 + (lane & 3);
+          uint32_t h1, h2, h3;  // byte i: piece of k = 4l + i
+          float lsum;
+          const float f = group_pieces(cur, m, h1, h2, h3, lsum);
+          // 16-block j = 8 g + l/4 (column bytes 32 j, 32 j + 16, kX1Sbo + 32 j),
+          // position b = l%4: value i goes to byte 4i + b
+          uint8_t* blk = xres + q * kX1Stage + 32 * (8 * g + (lane >> 2)) + (lane & 3);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             blk[4 * i] = static_cast<uint8_t>(h1 >> (8 * i));
-            blk[kX1Sbo + 4 * i] = static_cast<uint8_t>(h2 >> (8 * i));
+            blk[16 + 4 * i] = static_cast<uint8_t>(h2 >> (8 * i));
+            blk[kX1Sbo + 4 * i] = static_cast<uint8_t>(h3 >> (8 * i));
           }
-          if (lane == 0) ftab[ks * kGS + g] = f;
+          if (lane == 0) ftab[q * kGS + g] = make_float2(f, lsum);
           fence_proxy_async_smem();  // the MMA reads the block through the async proxy
           __syncwarp();
-          if (lane == 0) mbar_arrive(&xready[ks]);
+          if (lane == 0) mbar_arrive(&xready[q]);
+        }
+      }
+    }
+    // ------------------------------------------------------------ split-row sums
+    // Warp kXWarp0 (at T = 1 once its activation blocks are built) combines
+    // the CTA's split row blocks as the fold publishes them: it takes the
+    // row block's ticket (kept at the index of its first CTA); if every other
+    // CTA of the row block has already taken it, this CTA adds all partials
+    // in CTA order and writes y, and puts the ticket back to zero for the next
+    // launch.  The fold never waits for any of this.
+    if (warp == kXWarp0) {
+      auto first_rb = [&](int c) { return static_cast<int>(U * c / P / KS); };
+      for (int i = 0; i < nsp; ++i) {
+        const int rb = sp[i];
+        if (!__all_sync(0xffffffffu, mbar_wait(&pub[i], 0, err))) break;
+        const long long u0 = static_cast<long long>(rb) * KS;
+        const int c0 = owner_of(u0, U, P), c1 = owner_of(u0 + KS - 1, U, P);
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(&tickets[c0], 1) == c1 - c0;
+          if (last) atomicExch(&tickets[c0], 0);
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        __threadfence();
+        // lane l sums rows 4l .. 4l+3, four tokens and up to four CTAs' loads
+        // in flight at a time, adding the CTAs' partials in CTA order
+        constexpr int kTC = TT < 4 ? TT : 4;
+        for (int t0 = 0; t0 < Tt; t0 += kTC) {
+          float4 acc[kTC];
+#pragma unroll
+          for (int tj = 0; tj < kTC; ++tj) acc[tj] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cb = c0; cb <= c1; cb += 4) {
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+              const int c = cb + ci;
+              if (c > c1) break;
+              const float* pc =
+                  partials + static_cast<size_t>(c * 2 + (first_rb(c) == rb ? 0 : 1)) * TT * kRows +
+                  4 * lane;
+#pragma unroll
+              for (int tj = 0; tj < kTC; ++tj) {
+                if (t0 + tj < Tt) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(pc + (t0 + tj) * kRows));
+                  acc[tj].x += v.x;
+                  acc[tj].y += v.y;
+                  acc[tj].z += v.z;
+                  acc[tj].w += v.w;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int tj = 0; tj < kTC; ++tj) {
+            if (t0 + tj >= Tt) continue;
+            float* yr = y + static_cast<size_t>(tok0 + t0 + tj) * N + rb * kRows + 4 * lane;
+            const int n = rb * kRows + 4 * lane;
+            const float a[4] = {acc[tj].x, acc[tj].y, acc[tj].z, acc[tj].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (n + e < N) yr[e] = a[e];
+          }
         }
       }
     }
@@ -544,28 +823,32 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     // Each warp runs its loop whole so that addresses and descriptors stay
     // warp-uniform; one elected lane issues.  Half-stage hu = 2 it + hh
-    // (groups 2 hh, 2 hh + 1) uses A slot hu % NA and D slot hu % ND and is
+    // (groups 4 hh .. 4 hh + 3) uses A slot hu % NA and D slot hu % ND and is
     // issued by MMA warp hh.
     const int w = warp - kMmaWarp;
     const bool leader = elect_one();
-    constexpr uint32_t idesc = idesc_e4m3_f32(kRows, NC);
-    // Descriptor of stage 0's B block; a stage / k chunk only moves the start
-    // address field (address >> 4 in the low bits).
+    constexpr uint32_t idesc = idesc_e4m3_e5m2_f32(kRows, NC);
+    constexpr uint32_t idesc3 = idesc_e4m3_e5m2_f32(kRows, 16);  // piece-2 block
+    // Descriptor of stage (slot) 0's B block; a stage / k chunk only moves the
+    // start address field (address >> 4 in the low bits).
     const uint64_t desc0 =
         C::kInKernelX ? smem_desc_kmajor(smem_addr(xres), kX1Lbo, kX1Sbo)
                       : smem_desc_kmajor(smem_addr(smem + C::kXOff), kXLbo, kXSbo);
     constexpr uint32_t kLbo = C::kInKernelX ? kX1Lbo : kXLbo;
     int last = -1;
-    for (int hu = w; hu < 2 * nunits; hu += kMmaWarps) {
+    Cursor cu;
+    cu.start(vs);
+    for (int hu = w; hu < 2 * nunits; hu += kMmaWarps, cu.next(vs)) {
       const int it = hu >> 1, hh = hu & 1;
       const int s = it % S;
-      const int ks = static_cast<int>((ks0 + it) % KS);
+      const int ks = cu.ks;
       const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
+      const int q = stage_slot(vs, ks);  // (T = 1) resident slot
       const uint64_t dstage =
-          desc0 + static_cast<uint64_t>(
-                      (C::kInKernelX ? ks * kX1Stage : s * C::kXFrag) >> 4);
+          desc0 + static_cast<uint64_t>((C::kInKernelX ? q * kX1Stage : s * C::kXFrag) >> 4);
+      const uint64_t dstage3 = dstage + static_cast<uint64_t>(C::kXMain >> 4);
       if constexpr (C::kInKernelX) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&xready[q], 0, err))) break;
       }
       const int a = hu % NA;
       const int d = hu % ND;
@@ -589,10 +872,14 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
             const int g = kGH * hh + gg;
             if (g < ng) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8,
-                              dstage + static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4),
-                              idesc, kk > 0);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t koff = static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4);
+                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8, dstage + koff, idesc,
+                              kk > 0);
+                if constexpr (C::kH3)  // piece 2 onto piece 0's columns
+                  mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8, dstage3 + koff, idesc3,
+                                true);
+              }
             }
           }
           mma_commit(&afree[2 * a + b]);
@@ -621,15 +908,16 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     const int h = warp >> 2;
     const int r = q * 32 + lane;  // row within the block == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    int ks = ks0;
-    for (int it = 0; it < nunits; ++it) {
+    Cursor cu;
+    cu.start(vs);
+    for (int it = 0; it < nunits; ++it, cu.next(vs)) {
       const int s = it % S;
       const int hu = 2 * it + h;  // this warp's half-stage
       const int a = hu % NA;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / S) & 1, err))) break;
       // half-stage h is weight box h: groups kGH h .. kGH h + kGH - 1
       const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + h * (kRows * 128) + r * 128;
-      const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
+      const int ng = G - kGS * cu.ks < kGS ? G - kGS * cu.ks : kGS;
       bool ok_h = true;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {  // A sub-slot b: groups 2 b, 2 b + 1 of the half-stage
@@ -665,67 +953,42 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       }
       if (!ok_h) break;
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (++ks == KS) ks = 0;
     }
   } else {
     // ------------------------------------------------------------ fold
     // Fold warp f owns TMEM lane quarter fq = f % 4 (rows 32 fq .. 32 fq + 31)
-    // and half-stage fh = f / 4 (groups 2 fh, 2 fh + 1) of every stage:
-    // y[t][row] += s[row][g] * f[g][t] * (D[g][piece 0, t] + D[g][piece 1, t]).
-    // At the end of a row block the fh = 1 warp hands its sums to the fh = 0
-    // warp of the same quarter, which writes y.
+    // and half-stage fh = f / 4 (groups 4 fh .. 4 fh + 3) of every stage:
+    // y[t][row] += s[row][g] * f[g][t] * (sum of the pieces' accumulators of
+    // token t).  At the end of a row block the fh = 1 warp hands its sums to
+    // the fh = 0 warp of the same quarter, which writes y (or, for a row
+    // block shared with other CTAs, publishes them for the split-row warp).
+    //
+    // Leftovers (a group's elements more than 21 binades below its absmax,
+    // flagged by a negative f, with their sum of |x| in L): for each output,
+    // their contribution is at most s * L.  The running sum |yacc| of this
+    // warp's groups is a lower bound of sum|s w x| over those groups (every
+    // term added is an exact part of y, or the pieces' sum, bounded by its own
+    // sum of |s w x|), so while the dropped bounds add up to at most 2^-12 of
+    // it the leftovers are left out: the error stays below 2^-12 of
+    // sum|s w x|.  Otherwise they are added exactly (leftover_dot).  One budget
+    // lam serves all tokens of a row: a token's own dropped bounds never
+    // exceed lam, which each drop keeps within 2^-12 of that token's |yacc|.
     const int fq = (warp - kDecWarps) & 3;  // == warp % 4
     const int fh = (warp - kDecWarps) >> 2;
     const int r = fq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
     float yacc[TT];
+    float lam = 0.f;  // leftover bounds left out so far in this row block
 #pragma unroll
     for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
 
-    // Row blocks split between CTAs are summed with fp32 atomics into y.
-    // Every CTA first zeroes the y rows of its split row blocks, then adds to
-    // the launch-arrival counter; a CTA adds into y only once the counter
-    // shows that every writing fold warp of the launch has done its zeroing.
-    // Each launch adds exactly 1024 in total, so the counter is a multiple of
-    // 1024 between launches and needs no reset.  (Only the fh = 0 warps write
-    // y, zero and count.)
-    auto is_split = [&](int rb) {
-      const long long u = static_cast<long long>(rb) * KS;
-      return owner_of(u, U, P) != owner_of(u + KS - 1, U, P);
-    };
-    grid_dependency_wait();  // y and the workspace may be in use by earlier work
-    const int rb_last = static_cast<int>((end - 1) / KS);
-    unsigned long long arrival_target = 0;
-    if (fh == 0) {
-      const int zr[2] = {rb0, rb_last};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if ((i == 1 && rb_last == rb0) || !is_split(zr[i])) continue;
-        const int n = zr[i] * kRows + r;
-        if (n < N)
-          for (int t = 0; t < Tt; ++t) y[static_cast<size_t>(tok0 + t) * N + n] = 0.f;
-      }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) {
-        const unsigned long long add =
-            (cta == 0 && fq == 0) ? 1024ull - 4ull * static_cast<unsigned long long>(P) + 1ull
-                                  : 1ull;
-        arrival_target = (atomicAdd(arrivals, add) & ~1023ull) + 1024ull;
-      }
-      arrival_target = __shfl_sync(0xffffffffu, arrival_target, 0);
-    }
-
-    // A split row block's sums are added into y only after the arrival
-    // counter shows every CTA has zeroed; so that the fold never stalls on
-    // that check mid-stream, the first row block's sums (when split) wait in
-    // shared memory and all atomics are issued once this CTA's last unit is
-    // folded.
-    float* first_part = reinterpret_cast<float*>(smem + C::kFirstOff);  // [TT][128]
-    float* half_part = reinterpret_cast<float*>(smem + C::kPartOff);    // [TT][128]
-    bool first_parked = false;
+    float* half_part = reinterpret_cast<float*>(smem + C::kPartOff);  // [TT][128]
     int nflush = 0;
-    // false: a bounded wait gave up (the error word is set)
+    int nsplit = 0;
+    // Row block rb's sums are final in yacc (fh = 0 warps): a row block whole
+    // in this CTA is stored; a split one's sums are published as this CTA's
+    // partial (slot 0: the CTA's first row block, 1: its last) for the
+    // split-row warp.  false: a bounded wait gave up.
     auto flush = [&](int rb) -> bool {
       const int n = rb * kRows + r;
       if (fh == 1) {
@@ -743,72 +1006,84 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         for (int t = 0; t < TT; ++t) yacc[t] += half_part[t * kRows + r];
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfree[fq]);
-        if (!is_split(rb)) {
+        if (nsplit < nsp && rb == sp[nsplit]) {
+          float* mine =
+              partials + static_cast<size_t>(cta * 2 + (rb == rb0 ? 0 : 1)) * TT * kRows;
+#pragma unroll
+          for (int t = 0; t < TT; ++t) mine[t * kRows + r] = yacc[t];
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pub[nsplit]);
+          ++nsplit;
+        } else {
 #pragma unroll
           for (int t = 0; t < TT; ++t)
             if (n < N && t < Tt) y[static_cast<size_t>(tok0 + t) * N + n] = yacc[t];
-        } else if (rb == rb0 && rb != rb_last) {
-#pragma unroll
-          for (int t = 0; t < TT; ++t) first_part[t * kRows + r] = yacc[t];
-          first_parked = true;
-        } else {
-          bool fine = true;
-          if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
-          fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
-          if (fine) {
-#pragma unroll
-            for (int t = 0; t < TT; ++t)
-              if (n < N && t < Tt) atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n], yacc[t]);
-            if (first_parked) {
-              const int n0 = rb0 * kRows + r;
-#pragma unroll
-              for (int t = 0; t < TT; ++t)
-                if (n0 < N && t < Tt)
-                  atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0],
-                            first_part[t * kRows + r]);
-              first_parked = false;
-            }
-          }
         }
       }
       ++nflush;
 #pragma unroll
       for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
+      lam = 0.f;
       return true;
     };
 
-    int ks = ks0;
+    Cursor cu;
+    cu.start(vs);
     bool ok = true;
-    for (int j = 0; j < nunits && ok; ++j) {
+    for (int j = 0; j < nunits && ok; ++j, cu.next(vs)) {
       const int ss = j % SS;
       if (!__all_sync(0xffffffffu, mbar_wait(&sfull[ss], (j / SS) & 1, err))) break;
+      const int ks = cu.ks;
       const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
       const uint8_t* sst = smem + C::kSOff + ss * C::kSBytes;
       // this half-stage's kGH fp16 scales
       const uint2 s4 = lds_v2(sst + r * (2 * kGS) + fh * (2 * kGH));
-      // f[g][t] at fv[g * FH + t]
-      constexpr int FH = C::kInKernelX ? 1 : H;
-      const float* fv = C::kInKernelX ? ftab + ks * kGS
-                                      : reinterpret_cast<const float*>(sst + kRows * 2 * kGS);
+      auto scale_of = [&](int gg) {
+        const uint32_t sp2 = gg < 2 ? s4.x : s4.y;
+        return __half2float(__ushort_as_half(
+            static_cast<unsigned short>((gg & 1) ? (sp2 >> 16) : (sp2 & 0xFFFFu))));
+      };
+      const int q = stage_slot(vs, ks);  // (T = 1) resident slot
+      // (f, L) of group g (within the stage), token t
+      auto fl_of = [&](int g, int t) -> float2 {
+        if constexpr (C::kInKernelX) {
+          return ftab[q * kGS + g];
+        } else {
+          const float* fl = reinterpret_cast<const float*>(sst + kRows * 2 * kGS);
+          return make_float2(fl[g * H + t], fl[(kGS + g) * H + t]);
+        }
+      };
       if constexpr (C::kInKernelX) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&xready[ks], 0, err))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&xready[q], 0, err))) break;
       }
       const int hu = 2 * j + fh;
       const int d = hu % ND;
       if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) break;
       tc_fence_after();
       const uint32_t dbase = tbase + lane_off + C::kDCol + d * C::kDSlot;
-      // only the accumulator columns that carry tokens are read back:
-      // piece 0 of token t is column t, piece 1 is H + t
+      // (warp-uniform) sign bit set: some group of the half-stage has
+      // leftovers for some token (an OR of the factors' bits)
+      uint32_t fbits = 0;
+      // Only the accumulator columns that carry tokens are read back; dv[]
+      // holds them with piece j of token t at dv[PJ[j] + t].
       auto fold_group = [&](int gg, const uint32_t* dv) {
-        const uint32_t sp = gg < 2 ? s4.x : s4.y;
-        const float sg = __half2float(__ushort_as_half(
-            static_cast<unsigned short>((gg & 1) ? (sp >> 16) : (sp & 0xFFFFu))));
+        const float sg = scale_of(gg);
         const int g = kGH * fh + gg;
 #pragma unroll
-        for (int t = 0; t < TT; ++t)
-          yacc[t] = fmaf(sg * fv[g * FH + t], __uint_as_float(dv[t]) + __uint_as_float(dv[H + t]),
-                         yacc[t]);
+        for (int t = 0; t < TT; ++t) {
+          float dsum;
+          if constexpr (TT == 1)
+            dsum = (__uint_as_float(dv[0]) + __uint_as_float(dv[1])) + __uint_as_float(dv[2]);
+          else if constexpr (C::kH3)
+            dsum = __uint_as_float(dv[t]) + __uint_as_float(dv[C::kP1 + t]);
+          else
+            dsum = (__uint_as_float(dv[t]) + __uint_as_float(dv[C::kP1 + t])) +
+                   __uint_as_float(dv[C::kP2 + t]);
+          const float f = fl_of(g, t).x;
+          fbits |= __float_as_uint(f);
+          yacc[t] = fmaf(sg * fabsf(f), dsum, yacc[t]);
+        }
       };
       static_assert(NC == 16 || NC == 32, "accumulator width");
       static_assert(TT == 1 || TT == 4 || TT == 8 || TT == 16, "token tiles");
@@ -831,17 +1106,19 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
           if (has) fold_group(gg, dv);
         }
       } else {
-        uint32_t dv[kGH][NC];
+        constexpr int kDV = TT == 1 ? 3 : 12;
+        uint32_t dv[kGH][kDV];
 #pragma unroll
         for (int gg = 0; gg < kGH; ++gg) {
           if (kGH * fh + gg < ng) {
             const uint32_t col = dbase + gg * NC;
             if constexpr (TT == 1) {
-              tmem_ld1(col, dv[gg][0]);
-              tmem_ld1(col + H, dv[gg][H]);
+              tmem_ld2(col, dv[gg]);            // pieces 0, 1 (columns 0, 1)
+              tmem_ld1(col + C::kP2, dv[gg][2]);  // piece 2 (column 8)
             } else {
               tmem_ld4(col, dv[gg]);
-              tmem_ld4(col + H, dv[gg] + H);
+              tmem_ld4(col + C::kP1, dv[gg] + 4);
+              tmem_ld4(col + C::kP2, dv[gg] + 8);
             }
           }
         }
@@ -853,26 +1130,38 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         for (int gg = 0; gg < kGH; ++gg)
           if (kGH * fh + gg < ng) fold_group(gg, dv[gg]);
       }
+      if (fbits >> 31) {  // rare: groups with leftovers (see above)
+        const int n = cu.rb * kRows + r;
+#pragma unroll 1
+        for (int bit = 0; bit < kGH * TT; ++bit) {
+          const int gg = bit / TT, t = bit % TT;
+          const int g = kGH * fh + gg;
+          if (g >= ng) break;
+          const float2 fl = fl_of(g, t);
+          if (!(fl.x < 0.f)) continue;
+          const float sg = scale_of(gg);
+          const float bound = sg * fl.y;
+          float acc = yacc[0];
+#pragma unroll
+          for (int u = 1; u < TT; ++u)
+            if (u == t) acc = yacc[u];
+          if (lam + bound <= 0x1p-12f * fabsf(acc)) {
+            lam += bound;
+          } else if (n < N && t < Tt) {
+            const int ga = ks * kGS + g;
+            acc = fmaf(sg,
+                       leftover_dot(wp, x + static_cast<size_t>(tok0 + t) * K + ga * 128, K, n,
+                                    ga, leftover_limit(-fl.x)),
+                       acc);
+          }
+#pragma unroll
+          for (int u = 0; u < TT; ++u)
+            if (u == t) yacc[u] = acc;
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[ss]);
-      if (++ks == KS) {
-        ok = flush(static_cast<int>((begin + j) / KS));
-        ks = 0;
-      }
-    }
-    // a row block whose last stage lies beyond this CTA's range
-    if (ok && ks != 0) ok = flush(rb_last);
-    if (ok && fh == 0 && first_parked) {
-      // the last row block was whole: add the parked first one now
-      bool fine = true;
-      if (lane == 0) fine = wait_counter_at_least(arrivals, arrival_target, err);
-      fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
-      const int n0 = rb0 * kRows + r;
-      if (fine)
-#pragma unroll
-        for (int t = 0; t < TT; ++t)
-          if (n0 < N && t < Tt)
-            atomicAdd(&y[static_cast<size_t>(tok0 + t) * N + n0], first_part[t * kRows + r]);
+      if (cu.ends_row_block(vs)) ok = flush(cu.rb);
     }
   }
 
@@ -902,35 +1191,60 @@ cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block, 
   return cfg;
 }
 
-template <int TT>
-cudaError_t launch_tt(const CUtensorMap* tmW, const uint16_t* scales, const uint16_t* x,
-                      int* sync, uint8_t* work, float* y, int K, int N, int tok0, int Tt,
-                      int num_sms, int* err, cudaStream_t stream) {
-  using C = TC<TT>;
-  const int KS = (K + kSTStageK - 1) / kSTStageK;
+// Grid of the small-T kernel for (K, N): units U, CTAs P, stages KS.
+struct SmallTGrid {
+  int KS;
+  long long U, P;
+};
+SmallTGrid smallt_grid(int K, int N, int num_sms) {
+  SmallTGrid g;
+  g.KS = (K + kSTStageK - 1) / kSTStageK;
   const long long NB = (N + kRows - 1) / kRows;
-  const long long U = NB * KS;
+  g.U = NB * g.KS;
   long long P = num_sms;  // one CTA per SM: each holds all 512 TMEM columns
   if (P > kSmallTMaxCtas) P = kSmallTMaxCtas;
-  if (P > U) P = U;
-  uint8_t* xprep = work;
+  if (P > g.U) P = g.U;
+  g.P = P;
+  return g;
+}
+
+// Resident activation slots of the one-token kernel: the distinct stages a CTA
+// visits at most.
+int t1_slots(const SmallTGrid& g) {
+  const long long per = (g.U + g.P - 1) / g.P;
+  return static_cast<int>(per < g.KS ? per : g.KS);
+}
+
+template <int TT>
+cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t* scales,
+                      const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
+                      int tok0, int Tt, int num_sms, int* err, cudaStream_t stream) {
+  using C = TC<TT>;
+  const SmallTGrid g = smallt_grid(K, N, num_sms);
+  const int nslots = C::kInKernelX ? t1_slots(g) : 0;
+  if (nslots > kSmallTX1MaxSlots) return cudaErrorInvalidValue;
+  float* partials = reinterpret_cast<float*>(work);
+  uint8_t* xprep = work + smallt_partials_bytes(TT);
 
   cudaLaunchAttribute attr[1];
   if constexpr (!C::kInKernelX) {
-    const int tasks = C::kH * kGS * KS;
+    const int tasks = C::kH * kGS * g.KS;
     cudaLaunchConfig_t pc = pdl_config(attr, dim3((tasks + 7) / 8), dim3(256), 0, stream);
-    cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, KS);
+    cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(static_cast<unsigned>(P)), dim3(C::kThreads),
-                                      C::smem_bytes(KS), stream);
-  return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, scales, x,
-                            static_cast<const uint8_t*>(xprep), y,
-                            reinterpret_cast<unsigned long long*>(sync), K, N, tok0, Tt, KS, U,
-                            err);
+  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(static_cast<unsigned>(g.P)), dim3(C::kThreads),
+                                      C::smem_bytes(nslots), stream);
+  return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, Wp, scales, x,
+                            static_cast<const uint8_t*>(xprep), y, sync, partials, K, N, tok0, Tt,
+                            g.KS, nslots, g.U, err);
 }
 
 }  // namespace
+
+size_t smallt_partials_bytes(int tt) {
+  return static_cast<size_t>(kSmallTMaxCtas) * 2 * tt * kRows * sizeof(float);
+}
 
 size_t smallt_work_bytes(int tt, int K) {
   const int KS = (K + kSTStageK - 1) / kSTStageK;
@@ -941,10 +1255,14 @@ size_t smallt_work_bytes(int tt, int K) {
     case 8: prep = static_cast<size_t>(TC<8>::kXBytes) * KS; break;
     default: prep = static_cast<size_t>(TC<16>::kXBytes) * KS; break;
   }
-  return prep;
+  return smallt_partials_bytes(tt) + prep;
 }
 
 int smallt_rows(int) { return kRows; }
+
+int smallt_gemv_tile(int K, int N, int num_sms) {
+  return t1_slots(smallt_grid(K, N, num_sms)) <= kSmallTX1MaxSlots ? 1 : 4;
+}
 
 cudaError_t smallt_set_attributes() {
   cudaError_t e;
@@ -955,18 +1273,20 @@ cudaError_t smallt_set_attributes() {
   return cudaSuccess;
 }
 
-cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint16_t* scales,
-                          const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
-                          int tok0, int Tt, int num_sms, int* err, cudaStream_t stream) {
+cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
+                          const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int* err,
+                          cudaStream_t stream) {
   switch (tt) {
     case 1:
-      return launch_tt<1>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
     case 4:
-      return launch_tt<4>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
     case 8:
-      return launch_tt<8>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
     default:
-      return launch_tt<16>(tmW, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err,
+                           stream);
   }
 }
 

@@ -189,12 +189,14 @@ def test_default_dispatch(tl, T, expect):
     assert _check_case(tl, case, None) == expect
 
 
-@pytest.mark.parametrize("K", [24576, 25088])
-def test_gemv_k_limit_of_the_one_token_tile(tl, K):
-    # 24576 is the largest K whose activation blocks stay resident in the
-    # one-token kernel; 25088 runs on the four-token tile.  N = 300 over 64+
-    # stages cuts most row blocks between CTAs.
-    _check_case(tl, synth.case("bigk", 1, K=K, N=300, seed=K))
+@pytest.mark.parametrize("K,N", [(24576, 300), (25088, 300), (16384, 34816), (17408, 34816)])
+def test_gemv_k_limit_of_the_one_token_tile(tl, K, N):
+    # The one-token kernel keeps the activation blocks of every k stage a CTA
+    # visits resident, at most 16: a CTA of K = 16384 x N = 34816 visits all
+    # 16 stages; K = 17408 x N = 34816 would need 17 and runs on the
+    # four-token tile; with N = 300 (3 row blocks) each CTA visits one or two
+    # stages at any K, and most row blocks are cut between CTAs.
+    _check_case(tl, synth.case("bigk", 1, K=K, N=N, seed=K), full=N < 1000)
 
 
 def test_workspace_reused_across_calls(tl):
@@ -213,9 +215,8 @@ def test_workspace_reused_across_calls(tl):
             wp_ref, _ = oracle.pack(c.W)
             y_ref, m = oracle.linear_f64(wp_ref, c.scales, c.x, c.T, c.K, c.N)
             assert_bf16_parity(y.cpu().numpy(), y_ref, m, f"{c.name} pass {rep}")
-    # the launch-arrival counter advances by whole launches
-    ctr = int(ws[:8].cpu().numpy().view(np.uint64)[0])
-    assert ctr % 1024 == 0 and ctr > 0
+    # every call leaves the ticket counters of the synchronisation area zeroed
+    assert not ws[:tl.SYNC_BYTES].cpu().numpy().any()
 
 
 @pytest.mark.parametrize("K,N", [(128, 1), (128, 17), (256, 129), (1152, 520), (2048, 4096)])
@@ -292,6 +293,144 @@ def test_s8_integer_accumulators_bit_exact(tl):
     exact = x32.astype(np.int64) @ W.astype(np.int64).T
     assert np.array_equal(y.astype(np.int64), exact)
     assert np.array_equal(y, exact.astype(np.float32))
+
+
+# ---------------------------------------------------------------- adversarial activations
+# Inputs real activations can have and the N(0,1) families do not: a group's
+# absmax on a weight that is zero in every row, a wide dynamic range inside
+# a group, bf16 subnormals, values spread over more binades than the
+# activation pieces cover (the kernels' exact leftover path), and one
+# outlier channel far above the rest.  Every rung is forced on each.
+
+def _adversarial_x(kind, T, K, seed, zero_cols=None):
+    """bf16 bits [T, K] of one adversarial kind (see the section comment)."""
+    rng = np.random.default_rng([seed, T, K])
+    sign = rng.choice([-1.0, 1.0], size=(T, K))
+    if kind == "absmax_on_zero_weight":
+        x = np.full((T, K), 0.01) * sign
+        x[:, zero_cols] = 80.0 * sign[:, zero_cols]
+    elif kind == "absmax_huge_on_zero_weight":
+        x = rng.standard_normal((T, K)) * 1e-3
+        x[:, zero_cols] = 2.0 ** 40 * sign[:, zero_cols]
+    elif kind == "range_2e-20":
+        x = np.exp2(-rng.uniform(0, 20, (T, K))) * sign
+    elif kind == "range_2e-60":
+        # several clusters per group: spans far beyond the pieces' 21 binades
+        x = np.exp2(rng.choice([40.0, 10.0, -15.0, -45.0], size=(T, K)) +
+                    rng.uniform(0, 4, (T, K))) * sign
+    elif kind == "subnormal":
+        # bf16 subnormals (below 2^-126) next to normal values, and whole
+        # groups of subnormals only
+        x = rng.standard_normal((T, K))
+        x[:, 1::3] = rng.integers(1, 128, size=(T, len(range(1, K, 3)))) * 2.0 ** -133
+        x[:, :128] = rng.integers(1, 128, size=(T, 128)) * 2.0 ** -133 * sign[:, :128]
+    elif kind == "outlier_x1000":
+        x = rng.standard_normal((T, K))
+        ch = rng.choice(K, size=max(1, K // 100), replace=False)
+        x[:, ch] *= 1000.0
+    else:
+        raise ValueError(kind)
+    return synth.f32_to_bf16_bits(x.astype(np.float32))
+
+
+ADVERSARIAL = ("absmax_on_zero_weight", "absmax_huge_on_zero_weight", "range_2e-20",
+               "range_2e-60", "subnormal", "outlier_x1000")
+
+
+@pytest.mark.parametrize("kind", ADVERSARIAL)
+@pytest.mark.parametrize("rung,T", [("gemv", 1), ("small_t", 3), ("small_t", 8),
+                                    ("small_t_tiled", 13), ("s8", 20)])
+def test_adversarial_activations(tl, kind, rung, T):
+    import torch
+    K, N = 1280, 300
+    W = synth.ternary_weights(N, K, 0.4, seed=31)
+    zero_cols = np.arange(5, K, 128)  # one per group, zero in every row
+    W[:, zero_cols] = 0
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=32)
+    xb = _adversarial_x(kind, T, K, seed=33, zero_cols=zero_cols)
+    x64 = synth.bf16_bits_to_f32(xb).astype(np.float64)
+    assert np.isfinite(x64).all()
+    if kind == "subnormal":
+        assert ((np.abs(x64) < 2.0 ** -126) & (x64 != 0)).any()
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, sd, xd)
+        assert tl.tern_last_rung() == rung
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    y = y.cpu().numpy()
+    wp_ref, _ = oracle.pack(W)
+    what = f"{kind} rung={rung} T={T}"
+    if rung == "s8":
+        q_ref, xs_ref = oracle.quant_s8(xb, T, K)
+        y_ref, m, _ = oracle.linear_s8(wp_ref, s, q_ref, xs_ref, T, K, N)
+        assert_s8_parity(y, y_ref, m, what)
+    else:
+        y_ref, m = oracle.linear_f64(wp_ref, s, xb, T, K, N)
+        assert_bf16_parity(y, y_ref, m, what)
+
+
+@pytest.mark.parametrize("rung,T", [("gemv", 1), ("small_t", 4), ("small_t_tiled", 16)])
+def test_leftovers_alone_carry_the_output(tl, rung, T):
+    """Only the leftovers have nonzero weights: a group's absmax 2^50 sits on
+    a zero weight and everything else lies 30+ binades below it, so y comes
+    entirely from the kernels' exact leftover path."""
+    import torch
+    K, N = 1024, 200
+    W = synth.ternary_weights(N, K, 1.0 / 3.0, seed=41)
+    big = np.arange(0, K, 128) + 7
+    W[:, big] = 0
+    s = synth.scales_lognormal(N, K, -3.5, 0.3, seed=42)
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((T, K)) * 2.0 ** 10
+    x[:, big] = 2.0 ** 50
+    xb = synth.f32_to_bf16_bits(x.astype(np.float32))
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, sd, xd)
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    wp_ref, _ = oracle.pack(W)
+    y_ref, m = oracle.linear_f64(wp_ref, s, xb, T, K, N)
+    assert np.abs(y_ref).max() > 1.0
+    assert_bf16_parity(y.cpu().numpy(), y_ref, m, f"leftovers only rung={rung}")
+
+
+def test_decode_gate_up_outlier_x1000_sampled(tl):
+    """The full-size gate+up projection at T = 1 with 1% outlier channels
+    scaled x1000 instead of x20."""
+    import torch
+    c = synth.config_decode("gu")
+    xb = synth.activations(1, c.K, seed=0, outlier_frac=0.01, outlier_gain=1000.0)
+    W, s, _ = to_device(c)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    Wp = tl.tern_pack(W)
+    del W
+    y = tl.tern_linear(Wp, s, x)
+    assert tl.tern_last_rung() == "gemv"
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    wp_ref, _ = oracle.pack(c.W)
+    y_ref, m = oracle.linear_f64(wp_ref, c.scales, xb, 1, c.K, c.N)
+    assert_bf16_parity(y.cpu().numpy(), y_ref, m, "gate+up T=1 outliers x1000")
+
+
+def test_split_row_blocks_are_deterministic(tl):
+    """Row blocks split between CTAs are reduced in CTA order: repeated calls
+    give identical bits."""
+    import torch
+    for proj, T in (("dn", 1), ("gu", 1), ("dn", 4), ("ao", 12)):
+        c = synth.case(proj, T, seed=51)
+        W, s, x = to_device(c)
+        Wp = tl.tern_pack(W)
+        del W
+        ys = [tl.tern_linear(Wp, s, x).clone() for _ in range(4)]
+        torch.cuda.synchronize()
+        assert tl.tern_device_status() == 0
+        for y in ys[1:]:
+            assert torch.equal(y.view(torch.int32), ys[0].view(torch.int32)), proj
 
 
 # ---------------------------------------------------------------- workload families
