@@ -103,6 +103,30 @@ __device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* 
   }
 }
 
+// atomicAdd with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Wait until the upper 16 bits of *p are nonzero (acquire, GPU scope).  Gives
+// up after kWaitLimitNs: ORs kErrTimeout into *err and returns false.
+__device__ __forceinline__ bool wait_word_high_nonzero(const int* p, int* err) {
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if ((v >> 16) != 0) return true;
+    if (it == 0) t0 = global_timer_ns();
+    else if ((it & 15u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // 2D tiled load of a box into shared memory, completing on `bar`.
 // x is the innermost coordinate (in elements of the tensor map's type).

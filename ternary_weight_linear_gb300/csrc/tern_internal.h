@@ -16,7 +16,7 @@ constexpr int kSmallTMaxCtas = 160;
 // Most activation blocks the one-token kernel keeps resident in shared memory
 // (one per distinct k stage a CTA visits); a one-token call that needs more
 // runs on the four-token tile.
-constexpr int kSmallTX1MaxSlots = 16;
+constexpr int kSmallTX1MaxSlots = 8;
 
 // Workspace layout shared by all rungs: a synchronisation area of kSyncBytes
 // (the small-T kernels' ticket counters, one int per CTA, which must hold

@@ -11,7 +11,8 @@
 // 1. Activation pieces.  Per token and per 128-wide group, x is scaled by a
 //    power of two 2^p so that the group's absmax m lies in [2^14, 2^15), and
 //    split into three fp8 e5m2 pieces
-//        v = x 2^p,  h1 = RN(v),  h2 = RN(v - h1),  h3 = RN(v - h1 - h2).
+//        v = x 2^p,  h1 = RN(v),  h2 = RN(v - h1),  h3 = RN(v - h1 - h2)
+//    (RN: nearest e5m2 value, ties to even, computed as round3).
 //    A bf16 value has 8 significant bits and an e5m2 value 3, and each
 //    rounding leaves a remainder at most half a step of the piece it rounds
 //    to; so for every element whose exponent is at least that of m minus 21
@@ -122,6 +123,9 @@ constexpr uint32_t kXSbo = kSTStageK / 16 * 128;  // N-direction stride (8 colum
 constexpr uint32_t kX1Lbo = 32;
 constexpr uint32_t kX1Sbo = kSTStageK / 16 * 32 + 128;  // second 8-column group
 constexpr int kX1Stage = 2 * kX1Sbo;                    // bytes per stage block
+// A stage's block and its groups' (f, L) pairs, as the prep kernel writes it
+// and the one-token kernel keeps it resident.
+constexpr int kX1Slot = kX1Stage + (kSTStageK / 128) * 8;
 static_assert(kX1Sbo >= kSTStageK / 16 * 32 + 7 * 16, "the junk columns' overrun stays inside");
 
 template <int TT>
@@ -142,51 +146,55 @@ struct TC {
   static constexpr int kXFrag = kXMain + (kH3 ? 16 * kSTStageK : 0);  // + piece-2 block
   // per (group, token): the factor f, then the leftovers' sum of |x| L
   static constexpr int kXF = 2 * kGS * kH * 4;                   // f[group][kH], L[group][kH]
-  static constexpr int kXBytes = kXFrag + kXF;                   // one stage of the prep buffer
-  static constexpr bool kInKernelX = TT == 1;                    // x blocks built by the main kernel
-  // (T = 1) activation warps, two groups of every stage each; the first of
-  // them (the only one for T > 1) then sums the CTA's split row blocks
-  static constexpr int kXWarps = kInKernelX ? 4 : 1;
+  // one stage of the prep buffer (T = 1: compact block + (f, L)[group])
+  static constexpr int kXBytes = TT == 1 ? kX1Slot : kXFrag + kXF;
+  // T = 1: the stages' blocks stay resident, copied once per call
+  static constexpr bool kInKernelX = TT == 1;
+  static constexpr int kXWarps = 1;  // the split-row warp
   static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
-  // TMEM is used in half-stage slots (kGH groups): A slots of kGH x 32
-  // columns (e4m3), D slots of kGH x kNC columns.
-  // Both ring lengths are even: half-stage hu uses slot hu % n, so every
-  // slot only ever holds half-stages of one parity, which one decode half,
-  // one MMA issuer and one fold half own.  A barrier a waiter checks is then
-  // never two phases behind it (with an odd length the slot alternates
-  // between the halves, and an issuer could pass a parity check while the
-  // other decode half was still one phase back).
-  static constexpr int kNAH = 2;
-  static constexpr int kNDH = TT <= 8 ? 4 : 2;
-  static_assert(kNAH % 2 == 0 && kNDH % 2 == 0, "slot rings must not mix half-stage parities");
-  static constexpr int kStages = TT == 1 ? 4 : (TT == 16 ? 2 : 3);  // weight (+ activation) ring
+  // TMEM.  A (e4m3 weights): each half-stage (one decode half, one MMA
+  // issuer) has its own ring of kNSub sub-slots of kGH / 2 groups (64
+  // columns), used in order by that half alone; its decoders can run
+  // kNSub / 2 units ahead of the MMAs that free the sub-slots.  A sub-slot
+  // needs one A-operand load of the tensor pipe per use, and only its own
+  // half ever waits on its barriers.  D (fp32 accumulators): one slot of
+  // kGH x kNC columns per half-stage; the fold drains it before the next
+  // unit's MMAs of that half.
+  static constexpr int kNSub = TT == 16 ? 2 : 3;
+  static constexpr int kNDH = 2;
+  static constexpr int kStages = TT == 1 ? 5 : (TT == 16 ? 2 : 3);  // weight (+ activation) ring
   // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
   // ring does not wait for the MMAs, so the fold must never wait for scales).
   static constexpr int kLead = kInKernelX ? 2 : 0;
   // scale (+ factor) ring: held until folded, which trails the weight ring
-  // by up to (kNAH + kNDH) / 2 stages
-  static constexpr int kSStages = kStages + kLead + (kNAH + kNDH + 1) / 2;
+  // by up to the A lookahead and the D slot
+  static constexpr int kSStages = kStages + kLead + (kNSub + 1) / 2 + 1;
   static constexpr int kWBytes = kRows * kSTStageK / 4;  // kWBoxes boxes of 128 rows x 128 B
   static constexpr int kSBytes = kRows * 2 * kGS + (kInKernelX ? 0 : kXF);  // scales [128][kGS], f, L
   static constexpr int kWOff = 0;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kXOff = kWOff + kStages * kWBytes;  // activation ring (T > 1)
   static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
   static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) (f, L)[slot][kGS]
-  static constexpr int kBarOff = kFOff + (kInKernelX ? kSmallTX1MaxSlots * kGS * 8 : 0);
-  static constexpr int kNumBars = 2 * kStages + 2 * kSStages + 4 * kNAH + 2 * kNDH + 8 + 2 +
+  static constexpr int kBarOff = kFOff;
+  static constexpr int kNumBars = 2 * kStages + 2 * kSStages + 4 * kNSub + 2 * kNDH + 8 + 2 +
                                   (kInKernelX ? kSmallTX1MaxSlots : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kPartOff = kTmemSlot + 16;  // fold: half-stage 1 sums [TT][128]
-  static constexpr int kX1Off = (kPartOff + TT * kRows * 4 + 127) / 128 * 128;  // (T = 1)
+  // fold: the CTA's split row blocks' sums [2][TT][128], for the split-row warp
+  static constexpr int kSplitOff = kPartOff + TT * kRows * 4;
+  // fold: one group of x per fold warp for exact leftovers [kFoldWarps][128] bf16
+  static constexpr int kLxOff = kSplitOff + 2 * TT * kRows * 4;
+  static constexpr int kX1Off = (kLxOff + kFoldWarps * 256 + 127) / 128 * 128;  // (T = 1)
   // shared memory for nslots resident T = 1 blocks: fixed part, blocks, alignment slack
   static constexpr int smem_bytes(int nslots) {
-    return kX1Off + (kInKernelX ? nslots * kX1Stage : 0) + 1024;
+    return kX1Off + (kInKernelX ? nslots * kX1Slot : 0) + 1024;
   }
   static constexpr int kAllocMax = smem_bytes(kInKernelX ? kSmallTX1MaxSlots : 0);
-  static constexpr uint32_t kASlot = kGH * 32;     // A[kNAH] slots
-  static constexpr uint32_t kDSlot = kGH * kNC;    // D[kNDH] slots
+  static constexpr uint32_t kSubCols = (kGH / 2) * 32;  // A sub-slot
+  static constexpr uint32_t kAHalf = kNSub * kSubCols;  // a half-stage's A ring
+  static constexpr uint32_t kDSlot = kGH * kNC;         // D[kNDH] slots
   static constexpr uint32_t kACol = 0;
-  static constexpr uint32_t kDCol = kNAH * kASlot;
+  static constexpr uint32_t kDCol = 2 * kAHalf;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kDCol + kNDH * kDSlot <= kTmemCols, "TMEM budget");
   static_assert(kXFrag % 16 == 0 && kXF % 16 == 0 && kXBytes % 16 == 0, "bulk copy sizes");
@@ -220,23 +228,26 @@ __device__ __forceinline__ void piece_band(float m, float& sc1, float& sc2, floa
 // computed the same way from |f| by the prep and by the fold.
 __device__ __forceinline__ float leftover_limit(float f_abs) { return f_abs * 0x1p-10f; }
 
-__device__ __forceinline__ float2 e5m2x2_to_float2(__nv_fp8x2_storage_t a) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E5M2);
-  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+// x rounded to 3 significant bits (the e5m2 grid for |x| >= 2^-14), nearest
+// with ties to even: (x + c) - c with c = 1.5 * 2^(exp(x) + 21) puts the last
+// bit of the sum at 2^(exp(x) - 2).  Two fp32 adds, no conversion latency.
+__device__ __forceinline__ float round3(float x) {
+  const uint32_t e = __float_as_uint(x) & 0x7F800000u;
+  const float c = __uint_as_float((e + (21u << 23)) | 0x00400000u);
+  return __fsub_rn(__fadd_rn(x, c), c);
 }
 
-// Three e5m2 pieces of two scaled values (low byte: v.x, high byte: v.y).
+// Three e5m2 pieces of two scaled values (low byte: v.x, high byte: v.y):
+// h1 = RN(v), h2 = RN(v - h1), h3 = RN(v - h1 - h2), computed in fp32 (every
+// difference is exact), then packed; each piece is an exact e5m2 value.
 __device__ __forceinline__ void split3_e5m2(float2 v, uint32_t& h1, uint32_t& h2, uint32_t& h3) {
-  const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E5M2);
-  const float2 af = e5m2x2_to_float2(a);
-  const float2 r1 = make_float2(v.x - af.x, v.y - af.y);
-  const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(r1, __NV_SATFINITE, __NV_E5M2);
-  const float2 bf = e5m2x2_to_float2(b);
-  const float2 r2 = make_float2(r1.x - bf.x, r1.y - bf.y);
-  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(r2, __NV_SATFINITE, __NV_E5M2);
-  h1 = a;
-  h2 = b;
-  h3 = c;
+  const float2 a = make_float2(round3(v.x), round3(v.y));
+  const float2 r1 = make_float2(v.x - a.x, v.y - a.y);
+  const float2 b = make_float2(round3(r1.x), round3(r1.y));
+  const float2 r2 = make_float2(r1.x - b.x, r1.y - b.y);
+  h1 = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E5M2);
+  h2 = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E5M2);
+  h3 = __nv_cvt_float2_to_fp8x2(r2, __NV_SATFINITE, __NV_E5M2);
 }
 
 // Pieces of one lane's four consecutive elements of a group (bf16 bits in
@@ -282,34 +293,25 @@ __device__ __forceinline__ float group_pieces(uint2 raw, float m, uint32_t& h1, 
 
 // The exact part of one group's dot product that the pieces leave out: the sum
 // of w[n][k] * x[k] over the group's elements with 0 < |x| < tau, in fp32
-// (every product is exact).  wp: packed weights, row n, group grp; xg: the
-// group's 128 bf16 values.  Kept out of line: only groups whose values span
-// more than 21 binades call it.
-__device__ __noinline__ float leftover_dot(const uint32_t* __restrict__ wp,
-                                           const uint16_t* __restrict__ xg, int K, int n, int grp,
-                                           float tau) {
-  const uint4* wq = reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 4) + grp * 8);
-  const uint4 wa = ldg_nc_v4(wq), wb = ldg_nc_v4(wq + 1);
-  uint4 xq[16];  // all loads in flight at once
-#pragma unroll
-  for (int i = 0; i < 16; ++i) xq[i] = ldg_nc_v4(xg + 8 * i);
+// (every product is exact).  wrow: row n's 8 packed words of the group; xs:
+// the group's 128 bf16 values (shared memory, two per 32-bit word).
+__device__ __forceinline__ float leftover_dot(uint4 wa, uint4 wb, const uint32_t* xs, float tau) {
   const uint32_t w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
   float acc = 0.f;
-#pragma unroll
+#pragma unroll 1
   for (int j = 0; j < 8; ++j) {  // word j: k = 16 j .. 16 j + 15 of the group
+    uint32_t wj = w[0];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint4 xv = xq[2 * j + c];
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    for (int u = 1; u < 8; ++u)
+      if (u == j) wj = w[u];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int kw = 8 * c + e;  // weight kw of the word: byte kw / 4, position kw % 4
-        const int bit = 8 * (kw >> 2) + ((kw & 3) < 2 ? (kw & 3) : (kw & 3) + 2);
-        const float xf = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
-        const bool nz = (w[j] >> bit) & 1u;
-        const bool neg = (w[j] >> (bit + 2)) & 1u;
-        if (nz && xf != 0.f && fabsf(xf) < tau) acc += neg ? -xf : xf;
-      }
+    for (int e = 0; e < 16; ++e) {
+      const int bit = 8 * (e >> 2) + ((e & 3) < 2 ? (e & 3) : (e & 3) + 2);
+      const uint32_t xw = xs[8 * j + (e >> 1)];
+      const float xf = __uint_as_float((e & 1) ? (xw & 0xFFFF0000u) : (xw << 16));
+      const bool nz = (wj >> bit) & 1u;
+      const bool neg = (wj >> (bit + 2)) & 1u;
+      if (nz && xf != 0.f && fabsf(xf) < tau) acc += neg ? -xf : xf;
     }
   }
   return acc;
@@ -353,6 +355,19 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
   float lsum;
   const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
   uint8_t* st = out + static_cast<size_t>(ks) * C::kXBytes;
+  if constexpr (TT == 1) {
+    // compact block: 16-block j = 8 jg + l/4 at bytes 32 j (piece 0), 32 j + 16
+    // (piece 1) and kX1Sbo + 32 j (piece 2); position b = l%4: value i at 4i + b
+    uint8_t* blk = st + 32 * (8 * jg + (lane >> 2)) + (lane & 3);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      blk[4 * e] = static_cast<uint8_t>(hp[0] >> (8 * e));
+      blk[16 + 4 * e] = static_cast<uint8_t>(hp[1] >> (8 * e));
+      blk[kX1Sbo + 4 * e] = static_cast<uint8_t>(hp[2] >> (8 * e));
+    }
+    if (lane == 0) reinterpret_cast<float2*>(st + kX1Stage)[jg] = make_float2(f, lsum);
+    return;
+  }
   auto put = [&](uint8_t* blk, int n, int slot, uint8_t b) {
     blk[(n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15)] = b;
   };
@@ -380,55 +395,44 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
 }
 
 // ------------------------------------------------------------------ main
-// The units of one CTA in visiting order.  The CTA's contiguous range of
-// units is visited in order, except that when its last row block is shared
-// with the next CTA, that row block's units (its first `head` stages) come
-// first: then both of the CTA's shared row blocks are finished early, and
-// their sums are combined while the rest of the range streams.
+// The units of one CTA: a contiguous range, from stage ks0 of row block rb0.
 struct Visit {
   int KS;      // k stages per row block
   int rb0;     // row block of the range's first unit, and its stage
   int ks0;
-  int rbh;     // the last row block, visited first when head > 0
-  int head;    // units of rbh visited first (0: plain order)
   int nunits;  // units in the range
 };
 
-// (row block, stage) of the unit at visit position v, stepped incrementally.
+// (row block, stage) of the unit at position v of the range, stepped
+// incrementally.
 struct Cursor {
   int rb, ks, v;
   __device__ __forceinline__ void start(const Visit& s) {
     v = 0;
-    rb = s.head ? s.rbh : s.rb0;
-    ks = s.head ? 0 : s.ks0;
+    rb = s.rb0;
+    ks = s.ks0;
   }
   __device__ __forceinline__ void next(const Visit& s) {
-    if (++v == s.head) {
-      rb = s.rb0;
-      ks = s.ks0;
-    } else if (++ks == s.KS) {
+    ++v;
+    if (++ks == s.KS) {
       ks = 0;
       ++rb;
     }
   }
   // this CTA's last unit of row block rb
   __device__ __forceinline__ bool ends_row_block(const Visit& s) const {
-    return v == s.nunits - 1 || v == s.head - 1 || (v >= s.head && ks == s.KS - 1);
+    return v == s.nunits - 1 || ks == s.KS - 1;
   }
 };
 
 // (T = 1) The CTA visits min(nunits, KS) distinct stages, a cyclic run from
-// ks0; stage ks keeps its activation block in slot (ks - ks0) mod KS.
+// ks0; stage ks keeps its activation block in slot (ks - ks0) mod KS, and
+// the i-th stage of the run is new_stage(i).
 __device__ __forceinline__ int stage_slot(const Visit& s, int ks) {
   return ks >= s.ks0 ? ks - s.ks0 : ks + s.KS - s.ks0;
 }
-// The i-th distinct stage in visiting order: the head's stages 0 .. head-1,
-// then the rest of the cyclic run from ks0 without them.
 __device__ __forceinline__ int new_stage(const Visit& s, int i) {
-  if (i < s.head) return i;
-  const int j = i - s.head;
-  if (s.ks0 >= s.head) return j < s.KS - s.ks0 ? s.ks0 + j : s.head + j - (s.KS - s.ks0);
-  return s.head + j;
+  return i < s.KS - s.ks0 ? s.ks0 + i : i - (s.KS - s.ks0);
 }
 
 // wp: the packed weights (read again only for leftovers); x: bf16 activations
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   using C = TC<TT>;
   constexpr int S = C::kStages;
   constexpr int SS = C::kSStages;
-  constexpr int NA = C::kNAH;
+  constexpr int NSUB = C::kNSub;
   constexpr int ND = C::kNDH;
   constexpr int H = C::kH;
   constexpr int NC = C::kNC;
@@ -464,9 +468,11 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   // A slots are used in two halves (sub-slots 2 a and 2 a + 1: groups 0-1
   // and 2-3 of the half-stage), each with its own barriers, so the MMAs on
   // one half overlap the decoding of the other.
-  uint64_t* afull = sempty + SS;     // A sub-slot written by its four decoders
-  uint64_t* afree = afull + 2 * NA;  // MMAs reading A sub-slot completed
-  uint64_t* mdone = afree + 2 * NA;  // MMAs writing D slot d completed
+  // [half][sub-slot]: A sub-slot written by its half's four decoders / the
+  // MMAs reading it completed
+  uint64_t* afull = sempty + SS;
+  uint64_t* afree = afull + 2 * NSUB;
+  uint64_t* mdone = afree + 2 * NSUB;  // MMAs writing D slot d completed
   uint64_t* dfree = mdone + ND;   // D slot d read back by the fold warps
   // fold pairs: [quarter] the half-stage-1 warp's row block sums are in
   // shared memory / have been taken by the half-stage-0 warp
@@ -476,8 +482,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   // CTA's i-th split row block
   uint64_t* pub = pfree + 4;
   uint64_t* xready = pub + 2;  // (T = 1) activation block of slot q built
-  uint8_t* xres = smem + C::kX1Off;                              // (T = 1) blocks
-  float2* ftab = reinterpret_cast<float2*>(smem + C::kFOff);     // (T = 1) (f, L)[slot][kGS]
+  uint8_t* xres = smem + C::kX1Off;  // (T = 1) resident slots: block + (f, L)[kGS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       mbar_init(&sfull[s], 32);
       mbar_init(&sempty[s], kFoldWarps);
     }
-    for (int a = 0; a < 2 * NA; ++a) {
+    for (int a = 0; a < 2 * NSUB; ++a) {
       mbar_init(&afull[a], kDecWarps / 2);
       mbar_init(&afree[a], 1);
     }
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) mbar_init(&pub[i], 4);  // the four half-stage-0 fold warps
     if constexpr (C::kInKernelX)
-      for (int q = 0; q < nslots; ++q) mbar_init(&xready[q], kGS);  // one arrival per group
+      for (int q = 0; q < nslots; ++q) mbar_init(&xready[q], 1);  // the producer's copy
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -528,23 +533,19 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   vs.nunits = static_cast<int>(end - begin);
   vs.rb0 = static_cast<int>(begin / KS);
   vs.ks0 = static_cast<int>(begin - static_cast<long long>(vs.rb0) * KS);
-  vs.rbh = static_cast<int>((end - 1) / KS);
-  {
-    const int ke = static_cast<int>(end - static_cast<long long>(vs.rbh) * KS);
-    vs.head = (vs.rbh != vs.rb0 && ke < KS) ? ke : 0;  // the last row block is shared
-  }
+  const int rb_last = static_cast<int>((end - 1) / KS);
   const int nunits = vs.nunits;
   const int rb0 = vs.rb0, ks0 = vs.ks0;
   auto is_split = [&](int rb) {
     const long long u = static_cast<long long>(rb) * KS;
     return owner_of(u, U, P) != owner_of(u + KS - 1, U, P);
   };
-  // The CTA's split row blocks in the order the fold finishes them: the head
-  // (the last row block), then the first row block (when shared).
+  // The CTA's split row blocks in the order the fold finishes them: the
+  // first row block, then the last (either when shared with another CTA).
   int sp[2];
   int nsp = 0;
-  if (vs.head) sp[nsp++] = vs.rbh;
-  if (is_split(rb0)) sp[nsp++] = rb0;  // (with head == 0 the last row block is not shared)
+  if (is_split(rb0)) sp[nsp++] = rb0;
+  if (rb_last != rb0 && is_split(rb_last)) sp[nsp++] = rb_last;
 
   // Every role but the producer (which first requests the weights of its
   // first stages) waits for the previous grid here, so that no bounded wait
@@ -647,13 +648,6 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
                     xprep + static_cast<size_t>(ks) * C::kXBytes, C::kXFrag, &full[it % S]);
       }
     };
-    auto prefetch_unit = [&](int rb, int ks) {
-      if (lane == 0) {
-#pragma unroll
-        for (int b = 0; b < kWBoxes; ++b)
-          tma_prefetch_2d(&tmW, ks * (kSTStageK / 4) + 128 * b, rb * kRows);
-      }
-    };
     // Weights and scales are not written by the previous kernels of the
     // stream's chain, so the first stages are requested before its end.
     bool ok = true;
@@ -668,11 +662,17 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       cw.next(vs);
     }
     const int su_early = su;
-    // L2 prefetch of the next S units: with it, twice the ring's bytes are on
-    // their way from DRAM while the ring waits for the decoders.
-    Cursor cp = cw;
-    for (; cp.v < nunits && cp.v < it + S; cp.next(vs)) prefetch_unit(cp.rb, cp.ks);
     grid_dependency_wait();
+    // (T = 1) the resident activation slots, in visiting order
+    const int nq = nunits < KS ? nunits : KS;
+    if constexpr (C::kInKernelX) {
+      if (lane == 0)
+        for (int q = 0; q < nq; ++q) {
+          mbar_arrive_expect_tx(&xready[q], kX1Slot);
+          bulk_load(xres + q * kX1Slot,
+                    xprep + static_cast<size_t>(new_stage(vs, q)) * kX1Slot, kX1Slot, &xready[q]);
+        }
+    }
     if constexpr (!C::kInKernelX) {
       Cursor ce;
       ce.start(vs);
@@ -686,7 +686,6 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (it >= S && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((it / S) & 1) ^ 1, err))) break;
       issue_weights(it, cw.rb, cw.ks);
       issue_x(it, cw.ks);
-      if (cp.v < nunits) prefetch_unit(cp.rb, cp.ks);
       if (su < nunits) {
         const int fks = cs.ks;
         const int fu = su;
@@ -694,93 +693,91 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         if (ok) issue_f(fu, fks);
       }
       cw.next(vs);
-      cp.next(vs);
     }
     // Stay until this CTA's copies have landed (bounded).
     for (int d = (it > S ? it - S : 0); d < it; ++d)
       if (!mbar_wait(&full[d % S], (d / S) & 1, err)) break;
     for (int d = (su > SS ? su - SS : 0); d < su; ++d)
       if (!mbar_wait(&sfull[d % SS], (d / SS) & 1, err)) break;
-  } else if (warp >= kXWarp0) {
-    // ------------------------------------------------------------ activations (T = 1)
-    // Activation warp xw builds groups xw and xw + 4 of every distinct stage
-    // the CTA visits, in visiting order, once: lane l splits k = 128 g + 4l ..
-    // +3 of the stage.  Item qi is group xw + 4 (qi & 1) of the (qi >> 1)-th
-    // distinct stage.
-    if constexpr (C::kInKernelX) {
-      const int xw = warp - kXWarp0;
-      const uint16_t* xt = x + static_cast<size_t>(tok0) * K;
-      const int nq = nunits < KS ? nunits : KS;
-      const int nitems = 2 * nq;
-      // loads of the next kXLoads items stay in flight while one is built
-      constexpr int kXLoads = 8;
-      uint2 raw[kXLoads];
-      auto load_item = [&](int qi) -> uint2 {
-        if (qi >= nitems) return make_uint2(0, 0);
-        const int ks = new_stage(vs, qi >> 1);
-        const int k = ks * kSTStageK + 128 * (xw + 4 * (qi & 1)) + 4 * lane;
-        return k < K ? *reinterpret_cast<const uint2*>(xt + k) : make_uint2(0, 0);
-      };
-#pragma unroll
-      for (int j = 0; j < kXLoads; ++j) raw[j] = load_item(j);
-      for (int q0 = 0; q0 < nitems; q0 += kXLoads) {
-#pragma unroll
-        for (int j = 0; j < kXLoads; ++j) {
-          const int qi = q0 + j;
-          if (qi >= nitems) break;
-          const int q = stage_slot(vs, new_stage(vs, qi >> 1));
-          const int g = xw + 4 * (qi & 1);
-          const uint2 cur = raw[j];
-          raw[j] = load_item(qi + kXLoads);
-          float m = fmaxf(fmaxf(fabsf(__uint_as_float(cur.x << 16)),
-                                fabsf(__uint_as_float(cur.x & 0xFFFF0000u))),
-                          fmaxf(fabsf(__uint_as_float(cur.y << 16)),
-                                fabsf(__uint_as_float(cur.y & 0xFFFF0000u))));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          uint32_t h1, h2, h3;  // byte i: piece of k = 4l + i
-          float lsum;
-          const float f = group_pieces(cur, m, h1, h2, h3, lsum);
-          // 16-block j = 8 g + l/4 (column bytes 32 j, 32 j + 16, kX1Sbo + 32 j),
-          // position b = l%4: value i goes to byte 4i + b
-          uint8_t* blk = xres + q * kX1Stage + 32 * (8 * g + (lane >> 2)) + (lane & 3);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            blk[4 * i] = static_cast<uint8_t>(h1 >> (8 * i));
-            blk[16 + 4 * i] = static_cast<uint8_t>(h2 >> (8 * i));
-            blk[kX1Sbo + 4 * i] = static_cast<uint8_t>(h3 >> (8 * i));
-          }
-          if (lane == 0) ftab[q * kGS + g] = make_float2(f, lsum);
-          fence_proxy_async_smem();  // the MMA reads the block through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&xready[q]);
-        }
-      }
-    }
+    if constexpr (C::kInKernelX)
+      for (int q = 0; q < nq; ++q)
+        if (!mbar_wait(&xready[q], 0, err)) break;
+  } else if (warp == kXWarp0) {
     // ------------------------------------------------------------ split-row sums
-    // Warp kXWarp0 (at T = 1 once its activation blocks are built) combines
-    // the CTA's split row blocks as the fold publishes them: it takes the
-    // row block's ticket (kept at the index of its first CTA); if every other
-    // CTA of the row block has already taken it, this CTA adds all partials
-    // in CTA order and writes y, and puts the ticket back to zero for the next
-    // launch.  The fold never waits for any of this.
-    if (warp == kXWarp0) {
+    // Warp kXWarp0 combines
+    // the CTA's split row blocks as the fold hands over their sums, with a
+    // ticket per row block (kept at the index of its first CTA).  The fold
+    // never waits for any of this, and no CTA waits for another to start.
+    //  - Two CTAs share the row block: the first to take the ticket stores its
+    //    sums to y and marks the ticket; the second waits for that mark (the
+    //    first is running: it has its ticket) and adds its sums with fp32
+    //    atomic adds.  y = RN(a + b) = RN(b + a): the same bits either way.
+    //  - More CTAs: each publishes its sums to the workspace and takes the
+    //    ticket; the last adds every partial in CTA order and writes y.
+    // The CTA that finishes puts the ticket back to zero for the next launch.
+    {
       auto first_rb = [&](int c) { return static_cast<int>(U * c / P / KS); };
+      const float* split_sums = reinterpret_cast<const float*>(smem + C::kSplitOff);
       for (int i = 0; i < nsp; ++i) {
         const int rb = sp[i];
         if (!__all_sync(0xffffffffu, mbar_wait(&pub[i], 0, err))) break;
         const long long u0 = static_cast<long long>(rb) * KS;
         const int c0 = owner_of(u0, U, P), c1 = owner_of(u0 + KS - 1, U, P);
-        int last = 0;
-        if (lane == 0) {
-          __threadfence();
-          last = atomicAdd(&tickets[c0], 1) == c1 - c0;
-          if (last) atomicExch(&tickets[c0], 0);
+        const float* mine = split_sums + i * TT * kRows;  // [TT][128] in shared memory
+        const int n = rb * kRows + 4 * lane;               // lane l: rows 4l .. 4l+3
+        if (c1 - c0 == 1) {
+          int old = 0;
+          if (lane == 0) old = atomic_add_acq_rel_gpu(&tickets[c0], 1);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if ((old & 0xFFFF) == 0) {
+            for (int t = 0; t < Tt; ++t) {
+              const float4 v = reinterpret_cast<const float4*>(mine + t * kRows)[lane];
+              float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
+              const float a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (n + e < N) yr[e] = a[e];
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(&tickets[c0], 1 << 16);  // stored
+          } else {
+            bool fine = true;
+            if (lane == 0 && (old >> 16) == 0) fine = wait_word_high_nonzero(&tickets[c0], err);
+            fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
+            __syncwarp();
+            if (!fine) break;
+            for (int t = 0; t < Tt; ++t) {
+              const float4 v = reinterpret_cast<const float4*>(mine + t * kRows)[lane];
+              float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
+              const float a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (n + e < N) atomicAdd(yr + e, a[e]);
+            }
+            if (lane == 0) tickets[c0] = 0;
+          }
+          continue;
         }
-        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
-        __threadfence();
-        // lane l sums rows 4l .. 4l+3, four tokens and up to four CTAs' loads
-        // in flight at a time, adding the CTAs' partials in CTA order
+        // publish this CTA's sums (slot 0: its first row block, 1: its last)
+        {
+          const float4* src = reinterpret_cast<const float4*>(mine);
+          float4* dst = reinterpret_cast<float4*>(
+              partials + static_cast<size_t>(cta * 2 + (rb == rb0 ? 0 : 1)) * TT * kRows);
+#pragma unroll
+          for (int e = 0; e < TT; ++e) dst[e * 32 + lane] = src[e * 32 + lane];
+          __threadfence();
+          __syncwarp();
+        }
+        // the ticket: acquire-release at GPU scope (every lane fenced its part
+        // of the partial first; a last arriver reads the others' after)
+        int last = 0;
+        if (lane == 0) last = atomic_add_acq_rel_gpu(&tickets[c0], 1) == c1 - c0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (!last) continue;
+        // four tokens and up to four CTAs' loads in flight at a time, the
+        // CTAs' partials added in CTA order
         constexpr int kTC = TT < 4 ? TT : 4;
         for (int t0 = 0; t0 < Tt; t0 += kTC) {
           float4 acc[kTC];
@@ -809,22 +806,22 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 #pragma unroll
           for (int tj = 0; tj < kTC; ++tj) {
             if (t0 + tj >= Tt) continue;
-            float* yr = y + static_cast<size_t>(tok0 + t0 + tj) * N + rb * kRows + 4 * lane;
-            const int n = rb * kRows + 4 * lane;
+            float* yr = y + static_cast<size_t>(tok0 + t0 + tj) * N + n;
             const float a[4] = {acc[tj].x, acc[tj].y, acc[tj].z, acc[tj].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               if (n + e < N) yr[e] = a[e];
           }
         }
+        if (lane == 0) tickets[c0] = 0;  // every other CTA has taken it: ready for the next launch
       }
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
     // ------------------------------------------------------------ MMA issuers
     // Each warp runs its loop whole so that addresses and descriptors stay
     // warp-uniform; one elected lane issues.  Half-stage hu = 2 it + hh
-    // (groups 4 hh .. 4 hh + 3) uses A slot hu % NA and D slot hu % ND and is
-    // issued by MMA warp hh.
+    // (groups 4 hh .. 4 hh + 3) uses A sub-slots (2 it + b) % NSUB of half
+    // hh's ring (b = 0, 1) and D slot hu % ND, and is issued by MMA warp hh.
     const int w = warp - kMmaWarp;
     const bool leader = elect_one();
     constexpr uint32_t idesc = idesc_e4m3_e5m2_f32(kRows, NC);
@@ -845,26 +842,27 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       const int ng = G - kGS * ks < kGS ? G - kGS * ks : kGS;
       const int q = stage_slot(vs, ks);  // (T = 1) resident slot
       const uint64_t dstage =
-          desc0 + static_cast<uint64_t>((C::kInKernelX ? q * kX1Stage : s * C::kXFrag) >> 4);
+          desc0 + static_cast<uint64_t>((C::kInKernelX ? q * kX1Slot : s * C::kXFrag) >> 4);
       const uint64_t dstage3 = dstage + static_cast<uint64_t>(C::kXMain >> 4);
       if constexpr (C::kInKernelX) {
         if (!__all_sync(0xffffffffu, mbar_wait(&xready[q], 0, err))) break;
       }
-      const int a = hu % NA;
       const int d = hu % ND;
       if (hu >= ND &&
           !__all_sync(0xffffffffu, mbar_wait(&dfree[d], ((hu / ND) & 1) ^ 1, err)))
         break;
       const uint32_t dcol = tbase + C::kDCol + d * C::kDSlot;
-      const uint32_t acol = tbase + C::kACol + a * C::kASlot;
       bool ok_h = true;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {  // the two A sub-slots of the half-stage
-        if (!__all_sync(0xffffffffu, mbar_wait(&afull[2 * a + b], (hu / NA) & 1, err))) {
+        const int u = 2 * it + b, j = u % NSUB;
+        uint64_t* af = &afull[hh * NSUB + j];
+        if (!__all_sync(0xffffffffu, mbar_wait(af, (u / NSUB) & 1, err))) {
           ok_h = false;
           break;
         }
         tc_fence_after();
+        const uint32_t acol = tbase + C::kACol + hh * C::kAHalf + j * C::kSubCols;
         if (leader) {
 #pragma unroll
           for (int gs = 0; gs < kGH / 2; ++gs) {
@@ -874,15 +872,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t koff = static_cast<uint64_t>(((8 * g + 2 * kk) * kLbo) >> 4);
-                mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8, dstage + koff, idesc,
+                mma_f8f6f4_ts(dcol + gg * NC, acol + gs * 32 + kk * 8, dstage + koff, idesc,
                               kk > 0);
                 if constexpr (C::kH3)  // piece 2 onto piece 0's columns
-                  mma_f8f6f4_ts(dcol + gg * NC, acol + gg * 32 + kk * 8, dstage3 + koff, idesc3,
+                  mma_f8f6f4_ts(dcol + gg * NC, acol + gs * 32 + kk * 8, dstage3 + koff, idesc3,
                                 true);
               }
             }
           }
-          mma_commit(&afree[2 * a + b]);
+          mma_commit(&afree[hh * NSUB + j]);
         }
         __syncwarp();
       }
@@ -912,28 +910,40 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     cu.start(vs);
     for (int it = 0; it < nunits; ++it, cu.next(vs)) {
       const int s = it % S;
-      const int hu = 2 * it + h;  // this warp's half-stage
-      const int a = hu % NA;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (it / S) & 1, err))) break;
-      // half-stage h is weight box h: groups kGH h .. kGH h + kGH - 1
+      // half-stage h is weight box h: groups kGH h .. kGH h + kGH - 1.  All
+      // of this warp's packed words of the unit go to registers first, so
+      // that the ring slot is handed back to the producer at once (the slot
+      // of a T > 1 stage also holds the activation block: there the MMA
+      // commits release it).
       const uint8_t* wrow = smem + C::kWOff + s * C::kWBytes + h * (kRows * 128) + r * 128;
       const int ng = G - kGS * cu.ks < kGS ? G - kGS * cu.ks : kGS;
+      uint4 wv[kGH][2];
+#pragma unroll
+      for (int gg = 0; gg < kGH; ++gg) {
+        wv[gg][0] = lds_v4(wrow + (((2 * gg) ^ (r & 7)) << 4));
+        wv[gg][1] = lds_v4(wrow + (((2 * gg + 1) ^ (r & 7)) << 4));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
       bool ok_h = true;
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {  // A sub-slot b: groups 2 b, 2 b + 1 of the half-stage
-        if (hu >= NA &&
-            !__all_sync(0xffffffffu, mbar_wait(&afree[2 * a + b], ((hu / NA) & 1) ^ 1, err))) {
+      for (int b = 0; b < 2; ++b) {  // groups 2 b, 2 b + 1 of the half-stage
+        const int u = 2 * it + b, j = u % NSUB;  // into sub-slot j of this half's ring
+        if (u >= NSUB &&
+            !__all_sync(0xffffffffu,
+                        mbar_wait(&afree[h * NSUB + j], ((u / NSUB) & 1) ^ 1, err))) {
           ok_h = false;
           break;
         }
         tc_fence_after();
+        const uint32_t acol = tbase + lane_off + C::kACol + h * C::kAHalf + j * C::kSubCols;
 #pragma unroll
         for (int gs = 0; gs < kGH / 2; ++gs) {
           const int gg = (kGH / 2) * b + gs;
           const int g = kGH * h + gg;
           if (g < ng) {
-            const uint4 c0 = lds_v4(wrow + (((2 * gg) ^ (r & 7)) << 4));
-            const uint4 c1 = lds_v4(wrow + (((2 * gg + 1) ^ (r & 7)) << 4));
+            const uint4 c0 = wv[gg][0], c1 = wv[gg][1];
             const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             uint32_t av[32];
 #pragma unroll
@@ -943,16 +953,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
               av[4 * j + 2] = decode_e4m3<2>(w[j]);
               av[4 * j + 3] = decode_e4m3<3>(w[j]);
             }
-            tmem_st32(tbase + lane_off + C::kACol + a * C::kASlot + gg * 32, av);
+            tmem_st32(acol + gs * 32, av);
           }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[2 * a + b]);
+        if (lane == 0) mbar_arrive(&afull[h * NSUB + j]);
       }
       if (!ok_h) break;
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
   } else {
     // ------------------------------------------------------------ fold
@@ -968,11 +977,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // their contribution is at most s * L.  The running sum |yacc| of this
     // warp's groups is a lower bound of sum|s w x| over those groups (every
     // term added is an exact part of y, or the pieces' sum, bounded by its own
-    // sum of |s w x|), so while the dropped bounds add up to at most 2^-12 of
-    // it the leftovers are left out: the error stays below 2^-12 of
-    // sum|s w x|.  Otherwise they are added exactly (leftover_dot).  One budget
+    // sum of |s w x|), so while the dropped bounds add up to at most 2^-11 of
+    // it the leftovers are left out: the error stays below 2^-11 of
+    // sum|s w x|, half the bf16 rungs' bar.  Otherwise they are added exactly
+    // (leftover_dot, on the group's x staged in shared memory).  One budget
     // lam serves all tokens of a row: a token's own dropped bounds never
-    // exceed lam, which each drop keeps within 2^-12 of that token's |yacc|.
+    // exceed lam, which each drop keeps within 2^-11 of that token's |yacc|.
     const int fq = (warp - kDecWarps) & 3;  // == warp % 4
     const int fh = (warp - kDecWarps) >> 2;
     const int r = fq * 32 + lane;
@@ -983,6 +993,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     for (int t = 0; t < TT; ++t) yacc[t] = 0.f;
 
     float* half_part = reinterpret_cast<float*>(smem + C::kPartOff);  // [TT][128]
+    float* split_sums = reinterpret_cast<float*>(smem + C::kSplitOff);  // [2][TT][128]
+    uint2* lx = reinterpret_cast<uint2*>(smem + C::kLxOff) + (warp - kDecWarps) * 32;
     int nflush = 0;
     int nsplit = 0;
     // Row block rb's sums are final in yacc (fh = 0 warps): a row block whole
@@ -1007,11 +1019,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfree[fq]);
         if (nsplit < nsp && rb == sp[nsplit]) {
-          float* mine =
-              partials + static_cast<size_t>(cta * 2 + (rb == rb0 ? 0 : 1)) * TT * kRows;
+          float* mine = split_sums + nsplit * TT * kRows;
 #pragma unroll
           for (int t = 0; t < TT; ++t) mine[t * kRows + r] = yacc[t];
-          __threadfence();
           __syncwarp();
           if (lane == 0) mbar_arrive(&pub[nsplit]);
           ++nsplit;
@@ -1048,7 +1058,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       // (f, L) of group g (within the stage), token t
       auto fl_of = [&](int g, int t) -> float2 {
         if constexpr (C::kInKernelX) {
-          return ftab[q * kGS + g];
+          return reinterpret_cast<const float2*>(xres + q * kX1Slot + kX1Stage)[g];
         } else {
           const float* fl = reinterpret_cast<const float*>(sst + kRows * 2 * kGS);
           return make_float2(fl[g * H + t], fl[(kGS + g) * H + t]);
@@ -1062,14 +1072,15 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], (hu / ND) & 1, err))) break;
       tc_fence_after();
       const uint32_t dbase = tbase + lane_off + C::kDCol + d * C::kDSlot;
-      // (warp-uniform) sign bit set: some group of the half-stage has
-      // leftovers for some token (an OR of the factors' bits)
-      uint32_t fbits = 0;
+      // (warp-uniform) bit gg: group gg of the half-stage has leftovers for
+      // some token (from an OR of the factors' sign bits)
+      uint32_t gflag = 0;
       // Only the accumulator columns that carry tokens are read back; dv[]
       // holds them with piece j of token t at dv[PJ[j] + t].
       auto fold_group = [&](int gg, const uint32_t* dv) {
         const float sg = scale_of(gg);
         const int g = kGH * fh + gg;
+        uint32_t fbits = 0;
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           float dsum;
@@ -1084,6 +1095,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
           fbits |= __float_as_uint(f);
           yacc[t] = fmaf(sg * fabsf(f), dsum, yacc[t]);
         }
+        gflag |= (fbits >> 31) << gg;
       };
       static_assert(NC == 16 || NC == 32, "accumulator width");
       static_assert(TT == 1 || TT == 4 || TT == 8 || TT == 16, "token tiles");
@@ -1130,29 +1142,45 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         for (int gg = 0; gg < kGH; ++gg)
           if (kGH * fh + gg < ng) fold_group(gg, dv[gg]);
       }
-      if (fbits >> 31) {  // rare: groups with leftovers (see above)
+      if (gflag) {  // rare: groups with leftovers (see above)
         const int n = cu.rb * kRows + r;
 #pragma unroll 1
         for (int bit = 0; bit < kGH * TT; ++bit) {
           const int gg = bit / TT, t = bit % TT;
+          if (!((gflag >> gg) & 1u)) continue;
           const int g = kGH * fh + gg;
-          if (g >= ng) break;
           const float2 fl = fl_of(g, t);
           if (!(fl.x < 0.f)) continue;
           const float sg = scale_of(gg);
-          const float bound = sg * fl.y;
+          const float bound = sg * fl.y;  // |leftover contribution| <= bound
           float acc = yacc[0];
 #pragma unroll
           for (int u = 1; u < TT; ++u)
             if (u == t) acc = yacc[u];
-          if (lam + bound <= 0x1p-12f * fabsf(acc)) {
-            lam += bound;
-          } else if (n < N && t < Tt) {
+          const bool drop = lam + bound <= 0x1p-11f * fabsf(acc);
+          const bool exact = !drop && n < N && t < Tt;
+          if (drop) lam += bound;
+          if (__any_sync(0xffffffffu, exact)) {
+            // the group's x into this warp's staging area, the row's weights
+            // at the same time: one memory round trip
             const int ga = ks * kGS + g;
-            acc = fmaf(sg,
-                       leftover_dot(wp, x + static_cast<size_t>(tok0 + t) * K + ga * 128, K, n,
-                                    ga, leftover_limit(-fl.x)),
-                       acc);
+            const uint2 xv = *reinterpret_cast<const uint2*>(
+                x + static_cast<size_t>(tok0 + t) * K + ga * 128 + 4 * lane);
+            uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
+            if (exact) {
+              const uint4* wq =
+                  reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 4) + ga * 8);
+              wa = ldg_nc_v4(wq);
+              wb = ldg_nc_v4(wq + 1);
+            }
+            lx[lane] = xv;
+            __syncwarp();
+            if (exact)
+              acc = fmaf(sg,
+                         leftover_dot(wa, wb, reinterpret_cast<const uint32_t*>(lx),
+                                      leftover_limit(-fl.x)),
+                         acc);
+            __syncwarp();
           }
 #pragma unroll
           for (int u = 0; u < TT; ++u)
@@ -1227,7 +1255,7 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   uint8_t* xprep = work + smallt_partials_bytes(TT);
 
   cudaLaunchAttribute attr[1];
-  if constexpr (!C::kInKernelX) {
+  {
     const int tasks = C::kH * kGS * g.KS;
     cudaLaunchConfig_t pc = pdl_config(attr, dim3((tasks + 7) / 8), dim3(256), 0, stream);
     cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
@@ -1250,7 +1278,7 @@ size_t smallt_work_bytes(int tt, int K) {
   const int KS = (K + kSTStageK - 1) / kSTStageK;
   size_t prep = 0;
   switch (tt) {
-    case 1: prep = 0; break;  // built inside the main kernel
+    case 1: prep = static_cast<size_t>(TC<1>::kXBytes) * KS; break;
     case 4: prep = static_cast<size_t>(TC<4>::kXBytes) * KS; break;
     case 8: prep = static_cast<size_t>(TC<8>::kXBytes) * KS; break;
     default: prep = static_cast<size_t>(TC<16>::kXBytes) * KS; break;

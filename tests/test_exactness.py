@@ -90,6 +90,42 @@ def test_rne_e5m2_agrees_with_torch():
         [1.0, 1.5, 0.0, 2.0 ** -15]
 
 
+def _round3_fp32(x):
+    """The kernels' round3 in fp32: (x + c) - c with c = 1.5 * 2^(exp(x) + 21)."""
+    x = np.asarray(x, dtype=np.float32)
+    e = x.view(np.uint32) & np.uint32(0x7F800000)
+    c = ((e + np.uint32(21 << 23)) | np.uint32(0x00400000)).view(np.float32)
+    return ((x + c) - c).astype(np.float64)
+
+
+def test_round3_is_rne_to_e5m2_on_the_pieces_range():
+    # every fp32 value with at most 12 significant bits in [2^-14, 2^15), both
+    # signs: round3 equals e5m2 round to nearest even (and 0 stays 0)
+    mant = np.arange(0, 1 << 11, dtype=np.uint32) << np.uint32(12)
+    exps = np.arange(127 - 14, 127 + 15, dtype=np.uint32) << np.uint32(23)
+    bits = (exps[:, None] | mant[None, :]).ravel()
+    v = bits.view(np.float32)
+    v = np.concatenate([v, -v, np.zeros(1, np.float32)])
+    assert np.array_equal(_round3_fp32(v), rne_e5m2(v.astype(np.float64)))
+
+
+def _three_pieces_round3(v):
+    v32 = v.astype(np.float32)
+    h1 = _round3_fp32(v32)
+    r1 = v32 - h1.astype(np.float32)
+    h2 = _round3_fp32(r1)
+    r2 = r1 - h2.astype(np.float32)
+    return h1, h2, r2.astype(np.float64)
+
+
+def test_kernel_split_formula_matches_the_definition():
+    v = _all_bf16_between(2.0 ** -7, 2.0 ** 15)
+    h1, h2, h3, _, _ = _three_pieces(v)
+    g1, g2, g3 = _three_pieces_round3(v)
+    assert np.array_equal(g1, h1) and np.array_equal(g2, h2) and np.array_equal(g3, h3)
+    assert np.array_equal(rne_e5m2(g3), g3)  # the last piece is an e5m2 value
+
+
 def _three_pieces(v):
     """The kernels' split in fp32: pieces and the two fp32 remainders."""
     v32 = v.astype(np.float32)
