@@ -86,6 +86,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// One load of *p with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Wait until *ctr >= target (acquire, GPU scope).  Gives up after
 // kWaitLimitNs: ORs kErrTimeout into *err and returns false.
 __device__ __forceinline__ bool wait_counter_at_least(const unsigned long long* ctr,
@@ -109,22 +116,6 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
   asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                : "memory");
   return old;
-}
-
-// Wait until the upper 16 bits of *p are nonzero (acquire, GPU scope).  Gives
-// up after kWaitLimitNs: ORs kErrTimeout into *err and returns false.
-__device__ __forceinline__ bool wait_word_high_nonzero(const int* p, int* err) {
-  unsigned long long t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if ((v >> 16) != 0) return true;
-    if (it == 0) t0 = global_timer_ns();
-    else if ((it & 15u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
 }
 
 // ---------------------------------------------------------------- TMA

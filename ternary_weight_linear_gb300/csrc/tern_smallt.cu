@@ -184,7 +184,11 @@ struct TC {
   static constexpr int kSplitOff = kPartOff + TT * kRows * 4;
   // fold: one group of x per fold warp for exact leftovers [kFoldWarps][128] bf16
   static constexpr int kLxOff = kSplitOff + 2 * TT * kRows * 4;
-  static constexpr int kX1Off = (kLxOff + kFoldWarps * 256 + 127) / 128 * 128;  // (T = 1)
+  // fold: the leftover groups each fold warp has left out of its current row
+  // block, decided when the row block ends [kFoldWarps][kDefer] (code, |f|)
+  static constexpr int kDefer = 8;
+  static constexpr int kDefOff = kLxOff + kFoldWarps * 256;
+  static constexpr int kX1Off = (kDefOff + kFoldWarps * kDefer * 8 + 127) / 128 * 128;  // (T = 1)
   // shared memory for nslots resident T = 1 blocks: fixed part, blocks, alignment slack
   static constexpr int smem_bytes(int nslots) {
     return kX1Off + (kInKernelX ? nslots * kX1Slot : 0) + 1024;
@@ -324,28 +328,21 @@ __device__ __forceinline__ int owner_of(long long u, long long U, long long P) {
 }
 
 // ------------------------------------------------------------------ prep
-// Activation blocks of one token tile for all stages (T > 1).  One warp per
-// (token slot t < H, 128-wide group).  Lane l holds k = 4l .. 4l+3 of the
-// group.  Slot order inside each 16-wide block of k is the transpose the
-// decoder produces: slot 4i + b holds k = 4b + i.
+// Activation blocks of one token tile for all stages.  One warp per (token
+// slot t < H, 128-wide group), kPrepWarps warps per CTA looping over the
+// tasks, at most one CTA per SM: 4 warps of 32 registers and no shared memory
+// fit beside a resident main-kernel CTA (640 threads of at most 96
+// registers, at most 226 KB of shared memory), so a launch queued behind the
+// main kernel of the previous call takes no SM from the next one.  Lane l
+// holds k = 4l .. 4l+3 of the group.  Slot order inside each 16-wide block of
+// k is the transpose the decoder produces: slot 4i + b holds k = 4b + i.
+constexpr int kPrepWarps = 4;
+
 template <int TT>
-__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ x,
-                                                    uint8_t* __restrict__ out, int K, int tok0,
-                                                    int Tt, int KS) {
-  grid_dependents_launch();
-  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
+__device__ __forceinline__ void prep_task(uint2 raw, uint8_t* __restrict__ out, int t, int gi,
+                                          int lane) {
   using C = TC<TT>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int task = blockIdx.x * 8 + warp;
-  const int groups = kGS * KS;
-  if (task >= C::kH * groups) return;
-  const int t = task / groups;
-  const int gi = task % groups;
   const int ks = gi / kGS, jg = gi % kGS;
-  const int kbase = gi * 128 + 4 * lane;
-  uint2 raw = make_uint2(0u, 0u);
-  if (t < Tt && kbase < K)
-    raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
   const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
   float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -366,31 +363,60 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
       blk[kX1Sbo + 4 * e] = static_cast<uint8_t>(hp[2] >> (8 * e));
     }
     if (lane == 0) reinterpret_cast<float2*>(st + kX1Stage)[jg] = make_float2(f, lsum);
-    return;
-  }
-  auto put = [&](uint8_t* blk, int n, int slot, uint8_t b) {
-    blk[(n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15)] = b;
-  };
+  } else {
+    auto put = [&](uint8_t* blk, int n, int slot, uint8_t b) {
+      blk[(n >> 3) * kXSbo + (slot >> 4) * kXLbo + (n & 7) * 16 + (slot & 15)] = b;
+    };
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    // k = 4 lane + i: 16-block lane/4, position b = lane%4, i -> slot 4i + b
-    const int slot = 128 * jg + 16 * (lane >> 2) + 4 * i + (lane & 3);
-    const uint8_t b0 = static_cast<uint8_t>(hp[0] >> (8 * i));
-    const uint8_t b1 = static_cast<uint8_t>(hp[1] >> (8 * i));
-    const uint8_t b2 = static_cast<uint8_t>(hp[2] >> (8 * i));
-    put(st, t, slot, b0);
-    put(st, C::kP1 + t, slot, b1);
-    if constexpr (C::kH3) {
-      put(st + C::kXMain, t, slot, b2);
-      if constexpr (TT == 8) put(st + C::kXMain, 8 + t, slot, 0);  // the block's idle columns
-    } else {
-      put(st, C::kP2 + t, slot, b2);
+    for (int i = 0; i < 4; ++i) {
+      // k = 4 lane + i: 16-block lane/4, position b = lane%4, i -> slot 4i + b
+      const int slot = 128 * jg + 16 * (lane >> 2) + 4 * i + (lane & 3);
+      const uint8_t b0 = static_cast<uint8_t>(hp[0] >> (8 * i));
+      const uint8_t b1 = static_cast<uint8_t>(hp[1] >> (8 * i));
+      const uint8_t b2 = static_cast<uint8_t>(hp[2] >> (8 * i));
+      put(st, t, slot, b0);
+      put(st, C::kP1 + t, slot, b1);
+      if constexpr (C::kH3) {
+        put(st + C::kXMain, t, slot, b2);
+        if constexpr (TT == 8) put(st + C::kXMain, 8 + t, slot, 0);  // the block's idle columns
+      } else {
+        put(st, C::kP2 + t, slot, b2);
+      }
+    }
+    if (lane == 0) {
+      float* fl = reinterpret_cast<float*>(st + C::kXFrag);
+      fl[jg * C::kH + t] = f;
+      fl[(kGS + jg) * C::kH + t] = lsum;
     }
   }
-  if (lane == 0) {
-    float* fl = reinterpret_cast<float*>(st + C::kXFrag);
-    fl[jg * C::kH + t] = f;
-    fl[(kGS + jg) * C::kH + t] = lsum;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16_t* __restrict__ x,
+                                                               uint8_t* __restrict__ out, int K,
+                                                               int tok0, int Tt, int KS) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = kGS * KS;
+  const int tasks = TC<TT>::kH * groups;
+  const int stride = gridDim.x * kPrepWarps;
+  // two tasks' loads in flight before their arithmetic
+  for (int t0 = blockIdx.x * kPrepWarps + warp; t0 < tasks; t0 += 2 * stride) {
+    uint2 raw[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int task = t0 + u * stride;
+      const int t = task / groups, kbase = (task % groups) * 128 + 4 * lane;
+      raw[u] = make_uint2(0u, 0u);
+      if (task < tasks && t < Tt && kbase < K)
+        raw[u] = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K + kbase);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int task = t0 + u * stride;
+      if (task < tasks) prep_task<TT>(raw[u], out, task / groups, task % groups, lane);
+    }
   }
 }
 
@@ -707,56 +733,74 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // Warp kXWarp0 combines
     // the CTA's split row blocks as the fold hands over their sums, with a
     // ticket per row block (kept at the index of its first CTA).  The fold
-    // never waits for any of this, and no CTA waits for another to start.
-    //  - Two CTAs share the row block: the first to take the ticket stores its
-    //    sums to y and marks the ticket; the second waits for that mark (the
-    //    first is running: it has its ticket) and adds its sums with fp32
-    //    atomic adds.  y = RN(a + b) = RN(b + a): the same bits either way.
-    //  - More CTAs: each publishes its sums to the workspace and takes the
-    //    ticket; the last adds every partial in CTA order and writes y.
-    // The CTA that finishes puts the ticket back to zero for the next launch.
+    // never waits for any of this, and no CTA waits for another: each CTA
+    // publishes its sums to the workspace and takes the ticket; the last adds
+    // every partial in CTA order and writes y, so the bits do not depend on
+    // which CTA finished last.  It puts the ticket back to zero for the next
+    // launch.
+    //   A row block shared with one other CTA and begun here is this CTA's
+    // last; the other CTA starts with it and usually publishes long before
+    // this one is done.  So while the fold works, this warp polls the ticket
+    // and, once the other's partial is out, copies it into the free split
+    // slot; the end of the row block is then an add and the stores.  (When
+    // the poll finds nothing by then, the general way applies.)
     {
       auto first_rb = [&](int c) { return static_cast<int>(U * c / P / KS); };
-      const float* split_sums = reinterpret_cast<const float*>(smem + C::kSplitOff);
+      float* split_sums = reinterpret_cast<float*>(smem + C::kSplitOff);
       for (int i = 0; i < nsp; ++i) {
         const int rb = sp[i];
-        if (!__all_sync(0xffffffffu, mbar_wait(&pub[i], 0, err))) break;
         const long long u0 = static_cast<long long>(rb) * KS;
         const int c0 = owner_of(u0, U, P), c1 = owner_of(u0 + KS - 1, U, P);
         const float* mine = split_sums + i * TT * kRows;  // [TT][128] in shared memory
         const int n = rb * kRows + 4 * lane;               // lane l: rows 4l .. 4l+3
-        if (c1 - c0 == 1) {
-          int old = 0;
-          if (lane == 0) old = atomic_add_acq_rel_gpu(&tickets[c0], 1);
-          old = __shfl_sync(0xffffffffu, old, 0);
-          if ((old & 0xFFFF) == 0) {
-            for (int t = 0; t < Tt; ++t) {
-              const float4 v = reinterpret_cast<const float4*>(mine + t * kRows)[lane];
-              float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
-              const float a[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (n + e < N) yr[e] = a[e];
+        // slot 1 - i is free here: slot 0 is published before slot 1 is
+        // used, and with one split row block slot 1 is never used
+        float* other = split_sums + (1 - i) * TT * kRows;
+        bool early = false;
+        if (c1 - c0 == 1 && cta == c0 && i == nsp - 1) {
+          const unsigned long long t0 = global_timer_ns();
+          bool fine = true;
+          for (;;) {
+            const bool ready = __any_sync(0xffffffffu, mbar_try_wait(&pub[i], 0));
+            if (!early) {
+              int tk = 0;
+              if (lane == 0) tk = ld_acquire_gpu(&tickets[c0]);
+              tk = __shfl_sync(0xffffffffu, tk, 0);
+              __syncwarp();
+              if (tk == 1) {  // CTA c1 has published (its first row block: slot 0)
+                const float* pc = partials + static_cast<size_t>(c1) * 2 * TT * kRows + 4 * lane;
+                for (int t = 0; t < Tt; ++t)
+                  *reinterpret_cast<float4*>(other + t * kRows + 4 * lane) =
+                      __ldcg(reinterpret_cast<const float4*>(pc + t * kRows));
+                early = true;
+              }
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) atomicAdd(&tickets[c0], 1 << 16);  // stored
-          } else {
-            bool fine = true;
-            if (lane == 0 && (old >> 16) == 0) fine = wait_word_high_nonzero(&tickets[c0], err);
-            fine = __shfl_sync(0xffffffffu, fine ? 1 : 0, 0) != 0;
-            __syncwarp();
-            if (!fine) break;
-            for (int t = 0; t < Tt; ++t) {
-              const float4 v = reinterpret_cast<const float4*>(mine + t * kRows)[lane];
-              float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
-              const float a[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (n + e < N) atomicAdd(yr + e, a[e]);
+            if (ready) break;
+            if (early) break;  // nothing left to overlap: wait below
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              if (lane == 0) atomicOr(err, kErrTimeout);
+              fine = false;
+              break;
             }
-            if (lane == 0) tickets[c0] = 0;
+            __nanosleep(256);
           }
+          if (!fine) break;
+        }
+        // (every lane acquires the fold's stores to `mine`)
+        if (!__all_sync(0xffffffffu, mbar_wait(&pub[i], 0, err))) break;
+        if (early) {
+          // y = (0 + own) + other's: the general sum's order and bits
+          for (int t = 0; t < Tt; ++t) {
+            const float4 a = *reinterpret_cast<const float4*>(mine + t * kRows + 4 * lane);
+            const float4 b = *reinterpret_cast<const float4*>(other + t * kRows + 4 * lane);
+            const float v[4] = {(0.f + a.x) + b.x, (0.f + a.y) + b.y, (0.f + a.z) + b.z,
+                                (0.f + a.w) + b.w};
+            float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (n + e < N) yr[e] = v[e];
+          }
+          if (lane == 0) tickets[c0] = 0;  // the other CTA has taken it: ready for the next launch
           continue;
         }
         // publish this CTA's sums (slot 0: its first row block, 1: its last)
@@ -776,9 +820,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         last = __shfl_sync(0xffffffffu, last, 0);
         __syncwarp();
         if (!last) continue;
-        // four tokens and up to four CTAs' loads in flight at a time, the
+        // eight tokens and up to four CTAs' loads in flight at a time, the
         // CTAs' partials added in CTA order
-        constexpr int kTC = TT < 4 ? TT : 4;
+        constexpr int kTC = TT < 8 ? TT : 8;
         for (int t0 = 0; t0 < Tt; t0 += kTC) {
           float4 acc[kTC];
 #pragma unroll
@@ -974,15 +1018,18 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     //
     // Leftovers (a group's elements more than 21 binades below its absmax,
     // flagged by a negative f, with their sum of |x| in L): for each output,
-    // their contribution is at most s * L.  The running sum |yacc| of this
-    // warp's groups is a lower bound of sum|s w x| over those groups (every
-    // term added is an exact part of y, or the pieces' sum, bounded by its own
-    // sum of |s w x|), so while the dropped bounds add up to at most 2^-11 of
-    // it the leftovers are left out: the error stays below 2^-11 of
-    // sum|s w x|, half the bf16 rungs' bar.  Otherwise they are added exactly
-    // (leftover_dot, on the group's x staged in shared memory).  One budget
-    // lam serves all tokens of a row: a token's own dropped bounds never
-    // exceed lam, which each drop keeps within 2^-11 of that token's |yacc|.
+    // their contribution is at most s * L.  A leftover group is first left
+    // out, its bound added to the row's budget lam and the group noted (up to
+    // kDefer per row block; past that it is added exactly at once).  When the
+    // row block ends, |yacc| of this warp's groups is a lower bound of
+    // sum|s w x| over them (every term added is an exact part of y, or the
+    // pieces' sum, bounded by its own sum of |s w x|); if lam is within 2^-11
+    // of it the noted groups stay out: the error is below 2^-11 of
+    // sum|s w x|, half the bf16 rungs' bar.  Otherwise the noted groups of
+    // that token are added exactly (leftover_dot, on the group's x staged in
+    // shared memory, the weights and scale read again from global memory).
+    // One budget lam serves all tokens of a row: a token's own left-out
+    // bounds never exceed it.
     const int fq = (warp - kDecWarps) & 3;  // == warp % 4
     const int fh = (warp - kDecWarps) >> 2;
     const int r = fq * 32 + lane;
@@ -995,6 +1042,56 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     float* half_part = reinterpret_cast<float*>(smem + C::kPartOff);  // [TT][128]
     float* split_sums = reinterpret_cast<float*>(smem + C::kSplitOff);  // [2][TT][128]
     uint2* lx = reinterpret_cast<uint2*>(smem + C::kLxOff) + (warp - kDecWarps) * 32;
+    uint2* defer = reinterpret_cast<uint2*>(smem + C::kDefOff) + (warp - kDecWarps) * C::kDefer;
+    int ndef = 0;  // noted leftover groups in this row block (warp-uniform)
+    // Add leftover group g (within stage ks) of token t exactly to yacc[t]
+    // where pred; sg: the row's scale of the group.  The whole warp calls it.
+    auto add_exact = [&](int ks, int g, int t, float f_abs, float sg, bool pred, int n) {
+      if (!__any_sync(0xffffffffu, pred)) return;
+      // the group's x into this warp's staging area, the row's weights at the
+      // same time: one memory round trip
+      const int ga = ks * kGS + g;
+      const uint2 xv = *reinterpret_cast<const uint2*>(
+          x + static_cast<size_t>(tok0 + t) * K + ga * 128 + 4 * lane);
+      uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
+      if (pred) {
+        const uint4* wq =
+            reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 4) + ga * 8);
+        wa = ldg_nc_v4(wq);
+        wb = ldg_nc_v4(wq + 1);
+      }
+      lx[lane] = xv;
+      __syncwarp();
+      if (pred) {
+        const float d = leftover_dot(wa, wb, reinterpret_cast<const uint32_t*>(lx),
+                                     leftover_limit(f_abs));
+#pragma unroll
+        for (int u = 0; u < TT; ++u)
+          if (u == t) yacc[u] = fmaf(sg, d, yacc[u]);
+      }
+      __syncwarp();
+    };
+    // Decide the noted leftover groups of the row block ending here.
+    auto settle_leftovers = [&](int rb) {
+      if (ndef == 0) return;  // warp-uniform
+      const int n = rb * kRows + r;
+      uint32_t need = 0;  // bit t: token t's noted groups are added exactly
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+        if (lam > 0x1p-11f * fabsf(yacc[t])) need |= 1u << t;
+      __syncwarp();
+#pragma unroll 1
+      for (int e = 0; e < ndef; ++e) {
+        const uint2 de = defer[e];
+        const int t = de.x & 15, g = (de.x >> 4) & 15, ks = static_cast<int>(de.x >> 8);
+        const bool pred = ((need >> t) & 1u) && n < N && t < Tt;
+        float sg = 0.f;
+        if (pred)
+          sg = __half2float(__ushort_as_half(scales[static_cast<size_t>(n) * G + ks * kGS + g]));
+        add_exact(ks, g, t, __uint_as_float(de.y), sg, pred, n);
+      }
+      ndef = 0;
+    };
     int nflush = 0;
     int nsplit = 0;
     // Row block rb's sums are final in yacc (fh = 0 warps): a row block whole
@@ -1003,6 +1100,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // split-row warp.  false: a bounded wait gave up.
     auto flush = [&](int rb) -> bool {
       const int n = rb * kRows + r;
+      settle_leftovers(rb);
       if (fh == 1) {
         // hand the sums over once the previous hand-over has been taken
         if (nflush > 0 &&
@@ -1143,7 +1241,6 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
           if (kGH * fh + gg < ng) fold_group(gg, dv[gg]);
       }
       if (gflag) {  // rare: groups with leftovers (see above)
-        const int n = cu.rb * kRows + r;
 #pragma unroll 1
         for (int bit = 0; bit < kGH * TT; ++bit) {
           const int gg = bit / TT, t = bit % TT;
@@ -1152,39 +1249,16 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
           const float2 fl = fl_of(g, t);
           if (!(fl.x < 0.f)) continue;
           const float sg = scale_of(gg);
-          const float bound = sg * fl.y;  // |leftover contribution| <= bound
-          float acc = yacc[0];
-#pragma unroll
-          for (int u = 1; u < TT; ++u)
-            if (u == t) acc = yacc[u];
-          const bool drop = lam + bound <= 0x1p-11f * fabsf(acc);
-          const bool exact = !drop && n < N && t < Tt;
-          if (drop) lam += bound;
-          if (__any_sync(0xffffffffu, exact)) {
-            // the group's x into this warp's staging area, the row's weights
-            // at the same time: one memory round trip
-            const int ga = ks * kGS + g;
-            const uint2 xv = *reinterpret_cast<const uint2*>(
-                x + static_cast<size_t>(tok0 + t) * K + ga * 128 + 4 * lane);
-            uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
-            if (exact) {
-              const uint4* wq =
-                  reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 4) + ga * 8);
-              wa = ldg_nc_v4(wq);
-              wb = ldg_nc_v4(wq + 1);
-            }
-            lx[lane] = xv;
-            __syncwarp();
-            if (exact)
-              acc = fmaf(sg,
-                         leftover_dot(wa, wb, reinterpret_cast<const uint32_t*>(lx),
-                                      leftover_limit(-fl.x)),
-                         acc);
-            __syncwarp();
+          if (ndef < C::kDefer) {
+            lam += sg * fl.y;  // |leftover contribution| <= s * L
+            if (lane == 0)
+              defer[ndef] = make_uint2(static_cast<uint32_t>(ks << 8 | g << 4 | t),
+                                       __float_as_uint(-fl.x));
+            ++ndef;
+          } else {
+            const int n = cu.rb * kRows + r;
+            add_exact(ks, g, t, -fl.x, sg, n < N && t < Tt, n);
           }
-#pragma unroll
-          for (int u = 0; u < TT; ++u)
-            if (u == t) yacc[u] = acc;
         }
       }
       __syncwarp();
@@ -1257,7 +1331,9 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   cudaLaunchAttribute attr[1];
   {
     const int tasks = C::kH * kGS * g.KS;
-    cudaLaunchConfig_t pc = pdl_config(attr, dim3((tasks + 7) / 8), dim3(256), 0, stream);
+    int blocks = (tasks + kPrepWarps - 1) / kPrepWarps;
+    if (blocks > num_sms) blocks = num_sms;
+    cudaLaunchConfig_t pc = pdl_config(attr, dim3(blocks), dim3(kPrepWarps * 32), 0, stream);
     cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
     if (e != cudaSuccess) return e;
   }
