@@ -166,6 +166,11 @@ struct TC {
   // Scale loads run kLead units ahead of the weight loads (T = 1: the weight
   // ring does not wait for the MMAs, so the fold must never wait for scales).
   static constexpr int kLead = kInKernelX ? 2 : 0;
+  // Weight stages requested before the previous grid ends.  (T = 1) Only two:
+  // the activation copies, issued after it, queue behind whatever is in
+  // flight, and the first MMAs wait for them.
+  static constexpr int kEarly = kInKernelX ? 2 : kStages;
+  static_assert(2 * kEarly >= kNSub, "decoders fill the free A sub-slots from early stages only");
   // scale (+ factor) ring: held until folded, which trails the weight ring
   // by up to the A lookahead and the D slot
   static constexpr int kSStages = kStages + kLead + (kNSub + 1) / 2 + 1;
@@ -338,11 +343,11 @@ __device__ __forceinline__ int owner_of(long long u, long long U, long long P) {
 // k is the transpose the decoder produces: slot 4i + b holds k = 4b + i.
 constexpr int kPrepWarps = 4;
 
+// Group jg of a stage's block (at st) for token slot t, from the lane's four
+// bf16 values raw.  The whole warp calls it.
 template <int TT>
-__device__ __forceinline__ void prep_task(uint2 raw, uint8_t* __restrict__ out, int t, int gi,
-                                          int lane) {
+__device__ __forceinline__ void prep_task(uint2 raw, uint8_t* st, int t, int jg, int lane) {
   using C = TC<TT>;
-  const int ks = gi / kGS, jg = gi % kGS;
   const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
   float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -351,7 +356,6 @@ __device__ __forceinline__ void prep_task(uint2 raw, uint8_t* __restrict__ out, 
   uint32_t hp[3];
   float lsum;
   const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
-  uint8_t* st = out + static_cast<size_t>(ks) * C::kXBytes;
   if constexpr (TT == 1) {
     // compact block: 16-block j = 8 jg + l/4 at bytes 32 j (piece 0), 32 j + 16
     // (piece 1) and kX1Sbo + 32 j (piece 2); position b = l%4: value i at 4i + b
@@ -415,7 +419,11 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int task = t0 + u * stride;
-      if (task < tasks) prep_task<TT>(raw[u], out, task / groups, task % groups, lane);
+      if (task < tasks) {
+        const int gi = task % groups;
+        prep_task<TT>(raw[u], out + static_cast<size_t>(gi / kGS) * TC<TT>::kXBytes,
+                      task / groups, gi % kGS, lane);
+      }
     }
   }
 }
@@ -464,14 +472,16 @@ __device__ __forceinline__ int new_stage(const Visit& s, int i) {
 // wp: the packed weights (read again only for leftovers); x: bf16 activations
 // (read at T = 1, and for leftovers); xprep: prep blocks (T > 1).
 // tickets / partials: the workspace's ticket counters (one per CTA) and
-// partial row sums of split row blocks.  nslots: T = 1 resident blocks.
+// partial row sums of split row blocks.  nslots: T = 1 resident blocks;
+// build_x: (T = 1) the fold warps build them from x instead of copying the
+// prep kernel's.
 template <int TT>
 __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     smallt_kernel(const __grid_constant__ CUtensorMap tmW, const uint32_t* __restrict__ wp,
                   const uint16_t* __restrict__ scales, const uint16_t* __restrict__ x,
                   const uint8_t* __restrict__ xprep, float* __restrict__ y,
                   int* __restrict__ tickets, float* __restrict__ partials, int K, int N, int tok0,
-                  int Tt, int KS, int nslots, long long U, int* err) {
+                  int Tt, int KS, int nslots, long long U, int build_x, int* err) {
   using C = TC<TT>;
   constexpr int S = C::kStages;
   constexpr int SS = C::kSStages;
@@ -540,7 +550,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) mbar_init(&pub[i], 4);  // the four half-stage-0 fold warps
     if constexpr (C::kInKernelX)
-      for (int q = 0; q < nslots; ++q) mbar_init(&xready[q], 1);  // the producer's copy
+      for (int q = 0; q < nslots; ++q)  // the producer's copy, or one group per fold warp
+        mbar_init(&xready[q], build_x ? kFoldWarps : 1);
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -573,10 +584,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   if (is_split(rb0)) sp[nsp++] = rb0;
   if (rb_last != rb0 && is_split(rb_last)) sp[nsp++] = rb_last;
 
-  // Every role but the producer (which first requests the weights of its
-  // first stages) waits for the previous grid here, so that no bounded wait
-  // below starts its clock while a slow predecessor is still running.
-  if (warp != kProducerWarp) grid_dependency_wait();
+  // The roles wait for the previous grid before any bounded wait whose end
+  // depends on it, so that no clock starts while a slow predecessor is still
+  // running: here, except for the producer (which first requests the weights
+  // of its first stages) and the decoders (which decode those stages into
+  // the free A sub-slots first, and wait before the first sub-slot reuse).
+  if (warp >= kDecWarps && warp != kProducerWarp) grid_dependency_wait();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -677,7 +690,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // Weights and scales are not written by the previous kernels of the
     // stream's chain, so the first stages are requested before its end.
     bool ok = true;
-    const int first = nunits < S ? nunits : S;
+    const int first = nunits < C::kEarly ? nunits : C::kEarly;
     while (ok && su < nunits && su < C::kLead) ok = issue_scales();
     int it = 0;
     Cursor cw;
@@ -689,10 +702,11 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
     const int su_early = su;
     grid_dependency_wait();
-    // (T = 1) the resident activation slots, in visiting order
+    // (T = 1) the resident activation slots, in visiting order, unless the
+    // fold warps build them
     const int nq = nunits < KS ? nunits : KS;
     if constexpr (C::kInKernelX) {
-      if (lane == 0)
+      if (!build_x && lane == 0)
         for (int q = 0; q < nq; ++q) {
           mbar_arrive_expect_tx(&xready[q], kX1Slot);
           bulk_load(xres + q * kX1Slot,
@@ -726,8 +740,9 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     for (int d = (su > SS ? su - SS : 0); d < su; ++d)
       if (!mbar_wait(&sfull[d % SS], (d / SS) & 1, err)) break;
     if constexpr (C::kInKernelX)
-      for (int q = 0; q < nq; ++q)
-        if (!mbar_wait(&xready[q], 0, err)) break;
+      if (!build_x)
+        for (int q = 0; q < nq; ++q)
+          if (!mbar_wait(&xready[q], 0, err)) break;
   } else if (warp == kXWarp0) {
     // ------------------------------------------------------------ split-row sums
     // Warp kXWarp0 combines
@@ -974,6 +989,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 #pragma unroll
       for (int b = 0; b < 2; ++b) {  // groups 2 b, 2 b + 1 of the half-stage
         const int u = 2 * it + b, j = u % NSUB;  // into sub-slot j of this half's ring
+        if (u == NSUB) grid_dependency_wait();  // (the early stages cover u < NSUB)
         if (u >= NSUB &&
             !__all_sync(0xffffffffu,
                         mbar_wait(&afree[h * NSUB + j], ((u / NSUB) & 1) ^ 1, err))) {
@@ -1009,6 +1025,31 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ fold
+    if (C::kInKernelX && build_x) {
+      // (T = 1, few units per CTA) Before any accumulator is ready, fold warp
+      // jg builds group jg of the activation block of every stage the CTA
+      // visits, into the resident slots in visiting order (all loads first).
+      const int jg = warp - kDecWarps;
+      const int nq = nunits < KS ? nunits : KS;
+      uint2 raw[kSmallTX1MaxSlots];
+#pragma unroll
+      for (int q = 0; q < kSmallTX1MaxSlots; ++q) {
+        raw[q] = make_uint2(0u, 0u);
+        const int gi = q < nq ? new_stage(vs, q) * kGS + jg : G;
+        if (gi < G)
+          raw[q] = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0) * K + gi * 128 +
+                                                   4 * lane);
+      }
+#pragma unroll
+      for (int q = 0; q < kSmallTX1MaxSlots; ++q) {
+        if (q < nq) {
+          prep_task<1>(raw[q], xres + q * kX1Slot, 0, jg, lane);
+          fence_proxy_async_smem();  // the MMA reads the block through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xready[q]);
+        }
+      }
+    }
     // Fold warp f owns TMEM lane quarter fq = f % 4 (rows 32 fq .. 32 fq + 31)
     // and half-stage fh = f / 4 (groups 4 fh .. 4 fh + 3) of every stage:
     // y[t][row] += s[row][g] * f[g][t] * (sum of the pieces' accumulators of
@@ -1328,8 +1369,14 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   float* partials = reinterpret_cast<float*>(work);
   uint8_t* xprep = work + smallt_partials_bytes(TT);
 
+  // (T = 1) With at most two units per CTA the call is short and the prep
+  // kernel's extra dependency step costs more than building the few stages
+  // in every CTA from x; with more, x is better read once by the prep kernel
+  // (an L2 hit for the main kernel, whose own reads of x would queue behind
+  // its weight stream).
+  const int build_x = C::kInKernelX && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
   cudaLaunchAttribute attr[1];
-  {
+  if (!build_x) {
     const int tasks = C::kH * kGS * g.KS;
     int blocks = (tasks + kPrepWarps - 1) / kPrepWarps;
     if (blocks > num_sms) blocks = num_sms;
@@ -1341,7 +1388,7 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
                                       C::smem_bytes(nslots), stream);
   return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, Wp, scales, x,
                             static_cast<const uint8_t*>(xprep), y, sync, partials, K, N, tok0, Tt,
-                            g.KS, nslots, g.U, err);
+                            g.KS, nslots, g.U, build_x, err);
 }
 
 }  // namespace
