@@ -835,30 +835,37 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
         last = __shfl_sync(0xffffffffu, last, 0);
         __syncwarp();
         if (!last) continue;
-        // eight tokens and up to four CTAs' loads in flight at a time, the
-        // CTAs' partials added in CTA order
+        // eight float4 loads in flight at a time (up to eight tokens of
+        // 8 / tokens CTAs), the CTAs' partials added in CTA order
         constexpr int kTC = TT < 8 ? TT : 8;
+        constexpr int kCB = 8 / kTC;
         for (int t0 = 0; t0 < Tt; t0 += kTC) {
           float4 acc[kTC];
 #pragma unroll
           for (int tj = 0; tj < kTC; ++tj) acc[tj] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int cb = c0; cb <= c1; cb += 4) {
+          for (int cb = c0; cb <= c1; cb += kCB) {
+            float4 v[kCB][kTC];
 #pragma unroll
-            for (int ci = 0; ci < 4; ++ci) {
+            for (int ci = 0; ci < kCB; ++ci) {
               const int c = cb + ci;
-              if (c > c1) break;
               const float* pc =
                   partials + static_cast<size_t>(c * 2 + (first_rb(c) == rb ? 0 : 1)) * TT * kRows +
                   4 * lane;
 #pragma unroll
+              for (int tj = 0; tj < kTC; ++tj)
+                v[ci][tj] = c <= c1 && t0 + tj < Tt
+                                ? __ldcg(reinterpret_cast<const float4*>(pc + (t0 + tj) * kRows))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int ci = 0; ci < kCB; ++ci) {
+              if (cb + ci > c1) break;
+#pragma unroll
               for (int tj = 0; tj < kTC; ++tj) {
-                if (t0 + tj < Tt) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(pc + (t0 + tj) * kRows));
-                  acc[tj].x += v.x;
-                  acc[tj].y += v.y;
-                  acc[tj].z += v.z;
-                  acc[tj].w += v.w;
-                }
+                acc[tj].x += v[ci][tj].x;
+                acc[tj].y += v[ci][tj].y;
+                acc[tj].z += v[ci][tj].z;
+                acc[tj].w += v[ci][tj].w;
               }
             }
           }
