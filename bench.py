@@ -63,6 +63,8 @@ def parse_args():
     ap.add_argument("--profile", choices=["gu", "dn", "s8gu", "s8dn"], default=None,
                     help="only call tern_linear on one projection at T=1 (for profilers)")
     ap.add_argument("--profile-calls", type=int, default=3)
+    ap.add_argument("--profile-t", type=int, default=None,
+                    help="token count for --profile (default 1 for gu/dn, 2048 for s8gu/s8dn)")
     ap.add_argument("--no-stack", action="store_true",
                     help="skip the 64-layer whole-stack passes")
     ap.add_argument("--formats", action="store_true",
@@ -260,6 +262,84 @@ def run_stack(tl, torch, gen, dev, peaks, stream):
     return res
 
 
+L2_BYTES = 129 * 2 ** 20
+COMPACT_T = {"gate_up": (1, 4, 8, 16, 17, 508, 2048), "down": (1, 4, 8, 16, 17, 508, 2048)}
+
+
+def rotated_copies(K, N):
+    """Distinct weight copies whose packed bytes exceed 4x L2."""
+    return -(-4 * L2_BYTES // weight_bytes(K, N))
+
+
+def time_rotated(tl, torch, layers, K, N, T, gen, dev, reps=10):
+    """Per-call time of tern_linear at (T, K, N), cycling over the weight
+    copies in `layers` (> 4x L2 of packed weights, so every call streams its
+    weights from HBM), all calls captured in one CUDA graph replayed between
+    CUDA events on the launching stream.  Returns (us per call, rung,
+    kernels launched per call)."""
+    copies = len(layers)
+    x = make_x(torch, T, K, gen, dev)
+    ys = [torch.empty(T, N, device=dev) for _ in range(copies)]
+    ws = torch.zeros(tl.tern_linear_workspace_bytes(T, K, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    launches = []
+
+    def calls(count=False):
+        for (w, sc), y in zip(layers, ys):
+            tl.tern_linear(w, sc, x, y, ws)
+            if count:
+                launches.append(tl.tern_last_launches())
+
+    with torch.cuda.stream(stream):
+        calls(count=True)  # library set-up outside capture
+    torch.cuda.synchronize()
+    rung = tl.tern_last_rung()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            calls()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+    del g, x, ys, ws
+    return us, rung, max(launches)
+
+
+def compact_sweep(tl, torch, gen, dev, peaks):
+    """The configs' token counts on the two 27B-like MLP projections: T = 1
+    (decode), 4, 8, 16 (speculative verify) on the bandwidth rungs and 17,
+    508, 2048 on s8, each over rotated weight copies."""
+    rows = []
+    for name, (K, N) in (("gate_up", GU), ("down", DN)):
+        layers = [make_layer(tl, torch, K, N, gen, dev) for _ in range(rotated_copies(K, N))]
+        for T in COMPACT_T[name]:
+            us, rung, nl = time_rotated(tl, torch, layers, K, N, T, gen, dev,
+                                        reps=10 if T < 2048 else 4)
+            gbs = algorithmic_bytes(T, K, N) / (us * 1e-6) / 1e9
+            row = {"proj": name, "K": K, "N": N, "T": T, "rung": rung, "copies": len(layers),
+                   "launches_per_call": nl, "us_per_call": round(us, 3)}
+            if rung == "s8":
+                tops = 2.0 * T * K * N / (us * 1e-6) / 1e12
+                row.update({"int8_TOPS": round(tops, 1),
+                            "frac_of_bf16_peak": round(tops / peaks["bf16_tflops"], 4)})
+            else:
+                row.update({"GB/s": round(gbs, 1),
+                            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)})
+            rows.append(row)
+        del layers
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args, rank, world, local):
     import torch
     import ternary_weight_linear_gb300 as tl
@@ -290,13 +370,19 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())  # inputs and the zeroed workspace
 
-    def step_calls():
+    step_launches = []
+
+    def step_calls(count=False):
         for i, ((gw, gs), (dw, ds)) in enumerate(layers):
             tl.tern_linear(gw, gs, x_gu, y_gu[i], ws)
+            if count:
+                step_launches.append(tl.tern_last_launches())
             tl.tern_linear(dw, ds, x_dn, y_dn[i], ws)
+            if count:
+                step_launches.append(tl.tern_last_launches())
 
     with torch.cuda.stream(stream):
-        step_calls()  # library init outside capture
+        step_calls(count=True)  # library init outside capture
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -330,63 +416,36 @@ def run_ours(args, rank, world, local):
     ms_per_step = ms / args.steps
     value = whole_job_gbs(world, step_bytes, ms_per_step)
 
-    # ---- dominant kernel: the gate+up T=1 call, timed back to back
-    reps = 200
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g2, stream=stream):
-            for i in range(L):
-                tl.tern_linear(layers[i][0][0], layers[i][0][1], x_gu, y_gu[i], ws)
-    g2.replay()
-    torch.cuda.synchronize()
-    e2, e3 = torch.cuda.Event(True), torch.cuda.Event(True)
-    with torch.cuda.stream(stream):
-        e2.record(stream)
-        for _ in range(reps):
-            g2.replay()
-        e3.record(stream)
-    torch.cuda.synchronize()
-    gu_us = e2.elapsed_time(e3) * 1e3 / (reps * L)
-    gu_alg = algorithmic_bytes(T, *GU)
-    gu_gbs = gu_alg / (gu_us * 1e-6) / 1e9
-    traffic = profile_traffic(os.path.join(ROOT, "ternary_weight_linear_gb300", "csrc", "tern_smallt.cu"),
-                              "smallt_kernel_gu_t1.md")
-    roofline = {"bound": "hbm", "kernel": "tern_linear T=1 gate+up 5120x34816 (smallt_kernel<1>)",
-                "achieved": round(gu_gbs, 1), "peak": peaks["hbm_gbs"], "peak_kind": peak_kind,
-                "unit": "GB/s", "frac": round(gu_gbs / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "algorithmic_bytes_per_launch": gu_alg,
-                "avg_launch_us": round(gu_us, 3)}
+    # ---- per-call legs over rotated weight copies (> 4x L2): the configs'
+    # token counts on both MLP projections; the T = 1 rows give the roofline
+    # of the dominant kernel (gate+up) and of the down projection
+    sweep = compact_sweep(tl, torch, gen, dev, peaks)
 
-    # ---- s8 prefill rung at T = 2048 (gate+up and down)
-    T8 = 2048
-    x8_gu = make_x(torch, T8, GU[0], gen, dev)
-    x8_dn = make_x(torch, T8, DN[0], gen, dev)
-    y8_gu = torch.empty(T8, GU[1], device=dev)
-    y8_dn = torch.empty(T8, DN[1], device=dev)
-    ws8 = torch.zeros(max(tl.tern_linear_workspace_bytes(T8, *GU), tl.tern_linear_workspace_bytes(T8, *DN)),
-                      dtype=torch.uint8, device=dev)
-    (gw, gs), (dw, ds) = layers[0]
-    for _ in range(3):
-        tl.tern_linear(gw, gs, x8_gu, y8_gu, ws8)
-        tl.tern_linear(dw, ds, x8_dn, y8_dn, ws8)
-    torch.cuda.synchronize()
-    reps8 = 10
-    e4, e5 = torch.cuda.Event(True), torch.cuda.Event(True)
-    e4.record()
-    for _ in range(reps8):
-        tl.tern_linear(gw, gs, x8_gu, y8_gu, ws8)
-        tl.tern_linear(dw, ds, x8_dn, y8_dn, ws8)
-    e5.record()
-    torch.cuda.synchronize()
-    s8_ms = e4.elapsed_time(e5) / reps8
-    s8_ops = 2.0 * T8 * (GU[0] * GU[1] + DN[0] * DN[1])
-    s8_tops = s8_ops / (s8_ms * 1e-3) / 1e12
+    def roofline_of(proj, summary):
+        row = next(r for r in sweep if r["proj"] == proj and r["T"] == 1)
+        K, N = row["K"], row["N"]
+        alg = algorithmic_bytes(1, K, N)
+        gbs = alg / (row["us_per_call"] * 1e-6) / 1e9
+        traffic = profile_traffic(
+            os.path.join(ROOT, "ternary_weight_linear_gb300", "csrc", "tern_smallt.cu"), summary)
+        return {"bound": "hbm", "kernel": f"tern_linear T=1 {proj} {K}x{N} (smallt_kernel<1>)",
+                "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+                "avg_launch_us": row["us_per_call"], "launches_per_call": row["launches_per_call"],
+                "rotation": f"{row['copies']} weight copies (> 4x L2)"}
+
+    roofline = roofline_of("gate_up", "smallt_kernel_gu_t1.md")
+    roofline_dn = roofline_of("down", "smallt_kernel_dn_t1.md")
+    s8_rows = [r for r in sweep if r["T"] == 2048]
+    s8_us = sum(r["us_per_call"] for r in s8_rows)
+    s8_tops = sum(2.0 * r["T"] * r["K"] * r["N"] for r in s8_rows) / (s8_us * 1e-6) / 1e12
     # The s8 rung contracts every int8 product as two e4m3 products (the
     # activation split into two exact pieces), so its ceiling in int8 ops is
     # half the e4m3 tensor rate, i.e. the bf16 rate: e4m3 runs at twice bf16
     # (nominal ratio), and the measured bf16 peak is the denominator.
     s8 = {"metric": "int8 TOPS at T=2048 (s8 rung, gate+up + down)", "value": round(s8_tops, 1),
-          "unit": "TOPS", "ms_per_pass": round(s8_ms, 3),
+          "unit": "TOPS", "us_per_pass": round(s8_us, 1),
           "roofline": {"bound": "tensor", "achieved": round(s8_tops, 1),
                        "peak": peaks.get("bf16_tflops", 1900.0), "peak_kind": peak_kind + " bf16",
                        "unit": "TOPS", "frac": round(s8_tops / peaks.get("bf16_tflops", 1900.0), 4),
@@ -423,12 +482,14 @@ def run_ours(args, rank, world, local):
     if tl.tern_device_status() != 0:
         raise RuntimeError("device error word set")
 
-    launches = args.steps * L * 2  # per T=1 call: one smallt_kernel<1> launch
+    launches = args.steps * sum(step_launches)  # counted by the library, per call
     out = {
         "metric": "ternary linear weight GB/s at T=1 (frac of HBM peak); int8 TOPS at T=2048",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 tensor-core products, fp32 accumulation",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x as three exact e5m2 pieces times e4m3 ternary codes (tcgen05 kind::f8f6f4), "
+                 "fp32 accumulation",
         "data": "synthetic",
         "config": {"workload": f"decode GEMV T=1 over {L} layers x (gate+up 5120x34816, down 17408x5120), "
                                "27B-like MLP shapes",
@@ -437,6 +498,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
         "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": roofline,
+        "roofline_down": roofline_dn,
+        "sweep": sweep,
         "s8_t2048": s8,
         "stack_c4": stack,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -526,8 +589,8 @@ def run_reference(args, rank, world):
 
 def run_profile(args):
     """A few calls on one synthetic projection, nothing else: the command a
-    profiler wraps to capture one kernel.  gu / dn: T = 1 (decode);
-    s8gu / s8dn: T = 2048 (the s8 prefill rung)."""
+    profiler wraps to capture one kernel.  gu / dn: T = 1 (decode) unless
+    --profile-t says otherwise; s8gu / s8dn: T = 2048 by default."""
     import torch
     import ternary_weight_linear_gb300 as tl
 
@@ -537,7 +600,7 @@ def run_profile(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234)
     K, N = GU if args.profile.endswith("gu") else DN
-    T = 2048 if args.profile.startswith("s8") else 1
+    T = args.profile_t or (2048 if args.profile.startswith("s8") else 1)
     Wp, s = make_layer(tl, torch, K, N, gen, dev)
     x = make_x(torch, T, K, gen, dev)
     y = torch.empty(T, N, device=dev)
@@ -546,7 +609,8 @@ def run_profile(args):
         tl.tern_linear(Wp, s, x, y, ws)
     torch.cuda.synchronize()
     status = tl.tern_device_status()
-    print(json.dumps({"profile": args.profile, "calls": args.profile_calls, "status": status}))
+    print(json.dumps({"profile": args.profile, "T": T, "rung": tl.tern_last_rung(),
+                      "calls": args.profile_calls, "status": status}))
     if status != 0:
         sys.exit(1)
 
@@ -616,7 +680,6 @@ def run_formats(args):
 
 
 SWEEP_T = (1, 2, 3, 4, 8, 9, 12, 16, 17, 508, 2048)
-L2_BYTES = 129 * 2 ** 20
 
 
 def run_sweep(args):

@@ -260,6 +260,13 @@ const char* tern_rung_name(int rung);
 int tern_last_rung_id(void);
 const char* tern_last_rung(void);
 
+/* Number of kernels this thread's last successful tern_linear (or
+ * tern_linear_small_t_noalloc) launched: per token tile of the bandwidth
+ * rungs one main kernel, plus the activation-prep kernel where the tile
+ * uses one; 2 on the s8 rung (activation pieces, then the GEMM).  0 before
+ * any call.  Host-only; for benchmarks and tests. */
+int tern_last_launches(void);
+
 /* Static text for a tern_status. */
 const char* tern_status_string(int status);
 

@@ -21,6 +21,7 @@ from .build import LIB_PATH, build  # noqa: F401  (re-exported for convenience)
 __all__ = [
     "tern_pack", "tern_quant_act_s8", "tern_linear", "tern_linear_workspace_bytes",
     "tern_select_rung", "tern_rung_name", "tern_last_rung", "tern_last_rung_id",
+    "tern_last_launches",
     "tern_reload_env", "tern_device_status", "tern_status_string", "TernError", "load",
     "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16",
     "tern_selftest_wait_timeout", "RUNGS",
@@ -33,7 +34,7 @@ RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8"}
 EXPORTED_SYMBOLS = (
     "tern_pack", "tern_quant_act_s8", "tern_linear_workspace_bytes", "tern_linear",
     "tern_select_rung", "tern_rung_name", "tern_last_rung_id", "tern_last_rung",
-    "tern_status_string", "tern_reload_env", "tern_device_status",
+    "tern_last_launches", "tern_status_string", "tern_reload_env", "tern_device_status",
     "tern_linear_small_t_noalloc", "tern_repack_t5", "tern_rotate_bf16",
     "tern_selftest_wait_timeout",
 )
@@ -86,6 +87,8 @@ def load() -> ctypes.CDLL:
         lib.tern_last_rung_id.restype = I
         lib.tern_last_rung.argtypes = []
         lib.tern_last_rung.restype = ctypes.c_char_p
+        lib.tern_last_launches.argtypes = []
+        lib.tern_last_launches.restype = I
         lib.tern_status_string.argtypes = [I]
         lib.tern_status_string.restype = ctypes.c_char_p
         lib.tern_reload_env.argtypes = []
@@ -264,6 +267,11 @@ def tern_last_rung() -> str:
 
 def tern_last_rung_id() -> int:
     return int(load().tern_last_rung_id())
+
+
+def tern_last_launches() -> int:
+    """Kernels this thread's last successful tern_linear launched."""
+    return int(load().tern_last_launches())
 
 
 def tern_reload_env() -> None:

@@ -109,6 +109,7 @@ void probe(const Config& c, int rung, int T, int K, int N) {
 }
 
 thread_local int t_last_rung = -1;
+thread_local int t_last_launches = 0;
 
 // ------------------------------------------------------------------ device state
 constexpr int kMaxDevices = 64;
@@ -205,7 +206,7 @@ void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* t
 
 // ws: workspace whose first kSyncBytes are the zeroed sync area.
 int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
-                float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st) {
+                float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st, int* launches) {
   CUtensorMap tmW;
   int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                        static_cast<uint64_t>(K) / 4, 128, smallt_rows(1),
@@ -215,7 +216,7 @@ int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, co
     int tt = 0, take = 0;
     small_t_tile(rung, T - tok0, K, N, d->sms, &tt, &take);
     if (launch_smallt(tt, &tmW, Wp, s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
-                      tok0, take, d->sms, d->err, st) != cudaSuccess)
+                      tok0, take, d->sms, d->err, st, launches) != cudaSuccess)
       return TERN_ECUDA;
     tok0 += take;
   }
@@ -294,6 +295,7 @@ int tern_select_rung(int T) {
 }
 
 int tern_last_rung_id(void) { return t_last_rung; }
+int tern_last_launches(void) { return t_last_launches; }
 const char* tern_last_rung(void) { return t_last_rung < 0 ? "none" : tern_rung_name(t_last_rung); }
 
 size_t tern_linear_workspace_bytes(int T, int K, int N) {
@@ -375,12 +377,13 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
   if (!workspace || workspace_bytes < need) return TERN_ENOSPACE;
   if (!aligned16(workspace)) return TERN_EALIGN;
 
+  int launches = 0;
   switch (rung) {
     case TERN_RUNG_GEMV:
     case TERN_RUNG_SMALL_T:
     case TERN_RUNG_SMALL_T_TILED:
       rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, static_cast<uint8_t*>(workspace),
-                       st);
+                       st, &launches);
       break;
     case TERN_RUNG_S8: {
       // after the sync area, which the s8 rung leaves untouched
@@ -390,6 +393,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       uint8_t* p2 = scratch + piece;
       float* xs = reinterpret_cast<float*>(scratch + 2 * piece);
       if (launch_quant_pieces(x, p1, p2, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
+      ++launches;
       CUtensorMap tmW, tmP1, tmP2;
       rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                        static_cast<uint64_t>(K) / 4, 32, kS8TileN, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -411,6 +415,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
                      d->err, st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
+      ++launches;
       break;
     }
     default:
@@ -418,6 +423,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
   }
   if (rc == TERN_OK) {
     t_last_rung = rung;
+    t_last_launches = launches;
     probe(c, rung, T, K, N);
   }
   return rc;
@@ -439,10 +445,12 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   uint8_t* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc != TERN_OK) return rc;
+  int launches = 0;
   rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch,
-                   static_cast<cudaStream_t>(stream));
+                   static_cast<cudaStream_t>(stream), &launches);
   if (rc == TERN_OK) {
     t_last_rung = rung;
+    t_last_launches = launches;
     probe(config(), rung, T, K, N);
   }
   return rc;

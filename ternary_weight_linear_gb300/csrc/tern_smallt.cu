@@ -1368,7 +1368,8 @@ int t1_slots(const SmallTGrid& g) {
 template <int TT>
 cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t* scales,
                       const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
-                      int tok0, int Tt, int num_sms, int* err, cudaStream_t stream) {
+                      int tok0, int Tt, int num_sms, int* err, cudaStream_t stream,
+                      int* launches) {
   using C = TC<TT>;
   const SmallTGrid g = smallt_grid(K, N, num_sms);
   const int nslots = C::kInKernelX ? t1_slots(g) : 0;
@@ -1390,12 +1391,16 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
     cudaLaunchConfig_t pc = pdl_config(attr, dim3(blocks), dim3(kPrepWarps * 32), 0, stream);
     cudaError_t e = cudaLaunchKernelEx(&pc, xprep_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
     if (e != cudaSuccess) return e;
+    ++*launches;
   }
   cudaLaunchConfig_t cfg = pdl_config(attr, dim3(static_cast<unsigned>(g.P)), dim3(C::kThreads),
                                       C::smem_bytes(nslots), stream);
-  return cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, Wp, scales, x,
-                            static_cast<const uint8_t*>(xprep), y, sync, partials, K, N, tok0, Tt,
-                            g.KS, nslots, g.U, build_x, err);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, Wp, scales, x,
+                         static_cast<const uint8_t*>(xprep), y, sync, partials, K, N, tok0, Tt,
+                         g.KS, nslots, g.U, build_x, err);
+  if (e == cudaSuccess) ++*launches;
+  return e;
 }
 
 }  // namespace
@@ -1434,17 +1439,20 @@ cudaError_t smallt_set_attributes() {
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
                           const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
                           float* y, int K, int N, int tok0, int Tt, int num_sms, int* err,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int* launches) {
   switch (tt) {
     case 1:
-      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
+                          launches);
     case 4:
-      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
+                          launches);
     case 8:
-      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream);
+      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
+                          launches);
     default:
       return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err,
-                           stream);
+                           stream, launches);
   }
 }
 

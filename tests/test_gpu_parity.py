@@ -570,3 +570,27 @@ torch.cuda.synchronize()
     lines = [l for l in r.stderr.splitlines() if l.startswith("tern: rung=")]
     # budget 3: the fourth call is not reported
     assert [l.split()[1] for l in lines] == ["rung=gemv", "rung=small_t", "rung=small_t_tiled"]
+
+
+# ---------------------------------------------------------------- launch counts
+
+@pytest.mark.parametrize("K,N,T,rung,expect", [
+    (5120, 34816, 1, "gemv", 2),     # nine units per CTA: prep kernel + main kernel
+    (5120, 6144, 1, "gemv", 1),      # two units per CTA: the main kernel builds x itself
+    (5120, 34816, 4, "small_t", 2),
+    (5120, 6144, 20, "small_t_tiled", 4),   # two token tiles (16 + 4)
+    (5120, 6144, 37, "s8", 2),
+])
+def test_launch_count_probe(tl, K, N, T, rung, expect):
+    import torch
+    W = torch.zeros((N, K), dtype=torch.int8, device="cuda")
+    Wp = tl.tern_pack(W)
+    s = torch.ones((N, K // 128), dtype=torch.float16, device="cuda")
+    x = torch.ones((T, K), dtype=torch.bfloat16, device="cuda")
+    with forced_rung(tl, rung):
+        y = tl.tern_linear(Wp, s, x)
+        assert tl.tern_last_rung() == rung
+        assert tl.tern_last_launches() == expect
+    torch.cuda.synchronize()
+    assert tl.tern_device_status() == 0
+    assert float(y.abs().max().item()) == 0.0
