@@ -152,14 +152,19 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  *   q, xs = tern_quant_act_s8(x)
  *   acc[t][n][g] = sum_{k in g} q[t][k] * w[n][k]   (exact integers)
  *   y[t][n]      = xs[t] * sum_g s[n][g] * acc[t][n][g]   (fp32).
- * Precision of the bf16 rungs, for every finite input: every product
- * s * w * x is formed exactly (each bf16 x is cut into three fp8 e5m2 pieces
- * at a power-of-two scale per token and 128-group, exact for the elements
- * within 21 binades of the group's largest; the rest are multiplied exactly
- * on the CUDA cores), and only the fp32 sums round, far inside
- * |y - y_exact| <= 1e-3 * sum|s w x| + 1e-6.  Groups whose values span more
- * than 21 binades cost extra time (their leftovers are read twice).
- * Results are bit-for-bit reproducible from call to call on every rung.
+ * Precision of the bf16 rungs, for every finite input: each bf16 x is cut
+ * into three fp8 e5m2 pieces at a power-of-two scale per token and
+ * 128-group, exactly for every element within 21 binades of the group's
+ * largest, so those products w * x are formed exactly on the tensor cores.
+ * The few elements further down (leftovers) are handled per row block: if
+ * the bound s * sum|x| of every leftover group of a row block adds up to at
+ * most 2^-11 of the row block's partial sum, they are left out, otherwise
+ * they are multiplied exactly on the CUDA cores.  Beside the fp32 sums'
+ * rounding the error is therefore at most 2^-11 * sum|s w x|, inside
+ * |y - y_exact| <= 1e-3 * sum|s w x| + 1e-6.  Row blocks that need their
+ * leftovers added read them twice (extra time, same result).
+ * Results are bit-for-bit reproducible from call to call on every rung: rows
+ * whose sums several CTAs share are added in a fixed CTA order.
  *   Wpacked  device uint32 [N][K/16] (layout above), read-only
  *   scales   device fp16 [N][K/128], read-only
  *   x        device bf16 [T][K], read-only

@@ -19,17 +19,21 @@
 //    (its scaled value at least 2^-7, its last bit at least 2^-14)
 //    h1 + h2 + h3 == v exactly, and every nonzero piece is a normal e5m2.
 //    Smaller nonzero elements ("leftovers", |x| < 2^-21 of m's binade) get no
-//    pieces; the group's factor is stored negated, and the fold adds their
-//    products exactly on the CUDA cores (leftover_dot), reading the group's
-//    packed weights and x again.  With bf16 activations this happens only in
-//    groups whose values span more than 21 binades.  The pieces are the
-//    columns of the MMA's B operand in the tcgen05 K-major shared-memory
-//    layout, one block per 1024-wide k stage, with the per-(group, token)
-//    factors f = 2^(3-p).  At T = 1 four warps of the main kernel build the
-//    blocks of every stage the CTA visits once, into shared memory where they
-//    stay (a compact layout: see kX1Lbo); for wider token tiles a prep kernel
-//    builds all blocks once per call and the main kernel copies each stage's
-//    block in with its weights.
+//    pieces; the group's factor is stored negated with their sum of |x|.  The
+//    fold notes such groups and, at the end of the row block, either leaves
+//    them out (their bound within 2^-11 of the row block's partial sum) or
+//    adds their products exactly on the CUDA cores (leftover_dot), reading
+//    the group's packed weights and x again.  With bf16 activations
+//    leftovers occur only in groups whose values span more than 21 binades.
+//    The pieces are the columns of the MMA's B operand in the tcgen05
+//    K-major shared-memory layout, one block per 1024-wide k stage, with the
+//    per-(group, token) factors f = 2^(3-p).  A prep kernel builds all
+//    blocks once per call; at T = 1 the main kernel copies the blocks of
+//    every stage it visits once into shared memory, where they stay (a
+//    compact layout: see kX1Lbo), and for wider token tiles it copies each
+//    stage's block in with its weights.  At T = 1 with at most two units per
+//    CTA the fold warps build the resident blocks from x instead, and the
+//    prep kernel is not launched.
 // 2. Weights as fp8, decoded into tensor memory.  The packed code puts each
 //    weight's nonzero bit and sign bit at the 2^-3 exponent bit and the sign
 //    bit of an e4m3 byte once shifted, so one shift and one AND turn a packed
@@ -39,8 +43,9 @@
 // 3. tcgen05.mma kind::f8f6f4 (A e4m3 in TMEM, B e5m2 in shared memory, fp32
 //    accumulator in TMEM): every product w/8 * piece is exact.  Fold threads
 //    read the accumulators back with tcgen05.ld and fold the pieces' sums
-//    into their row's running sums with s[n][g] * f[g][token].  The only
-//    roundings are the fp32 sums.
+//    into their row's running sums with s[n][g] * f[g][token].  Beside the
+//    leftovers left out within their budget, the only roundings are the
+//    fp32 sums.
 //
 // Pipeline (one CTA per SM, persistent; TMEM 512 columns):
 //   warp 16    producer: two 2D TMA boxes of packed weights (128 rows x 128 B
@@ -50,38 +55,43 @@
 //              weights and scales of the first stages are requested before
 //              the previous kernel on the stream has finished (they are not
 //              written by it); activations only after.
-//   warps 19-22 (T = 1) build the resident activation blocks and factors;
-//   warps 0-7  decode (four groups of 32 rows per warp) into A slots;
+//   warps 0-7  decode (four groups of 32 rows per warp) into A sub-slots;
+//              they start on the early stages before the previous grid ends;
 //   warps 17-18 issue the MMAs of half-stage 0 / 1 of every stage once its
-//              A slot is full and its D slot has been drained (warp 17 also
-//              allocates TMEM);
+//              A sub-slot is full and its D slot has been drained (warp 17
+//              also allocates TMEM);
 //   warps 8-15 fold D slots into per-row running sums (two threads per row,
-//              one per half-stage) and write y at the end of each row block.
+//              one per half-stage) and write y at the end of each row block
+//              (or hand split row blocks' sums to warp 19);
+//   warp 19    adds up the row blocks this CTA shares with others.
 //
 // Work split: the (row block, 1024-wide k stage) units are cut into equal
 // contiguous ranges, one per CTA, so every SM streams the same bytes.  A row
 // block whole inside one CTA is written to y directly.  A row block split
 // between CTAs is reduced without waiting on other CTAs: each CTA writes its
 // partial row sums to the workspace and takes a ticket; the CTA that arrives
-// last adds every partial in CTA order and writes y.  The result does not
-// depend on which CTA finishes last, so every output is reproducible bit for
-// bit, and no CTA ever waits for another to be scheduled.
+// last adds every partial in CTA order and writes y.  (A CTA that finishes a
+// row block shared with one other CTA, which started it earlier, polls the
+// ticket and copies the other partial in before its own sums are ready.)
+// The result does not depend on which CTA finishes last, so every output is
+// reproducible bit for bit, and no CTA ever waits for another to be
+// scheduled.
 //
 // A stage is 1024 k: two 128-byte weight boxes per row, eight groups; a
-// half-stage is one box, four groups.  TMEM is used in half-stage slots: the
-// decode warps of groups 0-3 and of groups 4-7 each fill their own A slot,
-// the MMAs of a half-stage write their own D slot, so decode, MMA and fold
-// can run half-stages apart; each A slot is filled and released in two
-// halves (groups 0-1, 2-3), so a half-stage's MMAs overlap the decoding of
-// its next use.
+// half-stage is one box, four groups.  TMEM is used per half-stage: the
+// decode warps of groups 0-3 and of groups 4-7 each fill their own ring of A
+// sub-slots (two groups each), the MMAs of a half-stage write their own D
+// slot, so decode, MMA and fold can run sub-slots apart.
 //
 // Calls chain by programmatic dependent launch: every kernel lets the next one
 // launch as soon as all of its CTAs run; the next kernel's CTAs set up, load
 // their first weight stages and wait for the previous grid before they read
-// anything it may have written (x) or write y / the workspace.  Every ring of
-// slots has an even length, so a slot only ever holds half-stages of one
-// parity (one decode half, one MMA issuer, one fold half): a waiter's barrier
-// is then never two phases behind it.
+// anything it may have written (x) or write y / the workspace.  The prep
+// kernel's CTAs are small enough (4 warps, 32 registers, no shared memory)
+// to sit beside a main-kernel CTA, so a prep launch never holds an SM the
+// next main kernel needs.  Each A sub-slot ring and D ring belongs to one
+// decode half, one MMA issuer and one fold half, so a waiter's barrier is
+// never two phases behind it.
 //
 // The pages' kernel for this band (the "small_t" rung of the
 // "ninfer-perf-tuning" skill page, sections 2 and 6) decodes through a LUT
@@ -179,8 +189,7 @@ struct TC {
   static constexpr int kWOff = 0;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kXOff = kWOff + kStages * kWBytes;  // activation ring (T > 1)
   static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
-  static constexpr int kFOff = kSOff + kSStages * kSBytes;  // (T = 1) (f, L)[slot][kGS]
-  static constexpr int kBarOff = kFOff;
+  static constexpr int kBarOff = kSOff + kSStages * kSBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kSStages + 4 * kNSub + 2 * kNDH + 8 + 2 +
                                   (kInKernelX ? kSmallTX1MaxSlots : 0);
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
