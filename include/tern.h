@@ -193,6 +193,17 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  * kernel starts.
  * x, y and the workspace are touched only after the previous kernel has
  * completed.
+ * With TERN_ROTATE=1 in the environment the layer runs on the blockwise
+ * Hadamard rotation of x (the operation of tern_rotate_bf16: each 1024-wide
+ * block of each token rotated and rounded once to bf16) instead of x itself,
+ * for weights stored in the rotated basis.  Every rung rotates inside its own
+ * activation staging (x is never written and no extra call is made); K must
+ * then be a multiple of 1024 and at most 65536, else TERN_EINVAL.  The
+ * rotation's fp32 sums may round an element the other way where its exact
+ * value lies within tern_rotate_bf16's stated bound of a bf16 rounding
+ * boundary; otherwise the result is that of tern_linear on tern_rotate_bf16's
+ * output.  Source: the rotation the "NInfer sm_89 fork" write-up (section 9
+ * item 2) fuses into the activation quantisation.
  * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
  * Every rung is correct for every T. */
 int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
@@ -276,7 +287,7 @@ int tern_last_launches(void);
 const char* tern_status_string(int status);
 
 /* Re-read the environment (TERN_RUNG, TERN_SMALL_T_MAX, TERN_TILED_MAX,
- * TERN_S8_MIN_T, TERN_DEBUG, TERN_DEBUG_MIN_T, TERN_DEBUG_BUDGET).  The
+ * TERN_S8_MIN_T, TERN_ROTATE, TERN_DEBUG, TERN_DEBUG_MIN_T, TERN_DEBUG_BUDGET).  The
  * environment is otherwise read once per process, on first use. */
 void tern_reload_env(void);
 

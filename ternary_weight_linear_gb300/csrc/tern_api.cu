@@ -40,6 +40,7 @@ struct Config {
   bool debug = false;   // TERN_DEBUG
   int debug_min_t = 1;  // TERN_DEBUG_MIN_T
   long debug_budget = 1000;  // TERN_DEBUG_BUDGET (lines)
+  bool rotate = false;  // TERN_ROTATE: Hadamard-rotate the activations first
 };
 
 std::mutex g_mu;
@@ -74,6 +75,7 @@ void load_config_locked() {
   c.debug = env_int("TERN_DEBUG", 0) != 0;
   c.debug_min_t = env_int("TERN_DEBUG_MIN_T", 1);
   c.debug_budget = env_int("TERN_DEBUG_BUDGET", 1000);
+  c.rotate = env_int("TERN_ROTATE", 0) != 0;
   // keep the bands well formed
   if (c.small_t_max < 1) c.small_t_max = 1;
   if (c.small_t_max > 8) c.small_t_max = 8;
@@ -104,7 +106,8 @@ void probe(const Config& c, int rung, int T, int K, int N) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_debug_lines >= c.debug_budget) return;
   ++g_debug_lines;
-  fprintf(stderr, "tern: rung=%s T=%d K=%d N=%d\n", tern_rung_name(rung), T, K, N);
+  fprintf(stderr, "tern: rung=%s T=%d K=%d N=%d%s\n", tern_rung_name(rung), T, K, N,
+          c.rotate ? " rotated" : "");
   fflush(stderr);
 }
 
@@ -137,6 +140,7 @@ int device_state(DevState** out) {
     d.err = static_cast<int*>(p);
     if (smallt_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (s8_set_attributes() != cudaSuccess) return TERN_ECUDA;
+    if (quant_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -190,6 +194,10 @@ size_t s8_workspace_bytes(int T, int K) {
   return 2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
 }
 
+// K for which the activations can be staged rotated (whole 1024-wide
+// rotation blocks, and a rotated s8 token row fits in shared memory).
+bool rotation_shape_ok(int K) { return K % kRotBlock == 0 && K <= kRotateMaxK; }
+
 // Token tile for a rung, the tokens left, K and N: (TT, tokens in this launch).
 void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* take) {
   if (rung == TERN_RUNG_GEMV) {
@@ -206,7 +214,8 @@ void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* t
 
 // ws: workspace whose first kSyncBytes are the zeroed sync area.
 int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
-                float* y, int T, int K, int N, uint8_t* ws, cudaStream_t st, int* launches) {
+                float* y, int T, int K, int N, uint8_t* ws, int rotate, cudaStream_t st,
+                int* launches) {
   CUtensorMap tmW;
   int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                        static_cast<uint64_t>(K) / 4, 128, smallt_rows(1),
@@ -216,7 +225,7 @@ int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, co
     int tt = 0, take = 0;
     small_t_tile(rung, T - tok0, K, N, d->sms, &tt, &take);
     if (launch_smallt(tt, &tmW, Wp, s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
-                      tok0, take, d->sms, d->err, st, launches) != cudaSuccess)
+                      tok0, take, d->sms, rotate, d->err, st, launches) != cudaSuccess)
       return TERN_ECUDA;
     tok0 += take;
   }
@@ -366,12 +375,14 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
     return TERN_EINVAL;
   if (!aligned16(Wpacked) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
     return TERN_EALIGN;
+  const Config c = config();
+  if (c.rotate && !rotation_shape_ok(K)) return TERN_EINVAL;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;
-  const Config c = config();
   const int rung = pick_rung(c, T);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int rotate = c.rotate ? 1 : 0;
 
   const size_t need = tern_linear_workspace_bytes(T, K, N);
   if (!workspace || workspace_bytes < need) return TERN_ENOSPACE;
@@ -383,7 +394,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
     case TERN_RUNG_SMALL_T:
     case TERN_RUNG_SMALL_T_TILED:
       rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, static_cast<uint8_t*>(workspace),
-                       st, &launches);
+                       rotate, st, &launches);
       break;
     case TERN_RUNG_S8: {
       // after the sync area, which the s8 rung leaves untouched
@@ -392,7 +403,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       uint8_t* p1 = scratch;
       uint8_t* p2 = scratch + piece;
       float* xs = reinterpret_cast<float*>(scratch + 2 * piece);
-      if (launch_quant_pieces(x, p1, p2, xs, T, K, st) != cudaSuccess) return TERN_ECUDA;
+      if (launch_quant_pieces(x, p1, p2, xs, T, K, rotate, st) != cudaSuccess) return TERN_ECUDA;
       ++launches;
       CUtensorMap tmW, tmP1, tmP2;
       rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
@@ -439,6 +450,8 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
     return TERN_EALIGN;
   const int rung = T == 1 ? TERN_RUNG_GEMV : T <= 8 ? TERN_RUNG_SMALL_T : TERN_RUNG_SMALL_T_TILED;
   if (noalloc_need(T, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
+  const Config c = config();
+  if (c.rotate && !rotation_shape_ok(K)) return TERN_EINVAL;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;
@@ -446,12 +459,12 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   rc = noalloc_scratch(&scratch);
   if (rc != TERN_OK) return rc;
   int launches = 0;
-  rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch,
+  rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch, c.rotate ? 1 : 0,
                    static_cast<cudaStream_t>(stream), &launches);
   if (rc == TERN_OK) {
     t_last_rung = rung;
     t_last_launches = launches;
-    probe(config(), rung, T, K, N);
+    probe(c, rung, T, K, N);
   }
   return rc;
 }

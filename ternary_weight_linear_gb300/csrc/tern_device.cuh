@@ -352,6 +352,38 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lb
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
+// ---------------------------------------------------------------- rotation
+// Hadamard rotation of one 1024-wide block of one token held by a warp, in
+// the layout the activation staging uses: v[4 g + i] of lane l is element
+// 128 g + 4 l + i (g = 0..7, i = 0..3).  The orthonormal Sylvester matrix is
+// the tensor product of one 2 x 2 butterfly (a, b) -> (a + b, a - b) per
+// index bit, so the ten bits can be done in any order: element bits 0-1 and
+// 7-9 (the register index) inside the thread, bits 2-6 (the lane) across
+// lanes with shuffles.  The results are left unscaled (x 32); the caller
+// multiplies by 1/32 (exact) and rounds.
+__device__ __forceinline__ void hadamard_block_1024(float (&v)[32], int lane) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if ((r & h) == 0) {
+        const float a = v[r], b = v[r + h];
+        v[r] = a + b;
+        v[r + h] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    const bool upper = (lane & h) != 0;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[r], h);
+      v[r] = upper ? o - v[r] : v[r] + o;
+    }
+  }
+}
+
 // Instruction descriptor for kind::f8f6f4, e4m3 x e4m3 -> f32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |

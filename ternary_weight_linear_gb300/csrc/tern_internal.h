@@ -39,12 +39,13 @@ int smallt_gemv_tile(int K, int N, int num_sms);
 cudaError_t smallt_set_attributes();
 // Launch the small-T kernel(s) for tokens [tok0, tok0 + Tt) with Tt <= tt.
 // tmW: Wp's tensor map; sync: the zeroed sync area; work:
-// smallt_work_bytes(tt, K) bytes.  Adds the number of kernels launched to
+// smallt_work_bytes(tt, K) bytes.  rotate: stage the Hadamard-rotated
+// activations (K % 1024 == 0).  Adds the number of kernels launched to
 // *launches.
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
                           const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
-                          float* y, int K, int N, int tok0, int Tt, int num_sms, int* err,
-                          cudaStream_t stream, int* launches);
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int rotate,
+                          int* err, cudaStream_t stream, int* launches);
 
 // s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.
 constexpr int kS8TileN = 128;
@@ -68,14 +69,20 @@ cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, i
 cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int K,
                             cudaStream_t stream);
 // The s8 rung's activations: the int8 codes split into two exact e4m3 pieces.
+// rotate: quantise the blockwise Hadamard rotation of x (K % 1024 == 0,
+// K <= kRotateMaxK: the rotated row is staged in shared memory).
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
-                                int K, cudaStream_t stream);
+                                int K, int rotate, cudaStream_t stream);
+cudaError_t quant_set_attributes();
 
 // Base-3 packed weights (26 bytes per 128-weight group) -> 2-bit codes.
 cudaError_t launch_repack_t5(const uint8_t* P, uint32_t* Wp, int K, int N, int* bad,
                              cudaStream_t stream);
 // Blockwise (1024) Hadamard rotation of bf16 activations; xr may equal x.
 constexpr int kRotBlock = 1024;
+// Largest K for which tern_linear can stage rotated activations (the s8
+// rung keeps a rotated token row in shared memory).
+constexpr int kRotateMaxK = 65536;
 cudaError_t launch_rotate_bf16(const uint16_t* x, uint16_t* xr, int T, int K,
                                cudaStream_t stream);
 

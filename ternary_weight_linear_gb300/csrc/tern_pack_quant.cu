@@ -105,16 +105,50 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
 // p2 = q - p1 (multiples of 16 up to 128, and integers in [-8, 7]: all exact
 // in e4m3), written as p1[T][K] and p2[T][K] in the decoder's k order: within
 // every 16-wide block of k, byte slot 4i + b holds k = 4b + i.
+// rotate: the token's row is first Hadamard-rotated blockwise (each warp a
+// 1024-wide block at a time, hadamard_block_1024, scaled by 1/32 and rounded
+// once to bf16, nearest-even) into dynamic shared memory (2 K bytes), and
+// quantised from there.
 __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t* __restrict__ x,
                                                                  uint8_t* __restrict__ p1,
                                                                  uint8_t* __restrict__ p2,
-                                                                 float* __restrict__ xs, int K) {
+                                                                 float* __restrict__ xs, int K,
+                                                                 int rotate) {
+  extern __shared__ __align__(16) uint16_t xrow[];
   const int t = blockIdx.x;
   const uint16_t* row = x + static_cast<size_t>(t) * K;
+  if (rotate) {
+    const int lane = threadIdx.x & 31;
+    for (int b = threadIdx.x >> 5; b < K / kRotBlock; b += kQThreads / 32) {
+      float v[32];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(row + b * kRotBlock + 128 * g + 4 * lane);
+        v[4 * g + 0] = bf16_lo(raw.x);
+        v[4 * g + 1] = bf16_hi(raw.x);
+        v[4 * g + 2] = bf16_lo(raw.y);
+        v[4 * g + 3] = bf16_hi(raw.y);
+      }
+      hadamard_block_1024(v, lane);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          h[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[4 * g + i] * 0.03125f));
+        *reinterpret_cast<uint2*>(xrow + b * kRotBlock + 128 * g + 4 * lane) =
+            make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+      }
+    }
+    __syncthreads();
+    row = xrow;
+  }
+  // (plain 16-byte loads: row is global or, rotated, shared memory)
+  auto load16 = [&](int e) { return *reinterpret_cast<const uint4*>(row + e); };
   const int chunks = K >> 3;
   float a = 0.f;
   for (int c = threadIdx.x; c < chunks; c += kQThreads) {
-    const uint4 v = ldg_nc_v4(row + 8 * c);
+    const uint4 v = load16(8 * c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
@@ -130,8 +164,8 @@ __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t*
   const float scale = a / 127.0f;  // IEEE single-precision division
   if (threadIdx.x == 0) xs[t] = scale;
   for (int blk = threadIdx.x; blk < (K >> 4); blk += kQThreads) {
-    const uint4 v0 = ldg_nc_v4(row + 16 * blk);
-    const uint4 v1 = ldg_nc_v4(row + 16 * blk + 8);
+    const uint4 v0 = load16(16 * blk);
+    const uint4 v1 = load16(16 * blk + 8);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -319,9 +353,15 @@ cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int 
   return cudaGetLastError();
 }
 
+cudaError_t quant_set_attributes() {
+  return cudaFuncSetAttribute(quant_pieces_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              2 * kRotateMaxK);
+}
+
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
-                                int K, cudaStream_t stream) {
-  quant_pieces_kernel<<<T, kQThreads, 0, stream>>>(x, p1, p2, xs, K);
+                                int K, int rotate, cudaStream_t stream) {
+  const size_t smem = rotate ? 2 * static_cast<size_t>(K) : 0;
+  quant_pieces_kernel<<<T, kQThreads, smem, stream>>>(x, p1, p2, xs, K, rotate);
   return cudaGetLastError();
 }
 

@@ -437,6 +437,49 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16
   }
 }
 
+// Rotated activations (the Hadamard rotation of every 1024-wide block, fused
+// into the staging): one warp per (token slot, stage), the stage being one
+// rotation block.  The warp loads the block with lane l holding elements
+// 128 g + 4 l + i, rotates it in registers (hadamard_block_1024), scales by
+// 1/32 and rounds each value once to bf16, nearest-even; lane l then holds
+// exactly its four values of each of the stage's eight groups and builds
+// their pieces as the unrotated kernel does.  One-warp CTAs of at most 64
+// registers (at most one per SM), so they too fit beside a main-kernel CTA.
+template <int TT>
+__global__ void __launch_bounds__(32, 32) xprep_rot_kernel(const uint16_t* __restrict__ x,
+                                                           uint8_t* __restrict__ out, int K,
+                                                           int tok0, int Tt, int KS) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
+  const int lane = threadIdx.x;
+  const int tasks = TC<TT>::kH * KS;
+  for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
+    const int t = task / KS, ks = task % KS;
+    float v[32];
+#pragma unroll
+    for (int g = 0; g < kGS; ++g) {
+      uint2 raw = make_uint2(0u, 0u);
+      if (t < Tt)  // K is a multiple of 1024: every group of the stage exists
+        raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(tok0 + t) * K +
+                                              ks * kSTStageK + 128 * g + 4 * lane);
+      v[4 * g + 0] = __uint_as_float(raw.x << 16);
+      v[4 * g + 1] = __uint_as_float(raw.x & 0xFFFF0000u);
+      v[4 * g + 2] = __uint_as_float(raw.y << 16);
+      v[4 * g + 3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    }
+    hadamard_block_1024(v, lane);
+    uint8_t* st = out + static_cast<size_t>(ks) * TC<TT>::kXBytes;
+#pragma unroll
+    for (int g = 0; g < kGS; ++g) {
+      uint32_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[4 * g + i] * 0.03125f));
+      prep_task<TT>(make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16)), st, t, g, lane);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ main
 // The units of one CTA: a contiguous range, from stage ks0 of row block rb0.
 struct Visit {
@@ -1377,7 +1420,7 @@ int t1_slots(const SmallTGrid& g) {
 template <int TT>
 cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t* scales,
                       const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
-                      int tok0, int Tt, int num_sms, int* err, cudaStream_t stream,
+                      int tok0, int Tt, int num_sms, int rotate, int* err, cudaStream_t stream,
                       int* launches) {
   using C = TC<TT>;
   const SmallTGrid g = smallt_grid(K, N, num_sms);
@@ -1391,9 +1434,17 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   // in every CTA from x; with more, x is better read once by the prep kernel
   // (an L2 hit for the main kernel, whose own reads of x would queue behind
   // its weight stream).
-  const int build_x = C::kInKernelX && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
+  const int build_x = C::kInKernelX && !rotate && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
   cudaLaunchAttribute attr[1];
-  if (!build_x) {
+  if (rotate) {
+    // one warp per (token slot, stage): the stage is one rotation block
+    const int tasks = C::kH * g.KS;
+    const int blocks = tasks < num_sms ? tasks : num_sms;
+    cudaLaunchConfig_t pc = pdl_config(attr, dim3(blocks), dim3(32), 0, stream);
+    cudaError_t e = cudaLaunchKernelEx(&pc, xprep_rot_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  } else if (!build_x) {
     const int tasks = C::kH * kGS * g.KS;
     int blocks = (tasks + kPrepWarps - 1) / kPrepWarps;
     if (blocks > num_sms) blocks = num_sms;
@@ -1447,21 +1498,21 @@ cudaError_t smallt_set_attributes() {
 
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
                           const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
-                          float* y, int K, int N, int tok0, int Tt, int num_sms, int* err,
-                          cudaStream_t stream, int* launches) {
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int rotate,
+                          int* err, cudaStream_t stream, int* launches) {
   switch (tt) {
     case 1:
-      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
-                          launches);
+      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+                          stream, launches);
     case 4:
-      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
-                          launches);
+      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+                          stream, launches);
     case 8:
-      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err, stream,
-                          launches);
+      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+                          stream, launches);
     default:
-      return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, err,
-                           stream, launches);
+      return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate,
+                           err, stream, launches);
   }
 }
 

@@ -128,6 +128,21 @@ def test_invalid_arguments_are_rejected_before_device_work():
     assert lib.tern_selftest_wait_timeout(-1, None) == -1
 
 
+def test_rotation_switch_rejects_unrotatable_k(monkeypatch):
+    lib = tl.load()
+    p = 4096
+    monkeypatch.setenv("TERN_ROTATE", "1")
+    tl.tern_reload_env()
+    try:
+        # whole 1024-wide rotation blocks only, and K <= 65536
+        assert lib.tern_linear(p, p, p, p, 1, 512, 8, None, 0, None) == -1
+        assert lib.tern_linear(p, p, p, p, 1, 66560, 8, None, 0, None) == -1
+        assert lib.tern_linear_small_t_noalloc(p, p, p, p, 1, 1536, 8, None) == -1
+    finally:
+        monkeypatch.delenv("TERN_ROTATE")
+        tl.tern_reload_env()
+
+
 def test_no_gpu_gives_enodev():
     try:
         import torch
