@@ -67,7 +67,9 @@ typedef enum {
   TERN_RUNG_GEMV = 0,
   TERN_RUNG_SMALL_T = 1,
   TERN_RUNG_SMALL_T_TILED = 2,
-  TERN_RUNG_S8 = 3
+  TERN_RUNG_S8 = 3,
+  TERN_RUNG_BF16 = 4  /* exact bf16 prefill rung; chosen by TERN_RUNG=bf16 or,
+                         for T >= TERN_S8_MIN_T, TERN_PREFILL=bf16 */
 } tern_rung;
 
 /* Pack ternary int8 weights into the 2-bit layout above.
@@ -204,6 +206,10 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  * boundary; otherwise the result is that of tern_linear on tern_rotate_bf16's
  * output.  Source: the rotation the "NInfer sm_89 fork" write-up (section 9
  * item 2) fuses into the activation quantisation.
+ * The bf16 rung (TERN_RUNG=bf16, or TERN_PREFILL=bf16 for the s8 band)
+ * computes the bf16-rung definition above on tcgen05 kind::f16: weights as
+ * bf16 +-1, activations as they are, every product exact, fp32 sums; no
+ * activation quantisation (its workspace holds x reordered for the MMA).
  * The rung is chosen from T (see tern_select_rung); TERN_RUNG forces one.
  * Every rung is correct for every T. */
 int tern_linear(const uint32_t* Wpacked, const uint16_t* scales,
@@ -269,7 +275,7 @@ int tern_selftest_wait_timeout(int which, void* stream);
 /* Rung the dispatcher picks for T (after env overrides).  Host-only. */
 int tern_select_rung(int T);
 
-/* Name of a rung id ("gemv", "small_t", "small_t_tiled", "s8"), or "?". */
+/* Name of a rung id ("gemv", "small_t", "small_t_tiled", "s8", "bf16"), or "?". */
 const char* tern_rung_name(int rung);
 
 /* Rung launched by this thread's last successful tern_linear, or -1 / "none". */
@@ -287,7 +293,8 @@ int tern_last_launches(void);
 const char* tern_status_string(int status);
 
 /* Re-read the environment (TERN_RUNG, TERN_SMALL_T_MAX, TERN_TILED_MAX,
- * TERN_S8_MIN_T, TERN_ROTATE, TERN_DEBUG, TERN_DEBUG_MIN_T, TERN_DEBUG_BUDGET).  The
+ * TERN_S8_MIN_T, TERN_PREFILL, TERN_ROTATE, TERN_DEBUG, TERN_DEBUG_MIN_T,
+ * TERN_DEBUG_BUDGET).  The
  * environment is otherwise read once per process, on first use. */
 void tern_reload_env(void);
 

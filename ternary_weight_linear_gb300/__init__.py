@@ -28,7 +28,7 @@ __all__ = [
     "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES", "SYNC_BYTES", "T5_GROUP_BYTES", "ROTATION_BLOCK",
 ]
 
-RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8"}
+RUNGS = {0: "gemv", 1: "small_t", 2: "small_t_tiled", 3: "s8", 4: "bf16"}
 
 # Every symbol include/tern.h declares.
 EXPORTED_SYMBOLS = (

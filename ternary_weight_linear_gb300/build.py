@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libtern.so")
-SOURCES = ["tern_api.cu", "tern_pack_quant.cu", "tern_smallt.cu", "tern_s8.cu", "tern_selftest.cu"]
+SOURCES = ["tern_api.cu", "tern_pack_quant.cu", "tern_smallt.cu", "tern_s8.cu", "tern_bf16.cu",
+           "tern_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-I" + os.path.join(HERE, "..", "include"), "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
            "-Xptxas", "-warn-spills"]

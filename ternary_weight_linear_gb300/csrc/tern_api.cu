@@ -41,6 +41,7 @@ struct Config {
   int debug_min_t = 1;  // TERN_DEBUG_MIN_T
   long debug_budget = 1000;  // TERN_DEBUG_BUDGET (lines)
   bool rotate = false;  // TERN_ROTATE: Hadamard-rotate the activations first
+  bool prefill_bf16 = false;  // TERN_PREFILL=bf16: the bf16 rung for T >= s8_min_t
 };
 
 std::mutex g_mu;
@@ -63,6 +64,7 @@ int rung_from_name(const char* v) {
   if (!strcmp(v, "small_t")) return TERN_RUNG_SMALL_T;
   if (!strcmp(v, "small_t_tiled")) return TERN_RUNG_SMALL_T_TILED;
   if (!strcmp(v, "s8")) return TERN_RUNG_S8;
+  if (!strcmp(v, "bf16")) return TERN_RUNG_BF16;
   return -1;
 }
 
@@ -76,6 +78,10 @@ void load_config_locked() {
   c.debug_min_t = env_int("TERN_DEBUG_MIN_T", 1);
   c.debug_budget = env_int("TERN_DEBUG_BUDGET", 1000);
   c.rotate = env_int("TERN_ROTATE", 0) != 0;
+  {
+    const char* pf = getenv("TERN_PREFILL");
+    c.prefill_bf16 = pf && !strcmp(pf, "bf16");
+  }
   // keep the bands well formed
   if (c.small_t_max < 1) c.small_t_max = 1;
   if (c.small_t_max > 8) c.small_t_max = 8;
@@ -95,7 +101,7 @@ Config config() {
 
 int pick_rung(const Config& c, int T) {
   if (c.forced >= 0) return c.forced;
-  if (T >= c.s8_min_t) return TERN_RUNG_S8;
+  if (T >= c.s8_min_t) return c.prefill_bf16 ? TERN_RUNG_BF16 : TERN_RUNG_S8;
   if (T == 1) return TERN_RUNG_GEMV;
   if (T <= c.small_t_max) return TERN_RUNG_SMALL_T;
   return TERN_RUNG_SMALL_T_TILED;  // covers T up to tiled_max and any gap below s8_min_t
@@ -141,6 +147,7 @@ int device_state(DevState** out) {
     if (smallt_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (s8_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (quant_set_attributes() != cudaSuccess) return TERN_ECUDA;
+    if (bf16_set_attributes() != cudaSuccess) return TERN_ECUDA;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -276,6 +283,7 @@ const char* tern_rung_name(int rung) {
     case TERN_RUNG_SMALL_T: return "small_t";
     case TERN_RUNG_SMALL_T_TILED: return "small_t_tiled";
     case TERN_RUNG_S8: return "s8";
+    case TERN_RUNG_BF16: return "bf16";
     default: return "?";
   }
 }
@@ -424,6 +432,33 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       }
       rc = launch_s8(&tmW, &tmP1, &tmP2, y_tma ? &tmY : nullptr, scales, xs, y, T, K, N, d->sms,
                      d->err, st) == cudaSuccess
+               ? TERN_OK
+               : TERN_ECUDA;
+      ++launches;
+      break;
+    }
+    case TERN_RUNG_BF16: {
+      // after the sync area: x reordered for the MMA, 2 T K bytes (within
+      // the s8 scratch the workspace size covers)
+      uint16_t* xp = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + kSyncBytes);
+      if (launch_interleave(x, xp, T, K, rotate, d->sms, st) != cudaSuccess) return TERN_ECUDA;
+      ++launches;
+      CUtensorMap tmW, tmX;
+      rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
+                       static_cast<uint64_t>(K) / 4, 32, kS8TileN, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != TERN_OK) return rc;
+      rc = make_map_u8(&tmX, xp, 2 * static_cast<uint64_t>(K), static_cast<uint64_t>(T),
+                       2 * static_cast<uint64_t>(K), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != TERN_OK) return rc;
+      CUtensorMap tmY;
+      const bool y_tma = (N % 4) == 0;
+      if (y_tma) {
+        rc = make_map_f32(&tmY, y, static_cast<uint64_t>(N), static_cast<uint64_t>(T),
+                          static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);
+        if (rc != TERN_OK) return rc;
+      }
+      rc = launch_bf16(&tmW, &tmX, y_tma ? &tmY : nullptr, scales, y, T, K, N, d->sms, d->err,
+                       st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
       ++launches;

@@ -54,6 +54,17 @@ constexpr int kS8FoldWarps = 8;                          // warps folding the ac
 constexpr int kS8YBoxT = kS8TileT * 4 / kS8FoldWarps;   // tokens per fold warp's output box
 size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
+
+// bf16 rung: x reordered for the MMA (xp [T][K] bf16, optionally rotated
+// first), then tiles of 128 weight rows x 128 tokens on tcgen05 kind::f16.
+// tmW as for s8; tmX: xp as bytes [T][2K], box 128 B x 128 rows, 128-byte
+// swizzle; tmY as for s8 (or null).
+cudaError_t launch_interleave(const uint16_t* x, uint16_t* xp, int T, int K, int rotate,
+                              int num_sms, cudaStream_t stream);
+cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmY,
+                        const uint16_t* scales, float* y, int T, int K, int N, int num_sms,
+                        int* err, cudaStream_t stream);
+cudaError_t bf16_set_attributes();
 // tmW: packed weights, box 32 B x kS8TileN rows, no swizzle.  tmP1 / tmP2:
 // the two fp8 activation pieces [T][K], box 128 B x kS8TileT rows, 128-byte
 // swizzle.  tmY: y as fp32 [T][N], box 32 x kS8YBoxT, or null (then y is stored

@@ -16,7 +16,7 @@ from helpers import (assert_bf16_parity, assert_s8_parity, packed_to_numpy, samp
 
 pytestmark = pytest.mark.gpu
 
-RUNGS = ("gemv", "small_t", "small_t_tiled", "s8")
+RUNGS = ("gemv", "small_t", "small_t_tiled", "s8", "bf16")
 
 
 @pytest.fixture(scope="module")
@@ -339,7 +339,7 @@ ADVERSARIAL = ("absmax_on_zero_weight", "absmax_huge_on_zero_weight", "range_2e-
 
 @pytest.mark.parametrize("kind", ADVERSARIAL)
 @pytest.mark.parametrize("rung,T", [("gemv", 1), ("small_t", 3), ("small_t", 8),
-                                    ("small_t_tiled", 13), ("s8", 20)])
+                                    ("small_t_tiled", 13), ("s8", 20), ("bf16", 20)])
 def test_adversarial_activations(tl, kind, rung, T):
     import torch
     K, N = 1280, 300
@@ -455,6 +455,44 @@ def test_verify_config_sampled(tl, proj, T):
 @pytest.mark.parametrize("T", synth.PREFILL_T)
 def test_prefill_config_sampled(tl, proj, T):
     assert _check_case(tl, synth.config_prefill(proj, T), full=False) == "s8"
+
+
+class prefill_bf16:
+    """TERN_PREFILL=bf16 for the duration of a block: the s8 band runs on
+    the bf16 rung."""
+
+    def __init__(self, tl):
+        self.tl = tl
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in ("TERN_PREFILL", "TERN_RUNG")}
+        os.environ["TERN_PREFILL"] = "bf16"
+        os.environ.pop("TERN_RUNG", None)
+        self.tl.tern_reload_env()
+
+    def __exit__(self, *a):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        self.tl.tern_reload_env()
+
+
+@pytest.mark.parametrize("proj", ["gu", "dn", "ai", "ao"])
+@pytest.mark.parametrize("T", synth.PREFILL_T)
+def test_prefill_config_sampled_bf16_rung(tl, proj, T):
+    # the prefill configs on the exact bf16 rung: the bf16 bar, no quantisation
+    with prefill_bf16(tl):
+        assert tl.tern_select_rung(T) == 4
+        assert _check_case(tl, synth.config_prefill(proj, T), full=False) == "bf16"
+
+
+def test_prefill_switch_dispatch(tl):
+    with prefill_bf16(tl):
+        assert [tl.tern_rung_name(tl.tern_select_rung(T)) for T in (1, 16, 17, 2048)] == \
+            ["gemv", "small_t_tiled", "bf16", "bf16"]
+    assert tl.tern_rung_name(tl.tern_select_rung(17)) == "s8"
 
 
 @pytest.mark.parametrize("p_zero", synth.STACK_P_ZERO)
@@ -580,6 +618,7 @@ torch.cuda.synchronize()
     (5120, 34816, 4, "small_t", 2),
     (5120, 6144, 20, "small_t_tiled", 4),   # two token tiles (16 + 4)
     (5120, 6144, 37, "s8", 2),
+    (5120, 6144, 37, "bf16", 2),    # x reordered for the MMA, then the GEMM
 ])
 def test_launch_count_probe(tl, K, N, T, rung, expect):
     import torch
