@@ -264,6 +264,8 @@ def run_stack(tl, torch, gen, dev, peaks, stream):
 
 L2_BYTES = 129 * 2 ** 20
 COMPACT_T = {"gate_up": (1, 4, 8, 16, 17, 508, 2048), "down": (1, 4, 8, 16, 17, 508, 2048)}
+ROTATED_T = (1, 16, 2048)
+BF16_T = (17, 508, 2048)
 
 
 def rotated_copies(K, N):
@@ -317,7 +319,9 @@ def time_rotated(tl, torch, layers, K, N, T, gen, dev, reps=10):
 def compact_sweep(tl, torch, gen, dev, peaks):
     """The configs' token counts on the two 27B-like MLP projections: T = 1
     (decode), 4, 8, 16 (speculative verify) on the bandwidth rungs and 17,
-    508, 2048 on s8, each over rotated weight copies."""
+    508, 2048 on s8, each over rotated weight copies; then BF16_T again on
+    the exact bf16 prefill rung, and gate+up at ROTATED_T with the fused
+    Hadamard rotation switched on."""
     rows = []
     for name, (K, N) in (("gate_up", GU), ("down", DN)):
         layers = [make_layer(tl, torch, K, N, gen, dev) for _ in range(rotated_copies(K, N))]
@@ -335,6 +339,41 @@ def compact_sweep(tl, torch, gen, dev, peaks):
                 row.update({"GB/s": round(gbs, 1),
                             "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)})
             rows.append(row)
+        # the exact bf16 prefill rung (TERN_PREFILL=bf16) against s8 on the same calls
+        os.environ["TERN_PREFILL"] = "bf16"
+        tl.tern_reload_env()
+        try:
+            for T in BF16_T:
+                us, rung, nl = time_rotated(tl, torch, layers, K, N, T, gen, dev,
+                                            reps=10 if T < 2048 else 4)
+                s8row = next(r for r in rows if r["proj"] == name and r["T"] == T
+                             and r["rung"] == "s8")
+                tops = 2.0 * T * K * N / (us * 1e-6) / 1e12
+                rows.append({"proj": name, "K": K, "N": N, "T": T, "rung": rung,
+                             "copies": len(layers), "launches_per_call": nl,
+                             "us_per_call": round(us, 3), "TOPS": round(tops, 1),
+                             "frac_of_bf16_peak": round(tops / peaks["bf16_tflops"], 4),
+                             "vs_s8": round(us / s8row["us_per_call"], 3)})
+        finally:
+            os.environ.pop("TERN_PREFILL", None)
+            tl.tern_reload_env()
+        if name == "gate_up":
+            # the fused Hadamard rotation (TERN_ROTATE=1) against the plain calls above
+            os.environ["TERN_ROTATE"] = "1"
+            tl.tern_reload_env()
+            try:
+                for T in ROTATED_T:
+                    us, rung, nl = time_rotated(tl, torch, layers, K, N, T, gen, dev,
+                                                reps=10 if T < 2048 else 4)
+                    plain = next(r for r in rows if r["proj"] == name and r["T"] == T
+                                 and r["rung"] != "bf16")
+                    rows.append({"proj": name, "K": K, "N": N, "T": T, "rung": rung,
+                                 "rotated": True, "copies": len(layers),
+                                 "launches_per_call": nl, "us_per_call": round(us, 3),
+                                 "vs_plain": round(us / plain["us_per_call"], 3)})
+            finally:
+                os.environ.pop("TERN_ROTATE", None)
+                tl.tern_reload_env()
         del layers
         torch.cuda.empty_cache()
     return rows
@@ -422,7 +461,7 @@ def run_ours(args, rank, world, local):
     sweep = compact_sweep(tl, torch, gen, dev, peaks)
 
     def roofline_of(proj, summary):
-        row = next(r for r in sweep if r["proj"] == proj and r["T"] == 1)
+        row = next(r for r in sweep_plain if r["proj"] == proj and r["T"] == 1)
         K, N = row["K"], row["N"]
         alg = algorithmic_bytes(1, K, N)
         gbs = alg / (row["us_per_call"] * 1e-6) / 1e9
@@ -435,9 +474,10 @@ def run_ours(args, rank, world, local):
                 "avg_launch_us": row["us_per_call"], "launches_per_call": row["launches_per_call"],
                 "rotation": f"{row['copies']} weight copies (> 4x L2)"}
 
+    sweep_plain = [r for r in sweep if not r.get("rotated") and r["rung"] != "bf16"]
     roofline = roofline_of("gate_up", "smallt_kernel_gu_t1.md")
     roofline_dn = roofline_of("down", "smallt_kernel_dn_t1.md")
-    s8_rows = [r for r in sweep if r["T"] == 2048]
+    s8_rows = [r for r in sweep_plain if r["T"] == 2048]
     s8_us = sum(r["us_per_call"] for r in s8_rows)
     s8_tops = sum(2.0 * r["T"] * r["K"] * r["N"] for r in s8_rows) / (s8_us * 1e-6) / 1e12
     # The s8 rung contracts every int8 product as two e4m3 products (the

@@ -354,14 +354,17 @@ constexpr int kPrepWarps = 4;
 
 // Group jg of a stage's block (at st) for token slot t, from the lane's four
 // bf16 values raw.  The whole warp calls it.
-template <int TT>
-__device__ __forceinline__ void prep_task(uint2 raw, uint8_t* st, int t, int jg, int lane) {
-  using C = TC<TT>;
+__device__ __forceinline__ float lane_absmax4(uint2 raw) {
   const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
-  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+}
+
+// As prep_task, with the group's absmax m already reduced over the warp.
+template <int TT>
+__device__ __forceinline__ void prep_task_m(uint2 raw, float m, uint8_t* st, int t, int jg,
+                                            int lane) {
+  using C = TC<TT>;
   uint32_t hp[3];
   float lsum;
   const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
@@ -402,6 +405,14 @@ __device__ __forceinline__ void prep_task(uint2 raw, uint8_t* st, int t, int jg,
       fl[(kGS + jg) * C::kH + t] = lsum;
     }
   }
+}
+
+template <int TT>
+__device__ __forceinline__ void prep_task(uint2 raw, uint8_t* st, int t, int jg, int lane) {
+  float m = lane_absmax4(raw);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  prep_task_m<TT>(raw, m, st, t, jg, lane);
 }
 
 template <int TT>
@@ -469,14 +480,25 @@ __global__ void __launch_bounds__(32, 32) xprep_rot_kernel(const uint16_t* __res
     }
     hadamard_block_1024(v, lane);
     uint8_t* st = out + static_cast<size_t>(ks) * TC<TT>::kXBytes;
+    // the eight groups' bf16 values and absmax reductions side by side (eight
+    // independent shuffle chains), then their pieces
+    uint2 raw[kGS];
+    float m[kGS];
 #pragma unroll
     for (int g = 0; g < kGS; ++g) {
       uint32_t b[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         b[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[4 * g + i] * 0.03125f));
-      prep_task<TT>(make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16)), st, t, g, lane);
+      raw[g] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+      m[g] = lane_absmax4(raw[g]);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < kGS; ++g) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
+#pragma unroll
+    for (int g = 0; g < kGS; ++g) prep_task_m<TT>(raw[g], m[g], st, t, g, lane);
   }
 }
 
