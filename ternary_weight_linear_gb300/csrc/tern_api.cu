@@ -42,6 +42,7 @@ struct Config {
   long debug_budget = 1000;  // TERN_DEBUG_BUDGET (lines)
   bool rotate = false;  // TERN_ROTATE: Hadamard-rotate the activations first
   bool prefill_bf16 = false;  // TERN_PREFILL=bf16: the bf16 rung for T >= s8_min_t
+  bool decode_int8 = false;   // TERN_DECODE_ACT=int8: int8 activations on the T <= 16 rungs
 };
 
 std::mutex g_mu;
@@ -81,6 +82,8 @@ void load_config_locked() {
   {
     const char* pf = getenv("TERN_PREFILL");
     c.prefill_bf16 = pf && !strcmp(pf, "bf16");
+    const char* da = getenv("TERN_DECODE_ACT");
+    c.decode_int8 = da && !strcmp(da, "int8");
   }
   // keep the bands well formed
   if (c.small_t_max < 1) c.small_t_max = 1;
@@ -112,8 +115,9 @@ void probe(const Config& c, int rung, int T, int K, int N) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_debug_lines >= c.debug_budget) return;
   ++g_debug_lines;
-  fprintf(stderr, "tern: rung=%s T=%d K=%d N=%d%s\n", tern_rung_name(rung), T, K, N,
-          c.rotate ? " rotated" : "");
+  const bool bw = rung != TERN_RUNG_S8 && rung != TERN_RUNG_BF16;
+  fprintf(stderr, "tern: rung=%s T=%d K=%d N=%d%s%s\n", tern_rung_name(rung), T, K, N,
+          c.rotate ? " rotated" : "", c.decode_int8 && bw ? " int8" : "");
   fflush(stderr);
 }
 
@@ -205,6 +209,11 @@ size_t s8_workspace_bytes(int T, int K) {
 // rotation blocks, and a rotated s8 token row fits in shared memory).
 bool rotation_shape_ok(int K) { return K % kRotBlock == 0 && K <= kRotateMaxK; }
 
+// How the small-T rungs stage the activations under config c.
+int small_t_act(const Config& c) {
+  return c.decode_int8 ? kActInt8 : (c.rotate ? kActRotated : kActExact);
+}
+
 // Token tile for a rung, the tokens left, K and N: (TT, tokens in this launch).
 void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* take) {
   if (rung == TERN_RUNG_GEMV) {
@@ -221,7 +230,7 @@ void small_t_tile(int rung, int left, int K, int N, int num_sms, int* tt, int* t
 
 // ws: workspace whose first kSyncBytes are the zeroed sync area.
 int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, const uint16_t* x,
-                float* y, int T, int K, int N, uint8_t* ws, int rotate, cudaStream_t st,
+                float* y, int T, int K, int N, uint8_t* ws, int act, cudaStream_t st,
                 int* launches) {
   CUtensorMap tmW;
   int rc = make_map_u8(&tmW, Wp, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
@@ -232,7 +241,7 @@ int run_small_t(DevState* d, int rung, const uint32_t* Wp, const uint16_t* s, co
     int tt = 0, take = 0;
     small_t_tile(rung, T - tok0, K, N, d->sms, &tt, &take);
     if (launch_smallt(tt, &tmW, Wp, s, x, reinterpret_cast<int*>(ws), ws + kSyncBytes, y, K, N,
-                      tok0, take, d->sms, rotate, d->err, st, launches) != cudaSuccess)
+                      tok0, take, d->sms, act, d->err, st, launches) != cudaSuccess)
       return TERN_ECUDA;
     tok0 += take;
   }
@@ -385,10 +394,13 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
     return TERN_EALIGN;
   const Config c = config();
   if (c.rotate && !rotation_shape_ok(K)) return TERN_EINVAL;
+  const int rung = pick_rung(c, T);
+  // the int8 decode variant has no rotated form
+  if (c.rotate && c.decode_int8 && rung != TERN_RUNG_S8 && rung != TERN_RUNG_BF16)
+    return TERN_EINVAL;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;
-  const int rung = pick_rung(c, T);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int rotate = c.rotate ? 1 : 0;
 
@@ -402,7 +414,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
     case TERN_RUNG_SMALL_T:
     case TERN_RUNG_SMALL_T_TILED:
       rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, static_cast<uint8_t*>(workspace),
-                       rotate, st, &launches);
+                       small_t_act(c), st, &launches);
       break;
     case TERN_RUNG_S8: {
       // after the sync area, which the s8 rung leaves untouched
@@ -487,6 +499,7 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   if (noalloc_need(T, K) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ENOSPACE;
   const Config c = config();
   if (c.rotate && !rotation_shape_ok(K)) return TERN_EINVAL;
+  if (c.rotate && c.decode_int8) return TERN_EINVAL;
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != TERN_OK) return rc;
@@ -494,7 +507,7 @@ int tern_linear_small_t_noalloc(const uint32_t* Wpacked, const uint16_t* scales,
   rc = noalloc_scratch(&scratch);
   if (rc != TERN_OK) return rc;
   int launches = 0;
-  rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch, c.rotate ? 1 : 0,
+  rc = run_small_t(d, rung, Wpacked, scales, x, y, T, K, N, scratch, small_t_act(c),
                    static_cast<cudaStream_t>(stream), &launches);
   if (rc == TERN_OK) {
     t_last_rung = rung;

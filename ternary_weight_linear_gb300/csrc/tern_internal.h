@@ -39,12 +39,15 @@ int smallt_gemv_tile(int K, int N, int num_sms);
 cudaError_t smallt_set_attributes();
 // Launch the small-T kernel(s) for tokens [tok0, tok0 + Tt) with Tt <= tt.
 // tmW: Wp's tensor map; sync: the zeroed sync area; work:
-// smallt_work_bytes(tt, K) bytes.  rotate: stage the Hadamard-rotated
-// activations (K % 1024 == 0).  Adds the number of kernels launched to
+// smallt_work_bytes(tt, K) bytes.  act: how the activations are staged
+// (kActExact: exact bf16 pieces; kActRotated: the same for the
+// Hadamard-rotated activations, K % 1024 == 0; kActInt8: per-token int8
+// codes, the s8 definition).  Adds the number of kernels launched to
 // *launches.
+enum : int { kActExact = 0, kActRotated = 1, kActInt8 = 2 };
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
                           const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
-                          float* y, int K, int N, int tok0, int Tt, int num_sms, int rotate,
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int act,
                           int* err, cudaStream_t stream, int* launches);
 
 // s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.

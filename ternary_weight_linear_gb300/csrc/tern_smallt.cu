@@ -360,14 +360,13 @@ __device__ __forceinline__ float lane_absmax4(uint2 raw) {
   return fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 }
 
-// As prep_task, with the group's absmax m already reduced over the warp.
+// Write group jg of a stage's block (at st) for token slot t: the lane's
+// three piece bytes for its four elements (hp[j], element i in byte i), and
+// (lane 0) the group's factor f and leftover sum lsum.
 template <int TT>
-__device__ __forceinline__ void prep_task_m(uint2 raw, float m, uint8_t* st, int t, int jg,
-                                            int lane) {
+__device__ __forceinline__ void prep_write(const uint32_t (&hp)[3], float f, float lsum,
+                                           uint8_t* st, int t, int jg, int lane) {
   using C = TC<TT>;
-  uint32_t hp[3];
-  float lsum;
-  const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
   if constexpr (TT == 1) {
     // compact block: 16-block j = 8 jg + l/4 at bytes 32 j (piece 0), 32 j + 16
     // (piece 1) and kX1Sbo + 32 j (piece 2); position b = l%4: value i at 4i + b
@@ -407,6 +406,16 @@ __device__ __forceinline__ void prep_task_m(uint2 raw, float m, uint8_t* st, int
   }
 }
 
+// As prep_task, with the group's absmax m already reduced over the warp.
+template <int TT>
+__device__ __forceinline__ void prep_task_m(uint2 raw, float m, uint8_t* st, int t, int jg,
+                                            int lane) {
+  uint32_t hp[3];
+  float lsum;
+  const float f = group_pieces(raw, m, hp[0], hp[1], hp[2], lsum);
+  prep_write<TT>(hp, f, lsum, st, t, jg, lane);
+}
+
 template <int TT>
 __device__ __forceinline__ void prep_task(uint2 raw, uint8_t* st, int t, int jg, int lane) {
   float m = lane_absmax4(raw);
@@ -444,6 +453,67 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16
         prep_task<TT>(raw[u], out + static_cast<size_t>(gi / kGS) * TC<TT>::kXBytes,
                       task / groups, gi % kGS, lane);
       }
+    }
+  }
+}
+
+// int8 activations (the decode variant of the pages' int8 path): per token,
+// xs = absmax / 127 and q = clamp(rint(x / xs), -127, 127) with IEEE fp32
+// division, the arithmetic of tern_quant_act_s8; q is split as on the s8
+// rung into p1 = 16 floor((q + 8) / 16) and p2 = q - p1, both exact in e5m2
+// (multiples of 16 up to 128, integers in [-8, 7]), the third piece is zero
+// and the factor is 8 xs, so the fold adds s * 8 xs * (acc / 8): the s8
+// rung's value with exact integer group sums.  One CTA per (token slot,
+// stage): its four warps first find the token's absmax (the whole row), then
+// build the stage's eight groups, two per warp.  4 warps of 32 registers and
+// 16 bytes of shared memory: it fits beside a main-kernel CTA.
+template <int TT>
+__global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_i8_kernel(
+    const uint16_t* __restrict__ x, uint8_t* __restrict__ out, int K, int tok0, int Tt, int KS) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
+  __shared__ float red[kPrepWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = K >> 7;
+  const int tasks = TC<TT>::kH * KS;
+  for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
+    const int t = task / KS, ks = task % KS;
+    const uint16_t* row = x + static_cast<size_t>(tok0 + (t < Tt ? t : 0)) * K;
+    float a = 0.f;
+    if (t < Tt)
+      for (int c = threadIdx.x; c < (K >> 3); c += kPrepWarps * 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + 8 * c);
+        a = fmaxf(a, fmaxf(lane_absmax4(make_uint2(v.x, v.y)), lane_absmax4(make_uint2(v.z, v.w))));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kPrepWarps; ++w) a = fmaxf(a, red[w]);
+    __syncthreads();  // red is rewritten by the next task
+    const float xs = a / 127.0f;  // IEEE single-precision division
+    uint8_t* st = out + static_cast<size_t>(ks) * TC<TT>::kXBytes;
+    for (int jg = warp; jg < kGS; jg += kPrepWarps) {
+      const int g = ks * kGS + jg;
+      uint2 raw = make_uint2(0u, 0u);
+      if (t < Tt && g < G) raw = *reinterpret_cast<const uint2*>(row + g * 128 + 4 * lane);
+      const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      uint32_t hp[3] = {0u, 0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int q = 0;
+        if (a > 0.f) q = static_cast<int>(fminf(fmaxf(rintf(v[i] / xs), -127.f), 127.f));
+        const int h = (q + 8) >> 4;  // floor((q + 8) / 16), in [-8, 8]
+        hp[0] |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(static_cast<float>(16 * h),
+                                                             __NV_SATFINITE, __NV_E5M2))
+                 << (8 * i);
+        hp[1] |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(static_cast<float>(q - 16 * h),
+                                                             __NV_SATFINITE, __NV_E5M2))
+                 << (8 * i);
+      }
+      prep_write<TT>(hp, 8.0f * xs, 0.f, st, t, jg, lane);
     }
   }
 }
@@ -1442,8 +1512,9 @@ int t1_slots(const SmallTGrid& g) {
 template <int TT>
 cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t* scales,
                       const uint16_t* x, int* sync, uint8_t* work, float* y, int K, int N,
-                      int tok0, int Tt, int num_sms, int rotate, int* err, cudaStream_t stream,
+                      int tok0, int Tt, int num_sms, int act, int* err, cudaStream_t stream,
                       int* launches) {
+  const bool rotate = act == kActRotated;
   using C = TC<TT>;
   const SmallTGrid g = smallt_grid(K, N, num_sms);
   const int nslots = C::kInKernelX ? t1_slots(g) : 0;
@@ -1456,9 +1527,17 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   // in every CTA from x; with more, x is better read once by the prep kernel
   // (an L2 hit for the main kernel, whose own reads of x would queue behind
   // its weight stream).
-  const int build_x = C::kInKernelX && !rotate && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
+  const int build_x = C::kInKernelX && act == kActExact && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
   cudaLaunchAttribute attr[1];
-  if (rotate) {
+  if (act == kActInt8) {
+    // one 4-warp CTA per (token slot, stage)
+    const int tasks = C::kH * g.KS;
+    const int blocks = tasks < num_sms ? tasks : num_sms;
+    cudaLaunchConfig_t pc = pdl_config(attr, dim3(blocks), dim3(kPrepWarps * 32), 0, stream);
+    cudaError_t e = cudaLaunchKernelEx(&pc, xprep_i8_kernel<TT>, x, xprep, K, tok0, Tt, g.KS);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  } else if (rotate) {
     // one warp per (token slot, stage): the stage is one rotation block
     const int tasks = C::kH * g.KS;
     const int blocks = tasks < num_sms ? tasks : num_sms;
@@ -1520,20 +1599,20 @@ cudaError_t smallt_set_attributes() {
 
 cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
                           const uint16_t* scales, const uint16_t* x, int* sync, uint8_t* work,
-                          float* y, int K, int N, int tok0, int Tt, int num_sms, int rotate,
+                          float* y, int K, int N, int tok0, int Tt, int num_sms, int act,
                           int* err, cudaStream_t stream, int* launches) {
   switch (tt) {
     case 1:
-      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+      return launch_tt<1>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, act, err,
                           stream, launches);
     case 4:
-      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+      return launch_tt<4>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, act, err,
                           stream, launches);
     case 8:
-      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate, err,
+      return launch_tt<8>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, act, err,
                           stream, launches);
     default:
-      return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, rotate,
+      return launch_tt<16>(tmW, Wp, scales, x, sync, work, y, K, N, tok0, Tt, num_sms, act,
                            err, stream, launches);
   }
 }

@@ -143,6 +143,21 @@ def test_rotation_switch_rejects_unrotatable_k(monkeypatch):
         tl.tern_reload_env()
 
 
+def test_int8_decode_has_no_rotated_form(monkeypatch):
+    lib = tl.load()
+    p = 4096
+    monkeypatch.setenv("TERN_ROTATE", "1")
+    monkeypatch.setenv("TERN_DECODE_ACT", "int8")
+    tl.tern_reload_env()
+    try:
+        assert lib.tern_linear(p, p, p, p, 1, 1024, 8, None, 0, None) == -1
+        assert lib.tern_linear_small_t_noalloc(p, p, p, p, 4, 1024, 8, None) == -1
+    finally:
+        monkeypatch.delenv("TERN_ROTATE")
+        monkeypatch.delenv("TERN_DECODE_ACT")
+        tl.tern_reload_env()
+
+
 def test_no_gpu_gives_enodev():
     try:
         import torch
