@@ -266,6 +266,7 @@ L2_BYTES = 129 * 2 ** 20
 COMPACT_T = {"gate_up": (1, 4, 8, 16, 17, 508, 2048), "down": (1, 4, 8, 16, 17, 508, 2048)}
 ROTATED_T = (1, 16, 2048)
 BF16_T = (17, 508, 2048)
+INT8_DECODE_T = (1, 16)
 
 
 def rotated_copies(K, N):
@@ -357,6 +358,21 @@ def compact_sweep(tl, torch, gen, dev, peaks):
         finally:
             os.environ.pop("TERN_PREFILL", None)
             tl.tern_reload_env()
+        # the int8-activation decode variant (TERN_DECODE_ACT=int8) on the T <= 16 rungs
+        os.environ["TERN_DECODE_ACT"] = "int8"
+        tl.tern_reload_env()
+        try:
+            for T in INT8_DECODE_T:
+                us, rung, nl = time_rotated(tl, torch, layers, K, N, T, gen, dev)
+                plain = next(r for r in rows if r["proj"] == name and r["T"] == T
+                             and r["rung"] not in ("bf16",) and not r.get("int8_decode"))
+                rows.append({"proj": name, "K": K, "N": N, "T": T, "rung": rung,
+                             "int8_decode": True, "copies": len(layers),
+                             "launches_per_call": nl, "us_per_call": round(us, 3),
+                             "vs_exact": round(us / plain["us_per_call"], 3)})
+        finally:
+            os.environ.pop("TERN_DECODE_ACT", None)
+            tl.tern_reload_env()
         if name == "gate_up":
             # the fused Hadamard rotation (TERN_ROTATE=1) against the plain calls above
             os.environ["TERN_ROTATE"] = "1"
@@ -366,7 +382,7 @@ def compact_sweep(tl, torch, gen, dev, peaks):
                     us, rung, nl = time_rotated(tl, torch, layers, K, N, T, gen, dev,
                                                 reps=10 if T < 2048 else 4)
                     plain = next(r for r in rows if r["proj"] == name and r["T"] == T
-                                 and r["rung"] != "bf16")
+                                 and r["rung"] != "bf16" and not r.get("int8_decode"))
                     rows.append({"proj": name, "K": K, "N": N, "T": T, "rung": rung,
                                  "rotated": True, "copies": len(layers),
                                  "launches_per_call": nl, "us_per_call": round(us, 3),
@@ -474,7 +490,8 @@ def run_ours(args, rank, world, local):
                 "avg_launch_us": row["us_per_call"], "launches_per_call": row["launches_per_call"],
                 "rotation": f"{row['copies']} weight copies (> 4x L2)"}
 
-    sweep_plain = [r for r in sweep if not r.get("rotated") and r["rung"] != "bf16"]
+    sweep_plain = [r for r in sweep if not r.get("rotated") and not r.get("int8_decode")
+                   and r["rung"] != "bf16"]
     roofline = roofline_of("gate_up", "smallt_kernel_gu_t1.md")
     roofline_dn = roofline_of("down", "smallt_kernel_dn_t1.md")
     s8_rows = [r for r in sweep_plain if r["T"] == 2048]

@@ -206,6 +206,12 @@ size_t tern_linear_workspace_bytes(int T, int K, int N);
  * boundary; otherwise the result is that of tern_linear on tern_rotate_bf16's
  * output.  Source: the rotation the "NInfer sm_89 fork" write-up (section 9
  * item 2) fuses into the activation quantisation.
+ * With TERN_DECODE_ACT=int8 the T <= 16 rungs compute the s8 definition
+ * instead (per-token int8 codes as tern_quant_act_s8 makes them, exact
+ * integer group sums, y = xs * sum_g s * acc, held to the s8 rung's bars):
+ * the int8-activation decode path of the "NInfer sm_89 fork" write-up
+ * (section 9 item 2).  It has no rotated form (TERN_ROTATE with it:
+ * TERN_EINVAL on those rungs).
  * The bf16 rung (TERN_RUNG=bf16, or TERN_PREFILL=bf16 for the s8 band)
  * computes the bf16-rung definition above on tcgen05 kind::f16: weights as
  * bf16 +-1, activations as they are, every product exact, fp32 sums; no
@@ -293,8 +299,8 @@ int tern_last_launches(void);
 const char* tern_status_string(int status);
 
 /* Re-read the environment (TERN_RUNG, TERN_SMALL_T_MAX, TERN_TILED_MAX,
- * TERN_S8_MIN_T, TERN_PREFILL, TERN_ROTATE, TERN_DEBUG, TERN_DEBUG_MIN_T,
- * TERN_DEBUG_BUDGET).  The
+ * TERN_S8_MIN_T, TERN_PREFILL, TERN_ROTATE, TERN_DECODE_ACT, TERN_DEBUG,
+ * TERN_DEBUG_MIN_T, TERN_DEBUG_BUDGET).  The
  * environment is otherwise read once per process, on first use. */
 void tern_reload_env(void);
 
