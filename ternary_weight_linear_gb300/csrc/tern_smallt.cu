@@ -138,6 +138,9 @@ constexpr int kX1Stage = 2 * kX1Sbo;                    // bytes per stage block
 constexpr int kX1Slot = kX1Stage + (kSTStageK / 128) * 8;
 static_assert(kX1Sbo >= kSTStageK / 16 * 32 + 7 * 16, "the junk columns' overrun stays inside");
 
+// Largest cluster of CTAs sharing one row block (cluster mode, T = 1).
+constexpr int kMaxCl = 4;
+
 template <int TT>
 struct TC {
   // Token slots of the B operand and MMA N (= accumulator columns per group).
@@ -191,9 +194,10 @@ struct TC {
   static constexpr int kSOff = kXOff + (kInKernelX ? 0 : kStages * kXFrag);
   static constexpr int kBarOff = kSOff + kSStages * kSBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kSStages + 4 * kNSub + 2 * kNDH + 8 + 2 +
-                                  (kInKernelX ? kSmallTX1MaxSlots : 0);
+                                  (kInKernelX ? kSmallTX1MaxSlots : 0) + 1;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
-  static constexpr int kPartOff = kTmemSlot + 16;  // fold: half-stage 1 sums [TT][128]
+  // 16-byte aligned from here on: the regions below are read as float4 / uint2
+  static constexpr int kPartOff = (kTmemSlot + 16 + 15) / 16 * 16;  // fold: half-stage 1 sums [TT][128]
   // fold: the CTA's split row blocks' sums [2][TT][128], for the split-row warp
   static constexpr int kSplitOff = kPartOff + TT * kRows * 4;
   // fold: one group of x per fold warp for exact leftovers [kFoldWarps][128] bf16
@@ -202,7 +206,12 @@ struct TC {
   // block, decided when the row block ends [kFoldWarps][kDefer] (code, |f|)
   static constexpr int kDefer = 8;
   static constexpr int kDefOff = kLxOff + kFoldWarps * 256;
-  static constexpr int kX1Off = (kDefOff + kFoldWarps * kDefer * 8 + 127) / 128 * 128;  // (T = 1)
+  // cluster mode (TT = 1): the other ranks' partial sums of the row block,
+  // written into rank 0's shared memory [kMaxCl - 1][TT][128]
+  static constexpr bool kCluster = TT == 1;
+  static constexpr int kClOff = kDefOff + kFoldWarps * kDefer * 8;
+  static constexpr int kX1Off =
+      (kClOff + (kCluster ? (kMaxCl - 1) * TT * kRows * 4 : 0) + 127) / 128 * 128;  // (T = 1)
   // shared memory for nslots resident T = 1 blocks: fixed part, blocks, alignment slack
   static constexpr int smem_bytes(int nslots) {
     return kX1Off + (kInKernelX ? nslots * kX1Slot : 0) + 1024;
@@ -217,6 +226,9 @@ struct TC {
   static_assert(kDCol + kNDH * kDSlot <= kTmemCols, "TMEM budget");
   static_assert(kXFrag % 16 == 0 && kXF % 16 == 0 && kXBytes % 16 == 0, "bulk copy sizes");
   static_assert(kSBytes % 16 == 0 && kBarOff % 8 == 0, "alignment");
+  static_assert(kPartOff % 16 == 0 && kSplitOff % 16 == 0 && kLxOff % 16 == 0 &&
+                    kDefOff % 16 == 0 && kClOff % 16 == 0 && kX1Off % 128 == 0,
+                "vector-accessed regions must be 16-byte aligned");
   static_assert(kAllocMax <= 227 * 1024, "shared memory");
 };
 
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
                   const uint16_t* __restrict__ scales, const uint16_t* __restrict__ x,
                   const uint8_t* __restrict__ xprep, float* __restrict__ y,
                   int* __restrict__ tickets, float* __restrict__ partials, int K, int N, int tok0,
-                  int Tt, int KS, int nslots, long long U, int build_x, int* err) {
+                  int Tt, int KS, int nslots, long long U, int build_x, int cl, int* err) {
   using C = TC<TT>;
   constexpr int S = C::kStages;
   constexpr int SS = C::kSStages;
@@ -662,6 +674,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   // CTA's i-th split row block
   uint64_t* pub = pfree + 4;
   uint64_t* xready = pub + 2;  // (T = 1) activation block of slot q built
+  // (cluster mode, rank 0) the other ranks' partial sums have landed
+  uint64_t* cfull = xready + (C::kInKernelX ? kSmallTX1MaxSlots : 0);
   uint8_t* xres = smem + C::kX1Off;  // (T = 1) resident slots: block + (f, L)[kGS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlot);
 
@@ -696,6 +710,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     if constexpr (C::kInKernelX)
       for (int q = 0; q < nslots; ++q)  // the producer's copy, or one group per fold warp
         mbar_init(&xready[q], build_x ? kFoldWarps : 1);
+    // every lane of every other rank's split-row warp arrives once
+    mbar_init(cfull, cl > 1 ? (cl - 1) * 32 : 1);
     fence_mbar_init();
     prefetch_tensormap(&tmW);
   }
@@ -707,8 +723,21 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
 
   const long long P = gridDim.x;
   const int cta = blockIdx.x;
-  const long long begin = U * cta / P;
-  const long long end = U * (cta + 1) / P;
+  // Work: equal contiguous ranges of the (row block, stage) units; or, in
+  // cluster mode (cl > 1), row block cta / cl cut into cl contiguous stage
+  // ranges, one per rank of the cluster.
+  long long begin, end;
+  int crank = 0;
+  if (cl > 1) {
+    crank = static_cast<int>(cluster_ctarank());
+    const long long crb = cta / cl;
+    begin = crb * KS + static_cast<long long>(KS) * crank / cl;
+    end = crb * KS + static_cast<long long>(KS) * (crank + 1) / cl;
+    cluster_sync_all();  // every rank's barriers are initialised before any remote arrival
+  } else {
+    begin = U * cta / P;
+    end = U * (cta + 1) / P;
+  }
   Visit vs;
   vs.KS = KS;
   vs.nunits = static_cast<int>(end - begin);
@@ -725,8 +754,12 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   // first row block, then the last (either when shared with another CTA).
   int sp[2];
   int nsp = 0;
-  if (is_split(rb0)) sp[nsp++] = rb0;
-  if (rb_last != rb0 && is_split(rb_last)) sp[nsp++] = rb_last;
+  if (cl > 1) {
+    sp[nsp++] = rb0;  // the cluster's one row block
+  } else {
+    if (is_split(rb0)) sp[nsp++] = rb0;
+    if (rb_last != rb0 && is_split(rb_last)) sp[nsp++] = rb_last;
+  }
 
   // The roles wait for the previous grid before any bounded wait whose end
   // depends on it, so that no clock starts while a slow predecessor is still
@@ -903,7 +936,43 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
     // and, once the other's partial is out, copies it into the free split
     // slot; the end of the row block is then an add and the stores.  (When
     // the poll finds nothing by then, the general way applies.)
-    {
+    if (cl > 1) {
+      // Cluster mode: rank r > 0 stores its sums into rank 0's shared memory
+      // (slot r - 1) and every lane arrives on rank 0's barrier (release,
+      // cluster scope); rank 0 adds the ranks' sums to 0 in rank order.
+      const float* mine = reinterpret_cast<const float*>(smem + C::kSplitOff);
+      const int n = sp[0] * kRows + 4 * lane;
+      if (__all_sync(0xffffffffu, mbar_wait(&pub[0], 0, err))) {
+        if constexpr (C::kCluster) {
+          const float* buf = reinterpret_cast<const float*>(smem + C::kClOff);
+          if (crank != 0) {
+            const uint32_t dst = mapa_shared(
+                smem_addr(smem + C::kClOff) + static_cast<uint32_t>((crank - 1) * TT * kRows * 4), 0);
+            for (int t = 0; t < Tt; ++t)
+              st_cluster_v4(dst + static_cast<uint32_t>((t * kRows + 4 * lane) * 4),
+                            *reinterpret_cast<const float4*>(mine + t * kRows + 4 * lane));
+            mbar_arrive_remote(mapa_shared(smem_addr(cfull), 0));
+          } else if (__all_sync(0xffffffffu, mbar_wait_cluster(cfull, 0, err))) {
+            for (int t = 0; t < Tt; ++t) {
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int rk = 0; rk < cl; ++rk) {
+                const float* src = rk == 0 ? mine : buf + (rk - 1) * TT * kRows;
+                const float4 v = *reinterpret_cast<const float4*>(src + t * kRows + 4 * lane);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+              }
+              const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+              float* yr = y + static_cast<size_t>(tok0 + t) * N + n;
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (n + e < N) yr[e] = a[e];
+            }
+          }
+        }
+      }
+    } else {
       auto first_rb = [&](int c) { return static_cast<int>(U * c / P / KS); };
       float* split_sums = reinterpret_cast<float*>(smem + C::kSplitOff);
       for (int i = 0; i < nsp; ++i) {
@@ -1462,6 +1531,8 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no CTA of a cluster leaves while another may still write its shared memory
+  if (cl > 1) cluster_sync_all();
   if (warp == kMmaWarp) tmem_dealloc(tbase, C::kTmemCols);
 }
 
@@ -1486,11 +1557,49 @@ cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block, 
 }
 
 // Grid of the small-T kernel for (K, N): units U, CTAs P, stages KS.
+// Most clusters of c CTAs of smallt_kernel<TT> that can be resident at once
+// (cached per tile and size; 0 when the query fails).
+template <int TT>
+int max_active_clusters(int c) {
+  static int cache[kMaxCl + 1] = {-1, -1, -1, -1, -1};
+  if (cache[c] >= 0) return cache[c];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(c));
+  cfg.blockDim = dim3(TC<TT>::kThreads);
+  cfg.dynamicSmemBytes = TC<TT>::kAllocMax;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, smallt_kernel<TT>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[c] = n;
+  return n;
+}
+
+int max_active_clusters_tt(int tt, int c) {
+  switch (tt) {
+    case 1: return max_active_clusters<1>(c);
+    default: return 0;
+  }
+}
+
 struct SmallTGrid {
   int KS;
   long long U, P;
+  int cl;  // CTAs per row block in cluster mode, else 1
 };
-SmallTGrid smallt_grid(int K, int N, int num_sms) {
+// Grid of the small-T kernel for tile tt: units U, CTAs P, stages KS.  A
+// layer with few row blocks (each to be shared by several CTAs anyway) runs
+// in cluster mode when it fits: one cluster of cl CTAs per row block, all
+// clusters resident at once, so the row block's sums meet in shared memory.
+SmallTGrid smallt_grid(int K, int N, int num_sms, int tt) {
   SmallTGrid g;
   g.KS = (K + kSTStageK - 1) / kSTStageK;
   const long long NB = (N + kRows - 1) / kRows;
@@ -1499,13 +1608,31 @@ SmallTGrid smallt_grid(int K, int N, int num_sms) {
   if (P > kSmallTMaxCtas) P = kSmallTMaxCtas;
   if (P > g.U) P = g.U;
   g.P = P;
+  g.cl = 1;
+  // (one-token tile only: at T = 4 the smaller grid cost more than the
+  // on-chip sums saved)
+  if (tt == 1 && g.KS >= 2 && 2 * NB <= P) {
+    long long c = P / NB;
+    if (c > kMaxCl) c = kMaxCl;
+    if (c > g.KS) c = g.KS;
+    while (c >= 2 && max_active_clusters_tt(tt, static_cast<int>(c)) < NB) --c;
+    if (c >= 2) {
+      g.cl = static_cast<int>(c);
+      g.P = NB * c;
+    }
+  }
   return g;
+}
+
+// Units of the CTA with the most.
+long long max_units_per_cta(const SmallTGrid& g) {
+  return g.cl > 1 ? (g.KS + g.cl - 1) / g.cl : (g.U + g.P - 1) / g.P;
 }
 
 // Resident activation slots of the one-token kernel: the distinct stages a CTA
 // visits at most.
 int t1_slots(const SmallTGrid& g) {
-  const long long per = (g.U + g.P - 1) / g.P;
+  const long long per = max_units_per_cta(g);
   return static_cast<int>(per < g.KS ? per : g.KS);
 }
 
@@ -1516,7 +1643,7 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
                       int* launches) {
   const bool rotate = act == kActRotated;
   using C = TC<TT>;
-  const SmallTGrid g = smallt_grid(K, N, num_sms);
+  const SmallTGrid g = smallt_grid(K, N, num_sms, TT);
   const int nslots = C::kInKernelX ? t1_slots(g) : 0;
   if (nslots > kSmallTX1MaxSlots) return cudaErrorInvalidValue;
   float* partials = reinterpret_cast<float*>(work);
@@ -1527,7 +1654,7 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
   // in every CTA from x; with more, x is better read once by the prep kernel
   // (an L2 hit for the main kernel, whose own reads of x would queue behind
   // its weight stream).
-  const int build_x = C::kInKernelX && act == kActExact && (g.U + g.P - 1) / g.P <= 2 ? 1 : 0;
+  const int build_x = C::kInKernelX && act == kActExact && max_units_per_cta(g) <= 2 ? 1 : 0;
   cudaLaunchAttribute attr[1];
   if (act == kActInt8) {
     // one 4-warp CTA per (token slot, stage)
@@ -1554,12 +1681,20 @@ cudaError_t launch_tt(const CUtensorMap* tmW, const uint32_t* Wp, const uint16_t
     if (e != cudaSuccess) return e;
     ++*launches;
   }
-  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(static_cast<unsigned>(g.P)), dim3(C::kThreads),
+  cudaLaunchAttribute mattr[2];
+  cudaLaunchConfig_t cfg = pdl_config(mattr, dim3(static_cast<unsigned>(g.P)), dim3(C::kThreads),
                                       C::smem_bytes(nslots), stream);
+  if (g.cl > 1) {
+    mattr[1].id = cudaLaunchAttributeClusterDimension;
+    mattr[1].val.clusterDim.x = static_cast<unsigned>(g.cl);
+    mattr[1].val.clusterDim.y = 1;
+    mattr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, smallt_kernel<TT>, *tmW, Wp, scales, x,
                          static_cast<const uint8_t*>(xprep), y, sync, partials, K, N, tok0, Tt,
-                         g.KS, nslots, g.U, build_x, err);
+                         g.KS, nslots, g.U, build_x, g.cl, err);
   if (e == cudaSuccess) ++*launches;
   return e;
 }
@@ -1585,7 +1720,7 @@ size_t smallt_work_bytes(int tt, int K) {
 int smallt_rows(int) { return kRows; }
 
 int smallt_gemv_tile(int K, int N, int num_sms) {
-  return t1_slots(smallt_grid(K, N, num_sms)) <= kSmallTX1MaxSlots ? 1 : 4;
+  return t1_slots(smallt_grid(K, N, num_sms, 1)) <= kSmallTX1MaxSlots ? 1 : 4;
 }
 
 cudaError_t smallt_set_attributes() {

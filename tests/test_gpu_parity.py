@@ -614,7 +614,8 @@ torch.cuda.synchronize()
 
 @pytest.mark.parametrize("K,N,T,rung,expect", [
     (5120, 34816, 1, "gemv", 2),     # nine units per CTA: prep kernel + main kernel
-    (5120, 6144, 1, "gemv", 1),      # two units per CTA: the main kernel builds x itself
+    (1024, 34816, 1, "gemv", 1),     # two units per CTA: the main kernel builds x itself
+    (17408, 5120, 1, "gemv", 2),     # cluster mode (few row blocks): prep kernel + main kernel
     (5120, 34816, 4, "small_t", 2),
     (5120, 6144, 20, "small_t_tiled", 4),   # two token tiles (16 + 4)
     (5120, 6144, 37, "s8", 2),
