@@ -138,6 +138,11 @@ constexpr int kX1Stage = 2 * kX1Sbo;                    // bytes per stage block
 constexpr int kX1Slot = kX1Stage + (kSTStageK / 128) * 8;
 static_assert(kX1Sbo >= kSTStageK / 16 * 32 + 7 * 16, "the junk columns' overrun stays inside");
 
+// Tiles that run in cluster mode (the one-token tile: at T = 4 and 16 the
+// smaller, cluster-scheduled grid cost the down projection more than the
+// on-chip sums saved).
+constexpr bool cluster_tile(int tt) { return tt == 1; }
+
 // Largest cluster of CTAs sharing one row block (cluster mode, T = 1).
 constexpr int kMaxCl = 4;
 
@@ -208,7 +213,7 @@ struct TC {
   static constexpr int kDefOff = kLxOff + kFoldWarps * 256;
   // cluster mode (TT = 1): the other ranks' partial sums of the row block,
   // written into rank 0's shared memory [kMaxCl - 1][TT][128]
-  static constexpr bool kCluster = TT == 1;
+  static constexpr bool kCluster = cluster_tile(TT);
   static constexpr int kClOff = kDefOff + kFoldWarps * kDefer * 8;
   static constexpr int kX1Off =
       (kClOff + (kCluster ? (kMaxCl - 1) * TT * kRows * 4 : 0) + 127) / 128 * 128;  // (T = 1)
@@ -878,10 +883,21 @@ __global__ void __launch_bounds__(TC<TT>::kThreads, 1)
       cw.next(vs);
     }
     const int su_early = su;
-    grid_dependency_wait();
     // (T = 1) the resident activation slots, in visiting order, unless the
     // fold warps build them
     const int nq = nunits < KS ? nunits : KS;
+    if constexpr (C::kInKernelX) {
+      // The fold warps read the stages' x right after the previous grid ends:
+      // warm L2 with it first (a prefetch only moves lines into L2, so it is
+      // harmless while an earlier kernel may still write x).
+      if (build_x && lane < nq) {
+        const int ks = new_stage(vs, lane);
+        const int kk = K - ks * kSTStageK < kSTStageK ? K - ks * kSTStageK : kSTStageK;
+        bulk_prefetch_l2(x + static_cast<size_t>(tok0) * K + static_cast<size_t>(ks) * kSTStageK,
+                    static_cast<uint32_t>(kk) * 2u);
+      }
+    }
+    grid_dependency_wait();
     if constexpr (C::kInKernelX) {
       if (!build_x && lane == 0)
         for (int q = 0; q < nq; ++q) {
@@ -1609,9 +1625,7 @@ SmallTGrid smallt_grid(int K, int N, int num_sms, int tt) {
   if (P > g.U) P = g.U;
   g.P = P;
   g.cl = 1;
-  // (one-token tile only: at T = 4 the smaller grid cost more than the
-  // on-chip sums saved)
-  if (tt == 1 && g.KS >= 2 && 2 * NB <= P) {
+  if (cluster_tile(tt) && g.KS >= 2 && 2 * NB <= P) {
     long long c = P / NB;
     if (c > kMaxCl) c = kMaxCl;
     if (c > g.KS) c = g.KS;
