@@ -429,14 +429,15 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       rc = make_map_u8(&tmW, Wpacked, static_cast<uint64_t>(K) / 4, static_cast<uint64_t>(N),
                        static_cast<uint64_t>(K) / 4, 32, kS8TileN, CU_TENSOR_MAP_SWIZZLE_NONE);
       if (rc != TERN_OK) return rc;
+      const uint32_t tok = static_cast<uint32_t>(s8_token_tile(T));
       rc = make_map_u8(&tmP1, p1, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
-                       static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
+                       static_cast<uint64_t>(K), 128, tok, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != TERN_OK) return rc;
       rc = make_map_u8(&tmP2, p2, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
-                       static_cast<uint64_t>(K), 128, kS8TileT, CU_TENSOR_MAP_SWIZZLE_128B);
+                       static_cast<uint64_t>(K), 128, tok, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != TERN_OK) return rc;
       CUtensorMap tmY;
-      const bool y_tma = (N % 4) == 0;
+      const bool y_tma = (N % 4) == 0 && tok == kS8TileT;
       if (y_tma) {
         rc = make_map_f32(&tmY, y, static_cast<uint64_t>(N), static_cast<uint64_t>(T),
                           static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);

@@ -53,10 +53,14 @@ cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
 // s8 rung: tiles of 128 weight rows x 128 tokens on tcgen05.
 constexpr int kS8TileN = 128;
 constexpr int kS8TileT = 128;
+constexpr int kS8SmallTileT = 32;  // token tile of the s8 rung for T <= 32
 constexpr int kS8FoldWarps = 8;                          // warps folding the accumulators
 constexpr int kS8YBoxT = kS8TileT * 4 / kS8FoldWarps;   // tokens per fold warp's output box
 size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
+// Token tile the s8 rung uses for T tokens (the pieces' tensor maps' box
+// height): kS8SmallTileT for T <= kS8SmallTileT, else kS8TileT.
+int s8_token_tile(int T);
 
 // bf16 rung: x reordered for the MMA (xp [T][K] bf16, optionally rotated
 // first), then tiles of 128 weight rows x 128 tokens on tcgen05 kind::f16.

@@ -41,13 +41,9 @@ namespace tern {
 namespace {
 
 constexpr int kRowsS = 128;   // weight rows per tile
-constexpr int kTokS = 128;    // tokens per tile
-constexpr int kStagesS = 4;   // stage ring (each stage has an A slot of 32 TMEM columns)
-constexpr int kNDS = 3;       // D slots (128 columns)
+constexpr int kNDS = 3;       // D slots
 constexpr int kDecW = 4;
 constexpr int kFoldW = kS8FoldWarps;
-constexpr int kFC = kS8YBoxT;  // tokens (D columns) per fold warp
-static_assert(kFoldW % 4 == 0 && kFC % 32 == 0 && kFC * (kFoldW / 4) == kTokS, "fold split");
 constexpr int kProdW = kDecW + kFoldW;
 constexpr int kMmaW = kProdW + 1;  // first of kMmaWarps issuers
 // The issuing thread runs in step with the tensor pipe (an MMA issues about
@@ -61,23 +57,37 @@ constexpr int kThreadsS = (kMmaW + kMmaWarps) * 32;
 // kMmaWarps <= kNDS.
 static_assert(kMmaWarps <= kNDS, "issuers may outrun the accumulator ring's parity check");
 
+// Layout for a token tile of TOK tokens (MMA N): 128, or 32 for T <= 32.  A
+// 32-token tile does a quarter of the MMA and fold work per weight byte, so
+// the call is bound by the weight bytes in flight: it gets a ring of 12
+// stages (each stage has an A slot of 32 TMEM columns) where the 128-token
+// tile has 4.
+template <int TOK>
 struct SL {
-  static constexpr int kPB = kTokS * 128;   // one piece block of a group (16 KB)
-  static constexpr int kWB = kRowsS * 32;   // packed weights of a group (4 KB)
-  static constexpr int kP1Off = 0;          // 1024-aligned (128-byte swizzle atoms)
-  static constexpr int kP2Off = kP1Off + kStagesS * kPB;
-  static constexpr int kWOff = kP2Off + kStagesS * kPB;
+  static constexpr int kStages = TOK == 32 ? 12 : 4;
+  static constexpr int kFC = TOK * 4 / kFoldW;  // tokens (D columns) per fold warp
+  static_assert(kFoldW % 4 == 0 && kFC % 16 == 0, "fold split");
+  // y through TMA stores of one box per fold warp (the y map's box is
+  // kS8YBoxT tokens); the 32-token tile stores y directly
+  static constexpr bool kYTma = TOK == kS8TileT;
+  static_assert(!kYTma || kFC == kS8YBoxT, "the y map's box");
+  static constexpr int kPB = TOK * 128;   // one piece block of a group
+  static constexpr int kWB = kRowsS * 32;  // packed weights of a group (4 KB)
+  static constexpr int kP1Off = 0;         // 1024-aligned (128-byte swizzle atoms)
+  static constexpr int kP2Off = kP1Off + kStages * kPB;
+  static constexpr int kWOff = kP2Off + kStages * kPB;
   static constexpr int kYB = kFC * 32 * 4;  // one fold warp's output block (kFC tokens x 32 rows)
-  static constexpr int kYOff = kWOff + kStagesS * kWB;
-  static constexpr int kXsOff = kYOff + kFoldW * kYB;  // x_scale of 2 tiles
-  static constexpr int kBarOff = kXsOff + 2 * kTokS * 4;
-  static constexpr int kNumBars = 3 * kStagesS + 2 * kNDS + 4 + kMmaWarps;
+  static constexpr int kYOff = kWOff + kStages * kWB;
+  static constexpr int kXsOff = kYOff + (kYTma ? kFoldW * kYB : 0);  // x_scale of 2 tiles
+  static constexpr int kBarOff = kXsOff + 2 * TOK * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 * kNDS + 4 + kMmaWarps;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kACol = 0;
-  static constexpr uint32_t kDCol = kStagesS * 32;
-  static_assert(kDCol + kNDS * kTokS <= 512, "TMEM budget");
+  static constexpr uint32_t kDCol = kStages * 32;
+  static_assert(kP2Off % 1024 == 0 && kWOff % 1024 == 0 && kXsOff % 16 == 0, "alignment");
+  static_assert(kDCol + kNDS * TOK <= 512, "TMEM budget");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
@@ -89,39 +99,41 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+template <int TOK>
 __global__ void __launch_bounds__(kThreadsS, 1)
     s8tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmP1,
                 const __grid_constant__ CUtensorMap tmP2, const __grid_constant__ CUtensorMap tmY,
                 const uint16_t* __restrict__ scales, const float* __restrict__ x_scale,
                 float* __restrict__ y, int T, int K, int N, int y_tma, int* err) {
+  using L = SL<TOK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   // empty[s]: the stage's weights are decoded and its A slot and pieces are
   // read by the MMAs (the A ring is the stage ring, so a stage refilled by the
   // producer also has a free A slot by the time its copy lands)
-  uint64_t* empty = full + kStagesS;
-  uint64_t* afull = empty + kStagesS;  // A slot written
-  uint64_t* mdone = afull + kStagesS;  // MMAs writing the D slot done
+  uint64_t* empty = full + L::kStages;
+  uint64_t* afull = empty + L::kStages;  // A slot written
+  uint64_t* mdone = afull + L::kStages;  // MMAs writing the D slot done
   uint64_t* dfree = mdone + kNDS;      // D slot read back
   uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
   uint64_t* xsfree = xsfull + 2;       // [2] ... and used
   uint64_t* mfin = xsfree + 2;         // [issuer] all of that issuer's MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kTmemSlot);
-  const float* xs_tile = reinterpret_cast<const float*>(smem + SL::kXsOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  const float* xs_tile = reinterpret_cast<const float*>(smem + L::kXsOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = K >> 7;
   const int RB = (N + kRowsS - 1) / kRowsS;
-  const int TB = (T + kTokS - 1) / kTokS;
+  const int TB = (T + TOK - 1) / TOK;
   const int tiles = RB * TB;
   const int ntiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   const int units = ntiles * G;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesS; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecW + 1);
       mbar_init(&afull[s], kDecW);
@@ -161,28 +173,28 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         // workspace rounds the x_scale array up to 256 bytes)
         const int xb = m & 1;
         if (m >= 2 && !mbar_wait(&xsfree[xb], ((m >> 1) & 1) ^ 1, err)) break;
-        const int cnt = T - tb * kTokS < kTokS ? T - tb * kTokS : kTokS;
+        const int cnt = T - tb * TOK < TOK ? T - tb * TOK : TOK;
         const uint32_t bytes = static_cast<uint32_t>((cnt * 4 + 15) & ~15);
         mbar_arrive_expect_tx(&xsfull[xb], bytes);
-        bulk_load(smem + SL::kXsOff + xb * kTokS * 4, x_scale + tb * kTokS, bytes, &xsfull[xb]);
+        bulk_load(smem + L::kXsOff + xb * TOK * 4, x_scale + tb * TOK, bytes, &xsfull[xb]);
         for (int g = 0; g < G; ++g, ++u) {
-          if (u >= kStagesS && !mbar_wait(&empty[s], ph ^ 1, err)) {
+          if (u >= L::kStages && !mbar_wait(&empty[s], ph ^ 1, err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], SL::kWB + 2 * SL::kPB);
-          tma_load_2d(smem + SL::kWOff + s * SL::kWB, &tmW, g * 32, rb * kRowsS, &full[s]);
-          tma_load_2d(smem + SL::kP1Off + s * SL::kPB, &tmP1, g * 128, tb * kTokS, &full[s]);
-          tma_load_2d(smem + SL::kP2Off + s * SL::kPB, &tmP2, g * 128, tb * kTokS, &full[s]);
-          if (++s == kStagesS) {
+          mbar_arrive_expect_tx(&full[s], L::kWB + 2 * L::kPB);
+          tma_load_2d(smem + L::kWOff + s * L::kWB, &tmW, g * 32, rb * kRowsS, &full[s]);
+          tma_load_2d(smem + L::kP1Off + s * L::kPB, &tmP1, g * 128, tb * TOK, &full[s]);
+          tma_load_2d(smem + L::kP2Off + s * L::kPB, &tmP2, g * 128, tb * TOK, &full[s]);
+          if (++s == L::kStages) {
             s = 0;
             ph ^= 1;
           }
         }
       }
       // no copy of this CTA may still be in flight when it exits
-      for (int v = (u > kStagesS ? u - kStagesS : 0); v < u; ++v)
-        if (!mbar_wait(&full[v % kStagesS], (v / kStagesS) & 1, err)) break;
+      for (int v = (u > L::kStages ? u - L::kStages : 0); v < u; ++v)
+        if (!mbar_wait(&full[v % L::kStages], (v / L::kStages) & 1, err)) break;
       for (int m = (ntiles > 2 ? ntiles - 2 : 0); m < ntiles; ++m)
         if (!mbar_wait(&xsfull[m & 1], (m >> 1) & 1, err)) break;
     }
@@ -199,7 +211,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       // also frees the slot
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, err))) break;
       tc_fence_after();
-      const uint8_t* wrow = smem + SL::kWOff + s * SL::kWB + r * 32;
+      const uint8_t* wrow = smem + L::kWOff + s * L::kWB + r * 32;
       const uint4 c0 = lds_v4(wrow);
       const uint4 c1 = lds_v4(wrow + 16);
       const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         av[4 * j + 2] = decode_e4m3<2>(w[j]);
         av[4 * j + 3] = decode_e4m3<3>(w[j]);
       }
-      tmem_st32(tbase + lane_off + SL::kACol + s * 32, av);
+      tmem_st32(tbase + lane_off + L::kACol + s * 32, av);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -219,7 +231,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         mbar_arrive(&afull[s]);
         mbar_arrive(&empty[s]);
       }
-      if (++s == kStagesS) {
+      if (++s == L::kStages) {
         s = 0;
         ph ^= 1;
       }
@@ -229,25 +241,25 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // one thread per issuer warp, groups u = w, w + kMmaWarps, ...; no warp
     // votes, two commits per group
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, kTokS);
-      const uint64_t desc1 = smem_desc_sw128(smem_addr(smem + SL::kP1Off));
-      const uint64_t desc2 = smem_desc_sw128(smem_addr(smem + SL::kP2Off));
+      constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, TOK);
+      const uint64_t desc1 = smem_desc_sw128(smem_addr(smem + L::kP1Off));
+      const uint64_t desc2 = smem_desc_sw128(smem_addr(smem + L::kP2Off));
       int u = warp - kMmaW;
       for (; u < units; u += kMmaWarps) {
-        const int s = u % kStagesS, d = u % kNDS;
-        const uint32_t ph = (u / kStagesS) & 1, dph = (u / kNDS) & 1;
+        const int s = u % L::kStages, d = u % kNDS;
+        const uint32_t ph = (u / L::kStages) & 1, dph = (u / kNDS) & 1;
         if (!mbar_wait(&afull[s], ph, err)) break;
         // the pieces landed (implied by afull; waited on here as well so the
         // tensor core's reads are ordered after the copy for this thread)
         if (!mbar_wait(&full[s], ph, err)) break;
         if (u >= kNDS && !mbar_wait(&dfree[d], dph ^ 1, err)) break;
         tc_fence_after();
-        const uint32_t dcol = tbase + SL::kDCol + d * kTokS;
-        const uint32_t acol = tbase + SL::kACol + s * 32;
+        const uint32_t dcol = tbase + L::kDCol + d * TOK;
+        const uint32_t acol = tbase + L::kACol + s * 32;
         // descriptor start addresses advance in 16-byte units: a stage is
         // kPB bytes, a K = 32 step 32 bytes inside the swizzle atom
-        const uint64_t b1 = desc1 + static_cast<uint64_t>((s * SL::kPB) >> 4);
-        const uint64_t b2 = desc2 + static_cast<uint64_t>((s * SL::kPB) >> 4);
+        const uint64_t b1 = desc1 + static_cast<uint64_t>((s * L::kPB) >> 4);
+        const uint64_t b2 = desc2 + static_cast<uint64_t>((s * L::kPB) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_f8f6f4_ts(dcol, acol + kk * 8, b1 + 2 * kk, idesc, kk != 0);
@@ -269,9 +281,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     const int hc = (warp - kDecW) >> 2;     // token block of the tile
     const int r = fq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(fq * 32) << 16;
-    float acc[kFC];
+    float acc[L::kFC];
 #pragma unroll
-    for (int j = 0; j < kFC; ++j) acc[j] = 0.f;
+    for (int j = 0; j < L::kFC; ++j) acc[j] = 0.f;
     int d = 0;
     uint32_t dph = 0;
     bool ok = true;
@@ -289,22 +301,26 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           break;
         }
         tc_fence_after();
-        // 32 columns at a time: load, wait, fold (the slot is released after
-        // the last load has completed)
-        const uint32_t col = tbase + lane_off + SL::kDCol + d * kTokS + hc * kFC;
+        // kCh columns at a time: load, wait, fold (the slot is released
+        // after the last load has completed)
+        constexpr int kCh = L::kFC >= 32 ? 32 : L::kFC;
+        const uint32_t col = tbase + lane_off + L::kDCol + d * TOK + hc * L::kFC;
 #pragma unroll
-        for (int c = 0; c < kFC / 32; ++c) {
-          uint32_t dv[32];
-          tmem_ld32(col + 32 * c, dv);
+        for (int c = 0; c < L::kFC / kCh; ++c) {
+          uint32_t dv[kCh];
+          if constexpr (kCh == 32)
+            tmem_ld32(col + 32 * c, dv);
+          else
+            tmem_ld16(col + 16 * c, dv);
           tmem_wait_ld();
-          if (c == kFC / 32 - 1) {
+          if (c == L::kFC / kCh - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&dfree[d]);
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            acc[32 * c + j] = fmaf(sg, __uint_as_float(dv[j]), acc[32 * c + j]);
+          for (int j = 0; j < kCh; ++j)
+            acc[kCh * c + j] = fmaf(sg, __uint_as_float(dv[j]), acc[kCh * c + j]);
         }
         if (++d == kNDS) {
           d = 0;
@@ -315,16 +331,16 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       // end of the tile: y[t][n] = xs[t] * acc
       const int xb = m & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&xsfull[xb], (m >> 1) & 1, err))) break;
-      const float* xst = xs_tile + xb * kTokS + hc * kFC;
-      const int t0 = tb * kTokS + hc * kFC;
-      if (y_tma) {
-        // stage the warp's kFC x 32 block and store it asynchronously: the
+      const float* xst = xs_tile + xb * TOK + hc * L::kFC;
+      const int t0 = tb * TOK + hc * L::kFC;
+      if (L::kYTma && y_tma) {
+        // stage the warp's L::kFC x 32 block and store it asynchronously: the
         // next tile's groups overlap the write-back
-        float* stg = reinterpret_cast<float*>(smem + SL::kYOff + (warp - kDecW) * SL::kYB);
+        float* stg = reinterpret_cast<float*>(smem + L::kYOff + (warp - kDecW) * L::kYB);
         if (lane == 0) bulk_wait_group_read0();  // the warp's previous block was read out
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < kFC; ++j) {
+        for (int j = 0; j < L::kFC; ++j) {
           stg[j * 32 + lane] = xst[j] * acc[j];
           acc[j] = 0.f;
         }
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < kFC; ++j) {
+        for (int j = 0; j < L::kFC; ++j) {
           const int t = t0 + j;
           if (n < N && t < T) y[static_cast<size_t>(t) * N + n] = xst[j] * acc[j];
           acc[j] = 0.f;
@@ -357,24 +373,35 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 
 }  // namespace
 
-size_t s8_smem_bytes() { return SL::kAlloc; }
+size_t s8_smem_bytes() { return SL<kS8TileT>::kAlloc; }
 
 cudaError_t s8_set_attributes() {
-  return cudaFuncSetAttribute(s8tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SL::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(s8tc_kernel<kS8TileT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SL<kS8TileT>::kAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(s8tc_kernel<kS8SmallTileT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SL<kS8SmallTileT>::kAlloc);
 }
+
+int s8_token_tile(int T) { return T <= kS8SmallTileT ? kS8SmallTileT : kS8TileT; }
 
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
                       const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
                       float* y, int T, int K, int N, int num_sms, int* err, cudaStream_t stream) {
-  const long long tiles = static_cast<long long>((N + kRowsS - 1) / kRowsS) *
-                          ((T + kTokS - 1) / kTokS);
+  const int tok = s8_token_tile(T);
+  const long long tiles = static_cast<long long>((N + kRowsS - 1) / kRowsS) * ((T + tok - 1) / tok);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  // without a y tensor map (N % 4 != 0: rows not 16-byte strided) the fold
-  // warps store y directly; the map argument is then an unused copy
-  s8tc_kernel<<<grid, kThreadsS, SL::kAlloc, stream>>>(*tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW,
-                                                       scales, x_scale, y, T, K, N,
-                                                       tmY ? 1 : 0, err);
+  // without a y tensor map (N % 4 != 0: rows not 16-byte strided; or the
+  // 32-token tile) the fold warps store y directly; the map argument is then
+  // an unused copy
+  if (tok == kS8SmallTileT)
+    s8tc_kernel<kS8SmallTileT><<<grid, kThreadsS, SL<kS8SmallTileT>::kAlloc, stream>>>(
+        *tmW, *tmP1, *tmP2, *tmW, scales, x_scale, y, T, K, N, 0, err);
+  else
+    s8tc_kernel<kS8TileT><<<grid, kThreadsS, SL<kS8TileT>::kAlloc, stream>>>(
+        *tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW, scales, x_scale, y, T, K, N, tmY ? 1 : 0, err);
   return cudaGetLastError();
 }
 
