@@ -225,9 +225,16 @@ def test_shapes_bf16(tl, K, N):
         _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T))
 
 
-@pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 520, 200), (2048, 300, 129)])
+@pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 520, 200), (2048, 300, 129),
+                                   (1024, 77, 32), (3072, 1001, 31)])
 def test_shapes_s8(tl, K, N, T):
     _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T))
+
+
+@pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 521, 200), (2048, 300, 129)])
+def test_shapes_bf16_rung(tl, K, N, T):
+    # the exact bf16 prefill rung on ragged shapes (N % 4 != 0: y stored directly)
+    assert _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T + 1), "bf16") == "bf16"
 
 
 # ---------------------------------------------------------------- degenerate inputs
@@ -421,7 +428,8 @@ def test_split_row_blocks_are_deterministic(tl):
     """Row blocks split between CTAs are reduced in CTA order: repeated calls
     give identical bits."""
     import torch
-    for proj, T in (("dn", 1), ("gu", 1), ("dn", 4), ("ao", 12)):
+    # (the T = 1 down and attention-sized layers run in cluster mode)
+    for proj, T in (("dn", 1), ("gu", 1), ("ai", 1), ("ao", 1), ("dn", 4), ("ao", 12)):
         c = synth.case(proj, T, seed=51)
         W, s, x = to_device(c)
         Wp = tl.tern_pack(W)

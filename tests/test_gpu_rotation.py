@@ -85,7 +85,8 @@ def _integer_case(T, K, N, seed):
 
 
 CASES = [("gemv", 1, 2048, 1000), ("gemv", 1, 5120, 4200), ("small_t", 5, 3072, 777),
-         ("small_t_tiled", 13, 2048, 1300), ("s8", 37, 5120, 640)]
+         ("small_t_tiled", 13, 2048, 1300), ("s8", 37, 5120, 640), ("s8", 20, 2048, 300),
+         ("bf16", 37, 5120, 640)]
 
 
 @pytest.mark.parametrize("rung,T,K,N", CASES)
