@@ -200,9 +200,11 @@ int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // s8 scratch: the two fp8 pieces [T][K] each, then x_scale [T] (rounded up to
-// 256 bytes, so the kernel may read it in whole 16-byte chunks).
+// 256 bytes, so the kernel may read it in whole 16-byte chunks), then the
+// partial sums of the chunked last wave.
 size_t s8_workspace_bytes(int T, int K) {
-  return 2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256);
+  return 2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256) +
+         kS8PartialBytes;
 }
 
 // K for which the activations can be staged rotated (whole 1024-wide
@@ -417,7 +419,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
                        small_t_act(c), st, &launches);
       break;
     case TERN_RUNG_S8: {
-      // after the sync area, which the s8 rung leaves untouched
+      // after the sync area (whose tickets the chunked last wave uses)
       uint8_t* scratch = static_cast<uint8_t*>(workspace) + kSyncBytes;
       const size_t piece = align_up(static_cast<size_t>(T) * K, 256);
       uint8_t* p1 = scratch;
@@ -443,8 +445,10 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
                           static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);
         if (rc != TERN_OK) return rc;
       }
-      rc = launch_s8(&tmW, &tmP1, &tmP2, y_tma ? &tmY : nullptr, scales, xs, y, T, K, N, d->sms,
-                     d->err, st) == cudaSuccess
+      float* partials = reinterpret_cast<float*>(scratch + 2 * piece +
+                                                 align_up(sizeof(float) * T, 256));
+      rc = launch_s8(&tmW, &tmP1, &tmP2, y_tma ? &tmY : nullptr, scales, xs, y, T, K, N,
+                     static_cast<int*>(workspace), partials, d->sms, d->err, st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
       ++launches;

@@ -54,8 +54,15 @@ cudaError_t launch_smallt(int tt, const CUtensorMap* tmW, const uint32_t* Wp,
 constexpr int kS8TileN = 128;
 constexpr int kS8TileT = 128;
 constexpr int kS8SmallTileT = 32;  // token tile of the s8 rung for T <= 32
+// Chunked last wave of the s8 rung: at most this many group ranges per tile;
+// the chunks' partial sums take kS8PartialBytes of workspace after the
+// pieces, and their tickets the synchronisation area.
 constexpr int kS8FoldWarps = 8;                          // warps folding the accumulators
 constexpr int kS8YBoxT = kS8TileT * 4 / kS8FoldWarps;   // tokens per fold warp's output box
+constexpr int kS8MaxChunks = 4;
+// (at most 160 chunk items, each kS8FoldWarps blocks of kS8YBoxT x 32 floats)
+constexpr size_t kS8PartialBytes =
+    static_cast<size_t>(160) * kS8FoldWarps * kS8YBoxT * 32 * sizeof(float);
 size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
 // Token tile the s8 rung uses for T tokens (the pieces' tensor maps' box
@@ -79,7 +86,8 @@ cudaError_t bf16_set_attributes();
 // rounded up to 4.
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
                       const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
-                      float* y, int T, int K, int N, int num_sms, int* err, cudaStream_t stream);
+                      float* y, int T, int K, int N, int* tickets, float* partials, int num_sms,
+                      int* err, cudaStream_t stream);
 
 // Pack and quantise.
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,

@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     s8tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmP1,
                 const __grid_constant__ CUtensorMap tmP2, const __grid_constant__ CUtensorMap tmY,
                 const uint16_t* __restrict__ scales, const float* __restrict__ x_scale,
-                float* __restrict__ y, int T, int K, int N, int y_tma, int* err) {
+                float* __restrict__ y, int T, int K, int N, int y_tma, int nfull, int chunks,
+                int* __restrict__ tickets, float* __restrict__ partials, int* err) {
   using L = SL<TOK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -129,8 +130,39 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const int RB = (N + kRowsS - 1) / kRowsS;
   const int TB = (T + TOK - 1) / TOK;
   const int tiles = RB * TB;
-  const int ntiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int units = ntiles * G;
+  // Work items, walked by the persistent CTAs (item blockIdx.x + m gridDim.x):
+  // the first nfull tiles whole, then each remaining tile as `chunks` ranges
+  // of its groups.  A chunked tile's warps publish partial sums and the last
+  // chunk to finish adds them in chunk order (see the fold).
+  const int nitems_all = nfull + (tiles - nfull) * chunks;
+  struct Item {
+    int tile, g0, g1, chunk;  // chunk < 0: the whole tile
+  };
+  auto item_of = [&](int m) -> Item {
+    const int idx = blockIdx.x + m * static_cast<int>(gridDim.x);
+    Item it;
+    if (idx < nfull) {
+      it.tile = idx;
+      it.g0 = 0;
+      it.g1 = G;
+      it.chunk = -1;
+    } else {
+      const int j = idx - nfull;
+      it.tile = nfull + j / chunks;
+      it.chunk = j % chunks;
+      it.g0 = G * it.chunk / chunks;
+      it.g1 = G * (it.chunk + 1) / chunks;
+    }
+    return it;
+  };
+  const int nitems = blockIdx.x < nitems_all
+                         ? (nitems_all - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                         : 0;
+  int units = 0;
+  for (int m = 0; m < nitems; ++m) {
+    const Item it = item_of(m);
+    units += it.g1 - it.g0;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
@@ -166,9 +198,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       int u = 0, s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int m = 0; m < ntiles && ok; ++m) {
-        const int tile = blockIdx.x + m * gridDim.x;
-        const int rb = tile / TB, tb = tile % TB;
+      for (int m = 0; m < nitems && ok; ++m) {
+        const Item itm = item_of(m);
+        const int rb = itm.tile / TB, tb = itm.tile % TB;
         // this tile's x_scale block (padded to whole 16-byte chunks: the
         // workspace rounds the x_scale array up to 256 bytes)
         const int xb = m & 1;
@@ -177,7 +209,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         const uint32_t bytes = static_cast<uint32_t>((cnt * 4 + 15) & ~15);
         mbar_arrive_expect_tx(&xsfull[xb], bytes);
         bulk_load(smem + L::kXsOff + xb * TOK * 4, x_scale + tb * TOK, bytes, &xsfull[xb]);
-        for (int g = 0; g < G; ++g, ++u) {
+        for (int g = itm.g0; g < itm.g1; ++g, ++u) {
           if (u >= L::kStages && !mbar_wait(&empty[s], ph ^ 1, err)) {
             ok = false;
             break;
@@ -195,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       // no copy of this CTA may still be in flight when it exits
       for (int v = (u > L::kStages ? u - L::kStages : 0); v < u; ++v)
         if (!mbar_wait(&full[v % L::kStages], (v / L::kStages) & 1, err)) break;
-      for (int m = (ntiles > 2 ? ntiles - 2 : 0); m < ntiles; ++m)
+      for (int m = (nitems > 2 ? nitems - 2 : 0); m < nitems; ++m)
         if (!mbar_wait(&xsfull[m & 1], (m >> 1) & 1, err)) break;
     }
     __syncwarp();
@@ -287,15 +319,15 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     int d = 0;
     uint32_t dph = 0;
     bool ok = true;
-    for (int m = 0; m < ntiles && ok; ++m) {
-      const int tile = blockIdx.x + m * gridDim.x;
-      const int rb = tile / TB, tb = tile % TB;
+    for (int m = 0; m < nitems && ok; ++m) {
+      const Item itm = item_of(m);
+      const int rb = itm.tile / TB, tb = itm.tile % TB;
       const int n = rb * kRowsS + r;
       const uint16_t* srow = scales + static_cast<size_t>(n < N ? n : 0) * G;
-      float snext = n < N ? __half2float(__ushort_as_half(srow[0])) : 0.f;
-      for (int g = 0; g < G; ++g) {
+      float snext = n < N ? __half2float(__ushort_as_half(srow[itm.g0])) : 0.f;
+      for (int g = itm.g0; g < itm.g1; ++g) {
         const float sg = 8.0f * snext;  // D holds acc / 8
-        if (g + 1 < G) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
+        if (g + 1 < itm.g1) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
         if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], dph, err))) {
           ok = false;
           break;
@@ -333,7 +365,46 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&xsfull[xb], (m >> 1) & 1, err))) break;
       const float* xst = xs_tile + xb * TOK + hc * L::kFC;
       const int t0 = tb * TOK + hc * L::kFC;
-      if (L::kYTma && y_tma) {
+      bool store = true;
+      if (itm.chunk >= 0) {
+        // Chunked tile: publish this warp's partial sums (token-major, one
+        // 32-row column per token), take the (tile, warp) ticket; the last
+        // chunk to arrive adds every chunk's sums in chunk order.
+        const int fw = warp - kDecW;
+        const int ct = itm.tile - nfull;  // the tile's index among the chunked ones
+        auto part = [&](int c) {
+          return partials + (static_cast<size_t>(ct * chunks + c) * kFoldW + fw) * (L::kFC * 32);
+        };
+        float* mine = part(itm.chunk);
+#pragma unroll
+        for (int j = 0; j < L::kFC; ++j) mine[j * 32 + lane] = acc[j];
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0)
+          last = atomic_add_acq_rel_gpu(&tickets[ct * kFoldW + fw], 1) == chunks - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last) {
+          // every chunk's sums from the workspace (this one's too), added to
+          // 0 in chunk order into acc (published above, so free), then
+          // scaled and stored as a whole tile's: one chunk's loads in flight
+          // at a time
+#pragma unroll
+          for (int j = 0; j < L::kFC; ++j) acc[j] = 0.f;
+          for (int c = 0; c < chunks; ++c) {
+            const float* pc = part(c) + lane;
+#pragma unroll
+            for (int j = 0; j < L::kFC; ++j) acc[j] += __ldcg(pc + j * 32);
+          }
+          if (lane == 0) tickets[ct * kFoldW + fw] = 0;  // every chunk has taken it
+        }
+        store = last != 0;
+      }
+      if (!store) {
+#pragma unroll
+        for (int j = 0; j < L::kFC; ++j) acc[j] = 0.f;
+      } else if (L::kYTma && y_tma) {
         // stage the warp's L::kFC x 32 block and store it asynchronously: the
         // next tile's groups overlap the write-back
         float* stg = reinterpret_cast<float*>(smem + L::kYOff + (warp - kDecW) * L::kYB);
@@ -387,21 +458,52 @@ cudaError_t s8_set_attributes() {
 
 int s8_token_tile(int T) { return T <= kS8SmallTileT ? kS8SmallTileT : kS8TileT; }
 
+// Work split of the s8 rung: P CTAs walk nfull whole tiles, then the rest
+// of the tiles as `chunks` group ranges each.  Chunking applies when the
+// rest fills at most half a wave (then a quarter to a third of a tile per
+// CTA finishes the call instead of a whole tile on few SMs).
+struct S8Split {
+  int tok, P, nfull, chunks;
+};
+S8Split s8_split(int T, int K, int N, int num_sms) {
+  S8Split sp;
+  sp.tok = s8_token_tile(T);
+  const int tiles = ((N + kRowsS - 1) / kRowsS) * ((T + sp.tok - 1) / sp.tok);
+  const int G = K / 128;
+  const int rounds = tiles / num_sms;
+  const int rest = tiles - rounds * num_sms;
+  sp.nfull = tiles;
+  sp.chunks = 1;
+  if (rest > 0 && 2 * rest <= num_sms) {
+    int c = num_sms / rest;
+    if (c > kS8MaxChunks) c = kS8MaxChunks;
+    if (c > G / 2) c = G / 2;
+    if (c >= 2) {
+      sp.nfull = rounds * num_sms;
+      sp.chunks = c;
+    }
+  }
+  const int items = sp.nfull + (tiles - sp.nfull) * sp.chunks;
+  sp.P = items < num_sms ? items : num_sms;
+  return sp;
+}
+
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
                       const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
-                      float* y, int T, int K, int N, int num_sms, int* err, cudaStream_t stream) {
-  const int tok = s8_token_tile(T);
-  const long long tiles = static_cast<long long>((N + kRowsS - 1) / kRowsS) * ((T + tok - 1) / tok);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+                      float* y, int T, int K, int N, int* tickets, float* partials, int num_sms,
+                      int* err, cudaStream_t stream) {
+  const S8Split sp = s8_split(T, K, N, num_sms);
   // without a y tensor map (N % 4 != 0: rows not 16-byte strided; or the
   // 32-token tile) the fold warps store y directly; the map argument is then
   // an unused copy
-  if (tok == kS8SmallTileT)
-    s8tc_kernel<kS8SmallTileT><<<grid, kThreadsS, SL<kS8SmallTileT>::kAlloc, stream>>>(
-        *tmW, *tmP1, *tmP2, *tmW, scales, x_scale, y, T, K, N, 0, err);
+  if (sp.tok == kS8SmallTileT)
+    s8tc_kernel<kS8SmallTileT><<<sp.P, kThreadsS, SL<kS8SmallTileT>::kAlloc, stream>>>(
+        *tmW, *tmP1, *tmP2, *tmW, scales, x_scale, y, T, K, N, 0, sp.nfull, sp.chunks, tickets,
+        partials, err);
   else
-    s8tc_kernel<kS8TileT><<<grid, kThreadsS, SL<kS8TileT>::kAlloc, stream>>>(
-        *tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW, scales, x_scale, y, T, K, N, tmY ? 1 : 0, err);
+    s8tc_kernel<kS8TileT><<<sp.P, kThreadsS, SL<kS8TileT>::kAlloc, stream>>>(
+        *tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW, scales, x_scale, y, T, K, N, tmY ? 1 : 0,
+        sp.nfull, sp.chunks, tickets, partials, err);
   return cudaGetLastError();
 }
 
