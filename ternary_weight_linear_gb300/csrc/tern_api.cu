@@ -474,8 +474,12 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
                           static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);
         if (rc != TERN_OK) return rc;
       }
-      rc = launch_bf16(&tmW, &tmX, y_tma ? &tmY : nullptr, scales, y, T, K, N, d->sms, d->err,
-                       st) == cudaSuccess
+      // the chunked last wave's partial sums: where the s8 rung keeps its own
+      float* partials = reinterpret_cast<float*>(
+          static_cast<uint8_t*>(workspace) + kSyncBytes +
+          2 * align_up(static_cast<size_t>(T) * K, 256) + align_up(sizeof(float) * T, 256));
+      rc = launch_bf16(&tmW, &tmX, y_tma ? &tmY : nullptr, scales, y, T, K, N,
+                       static_cast<int*>(workspace), partials, d->sms, d->err, st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
       ++launches;

@@ -115,7 +115,8 @@ __device__ __forceinline__ uint32_t decode_bf16_pair(uint32_t w) {
 __global__ void __launch_bounds__(kThreadsB, 1)
     bf16tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const __grid_constant__ CUtensorMap tmY, const uint16_t* __restrict__ scales,
-                  float* __restrict__ y, int T, int K, int N, int y_tma, int* err) {
+                  float* __restrict__ y, int T, int K, int N, int y_tma, int nfull, int chunks,
+                  int* __restrict__ tickets, float* __restrict__ partials, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -135,8 +136,38 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int RB = (N + kRowsB - 1) / kRowsB;
   const int TB = (T + kTokB - 1) / kTokB;
   const int tiles = RB * TB;
-  const int ntiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int units = ntiles * G;
+  // Work items as in the s8 rung (tile_split): the first nfull tiles whole,
+  // then each remaining tile as `chunks` ranges of its groups, whose partial
+  // sums the last chunk to finish adds in chunk order.
+  const int nitems_all = nfull + (tiles - nfull) * chunks;
+  struct Item {
+    int tile, g0, g1, chunk;  // chunk < 0: the whole tile
+  };
+  auto item_of = [&](int m) -> Item {
+    const int idx = blockIdx.x + m * static_cast<int>(gridDim.x);
+    Item it;
+    if (idx < nfull) {
+      it.tile = idx;
+      it.g0 = 0;
+      it.g1 = G;
+      it.chunk = -1;
+    } else {
+      const int j = idx - nfull;
+      it.tile = nfull + j / chunks;
+      it.chunk = j % chunks;
+      it.g0 = G * it.chunk / chunks;
+      it.g1 = G * (it.chunk + 1) / chunks;
+    }
+    return it;
+  };
+  const int nitems = blockIdx.x < nitems_all
+                         ? (nitems_all - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                         : 0;
+  int units = 0;
+  for (int m = 0; m < nitems; ++m) {
+    const Item it = item_of(m);
+    units += it.g1 - it.g0;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesB; ++s) {
@@ -166,10 +197,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       int u = 0, s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int m = 0; m < ntiles && ok; ++m) {
-        const int tile = blockIdx.x + m * gridDim.x;
-        const int rb = tile / TB, tb = tile % TB;
-        for (int g = 0; g < G; ++g, ++u) {
+      for (int m = 0; m < nitems && ok; ++m) {
+        const Item itm = item_of(m);
+        const int rb = itm.tile / TB, tb = itm.tile % TB;
+        for (int g = itm.g0; g < itm.g1; ++g, ++u) {
           if (u >= kStagesB && !mbar_wait(&empty[s], ph ^ 1, err)) {
             ok = false;
             break;
@@ -281,15 +312,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     int d = 0;
     uint32_t dph = 0;
     bool ok = true;
-    for (int m = 0; m < ntiles && ok; ++m) {
-      const int tile = blockIdx.x + m * gridDim.x;
-      const int rb = tile / TB, tb = tile % TB;
+    for (int m = 0; m < nitems && ok; ++m) {
+      const Item itm = item_of(m);
+      const int rb = itm.tile / TB, tb = itm.tile % TB;
       const int n = rb * kRowsB + r;
       const uint16_t* srow = scales + static_cast<size_t>(n < N ? n : 0) * G;
-      float snext = n < N ? __half2float(__ushort_as_half(srow[0])) : 0.f;
-      for (int g = 0; g < G; ++g) {
+      float snext = n < N ? __half2float(__ushort_as_half(srow[itm.g0])) : 0.f;
+      for (int g = itm.g0; g < itm.g1; ++g) {
         const float sg = snext;
-        if (g + 1 < G) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
+        if (g + 1 < itm.g1) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
         if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], dph, err))) {
           ok = false;
           break;
@@ -317,7 +348,41 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       if (!ok) break;
       const int t0 = tb * kTokB + hc * kFCB;
-      if (y_tma) {
+      bool store = true;
+      if (itm.chunk >= 0) {
+        // chunked tile: publish, take the (tile, warp) ticket, the last adds
+        // every chunk's sums to 0 in chunk order (as in the s8 rung)
+        const int fw = warp - kDecWB;
+        const int ct = itm.tile - nfull;
+        auto part = [&](int c) {
+          return partials + (static_cast<size_t>(ct * chunks + c) * kFoldWB + fw) * (kFCB * 32);
+        };
+        float* mine = part(itm.chunk);
+#pragma unroll
+        for (int j = 0; j < kFCB; ++j) mine[j * 32 + lane] = acc[j];
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0)
+          last = atomic_add_acq_rel_gpu(&tickets[ct * kFoldWB + fw], 1) == chunks - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last) {
+#pragma unroll
+          for (int j = 0; j < kFCB; ++j) acc[j] = 0.f;
+          for (int c = 0; c < chunks; ++c) {
+            const float* pc = part(c) + lane;
+#pragma unroll
+            for (int j = 0; j < kFCB; ++j) acc[j] += __ldcg(pc + j * 32);
+          }
+          if (lane == 0) tickets[ct * kFoldWB + fw] = 0;  // every chunk has taken it
+        }
+        store = last != 0;
+      }
+      if (!store) {
+#pragma unroll
+        for (int j = 0; j < kFCB; ++j) acc[j] = 0.f;
+      } else if (y_tma) {
         // stage the warp's kFCB x 32 block and store it asynchronously: the
         // next tile's groups overlap the write-back
         float* stg = reinterpret_cast<float*>(smem + BL::kYOff + (warp - kDecWB) * BL::kYB);
@@ -446,13 +511,13 @@ cudaError_t launch_interleave(const uint16_t* x, uint16_t* xp, int T, int K, int
 }
 
 cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmY,
-                        const uint16_t* scales, float* y, int T, int K, int N, int num_sms,
-                        int* err, cudaStream_t stream) {
-  const long long tiles = static_cast<long long>((N + kRowsB - 1) / kRowsB) *
-                          ((T + kTokB - 1) / kTokB);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  bf16tc_kernel<<<grid, kThreadsB, BL::kAlloc, stream>>>(*tmW, *tmX, tmY ? *tmY : *tmW, scales, y,
-                                                          T, K, N, tmY ? 1 : 0, err);
+                        const uint16_t* scales, float* y, int T, int K, int N, int* tickets,
+                        float* partials, int num_sms, int* err, cudaStream_t stream) {
+  const int tiles = ((N + kRowsB - 1) / kRowsB) * ((T + kTokB - 1) / kTokB);
+  const TileSplit sp = tile_split(tiles, K / 128, num_sms);
+  bf16tc_kernel<<<sp.P, kThreadsB, BL::kAlloc, stream>>>(*tmW, *tmX, tmY ? *tmY : *tmW, scales, y,
+                                                          T, K, N, tmY ? 1 : 0, sp.nfull, sp.chunks,
+                                                          tickets, partials, err);
   return cudaGetLastError();
 }
 

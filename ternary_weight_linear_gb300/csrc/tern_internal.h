@@ -60,6 +60,33 @@ constexpr int kS8SmallTileT = 32;  // token tile of the s8 rung for T <= 32
 constexpr int kS8FoldWarps = 8;                          // warps folding the accumulators
 constexpr int kS8YBoxT = kS8TileT * 4 / kS8FoldWarps;   // tokens per fold warp's output box
 constexpr int kS8MaxChunks = 4;
+
+// Work split of the prefill rungs (s8, bf16): P CTAs walk nfull whole tiles,
+// then the rest of the tiles as `chunks` group ranges each.  Chunking applies
+// when the rest fills at most half a wave, so that a fraction of a tile per
+// CTA finishes the call instead of a whole tile on few SMs.
+struct TileSplit {
+  int P, nfull, chunks;
+};
+inline TileSplit tile_split(int tiles, int G, int num_sms) {
+  TileSplit sp;
+  const int rounds = tiles / num_sms;
+  const int rest = tiles - rounds * num_sms;
+  sp.nfull = tiles;
+  sp.chunks = 1;
+  if (rest > 0 && 2 * rest <= num_sms) {
+    int c = num_sms / rest;
+    if (c > kS8MaxChunks) c = kS8MaxChunks;
+    if (c > G / 2) c = G / 2;
+    if (c >= 2) {
+      sp.nfull = rounds * num_sms;
+      sp.chunks = c;
+    }
+  }
+  const int items = sp.nfull + (tiles - sp.nfull) * sp.chunks;
+  sp.P = items < num_sms ? items : num_sms;
+  return sp;
+}
 // (at most 160 chunk items, each kS8FoldWarps blocks of kS8YBoxT x 32 floats)
 constexpr size_t kS8PartialBytes =
     static_cast<size_t>(160) * kS8FoldWarps * kS8YBoxT * 32 * sizeof(float);
@@ -76,8 +103,8 @@ int s8_token_tile(int T);
 cudaError_t launch_interleave(const uint16_t* x, uint16_t* xp, int T, int K, int rotate,
                               int num_sms, cudaStream_t stream);
 cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmY,
-                        const uint16_t* scales, float* y, int T, int K, int N, int num_sms,
-                        int* err, cudaStream_t stream);
+                        const uint16_t* scales, float* y, int T, int K, int N, int* tickets,
+                        float* partials, int num_sms, int* err, cudaStream_t stream);
 cudaError_t bf16_set_attributes();
 // tmW: packed weights, box 32 B x kS8TileN rows, no swizzle.  tmP1 / tmP2:
 // the two fp8 activation pieces [T][K], box 128 B x kS8TileT rows, 128-byte

@@ -458,45 +458,17 @@ cudaError_t s8_set_attributes() {
 
 int s8_token_tile(int T) { return T <= kS8SmallTileT ? kS8SmallTileT : kS8TileT; }
 
-// Work split of the s8 rung: P CTAs walk nfull whole tiles, then the rest
-// of the tiles as `chunks` group ranges each.  Chunking applies when the
-// rest fills at most half a wave (then a quarter to a third of a tile per
-// CTA finishes the call instead of a whole tile on few SMs).
-struct S8Split {
-  int tok, P, nfull, chunks;
-};
-S8Split s8_split(int T, int K, int N, int num_sms) {
-  S8Split sp;
-  sp.tok = s8_token_tile(T);
-  const int tiles = ((N + kRowsS - 1) / kRowsS) * ((T + sp.tok - 1) / sp.tok);
-  const int G = K / 128;
-  const int rounds = tiles / num_sms;
-  const int rest = tiles - rounds * num_sms;
-  sp.nfull = tiles;
-  sp.chunks = 1;
-  if (rest > 0 && 2 * rest <= num_sms) {
-    int c = num_sms / rest;
-    if (c > kS8MaxChunks) c = kS8MaxChunks;
-    if (c > G / 2) c = G / 2;
-    if (c >= 2) {
-      sp.nfull = rounds * num_sms;
-      sp.chunks = c;
-    }
-  }
-  const int items = sp.nfull + (tiles - sp.nfull) * sp.chunks;
-  sp.P = items < num_sms ? items : num_sms;
-  return sp;
-}
-
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
                       const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
                       float* y, int T, int K, int N, int* tickets, float* partials, int num_sms,
                       int* err, cudaStream_t stream) {
-  const S8Split sp = s8_split(T, K, N, num_sms);
+  const int tok = s8_token_tile(T);
+  const int tiles = ((N + kRowsS - 1) / kRowsS) * ((T + tok - 1) / tok);
+  const TileSplit sp = tile_split(tiles, K / 128, num_sms);
   // without a y tensor map (N % 4 != 0: rows not 16-byte strided; or the
   // 32-token tile) the fold warps store y directly; the map argument is then
   // an unused copy
-  if (sp.tok == kS8SmallTileT)
+  if (tok == kS8SmallTileT)
     s8tc_kernel<kS8SmallTileT><<<sp.P, kThreadsS, SL<kS8SmallTileT>::kAlloc, stream>>>(
         *tmW, *tmP1, *tmP2, *tmW, scales, x_scale, y, T, K, N, 0, sp.nfull, sp.chunks, tickets,
         partials, err);
