@@ -129,6 +129,7 @@ constexpr int kMaxDevices = 64;
 struct DevState {
   bool ready = false;
   int sms = 0;
+  size_t l2 = 0;  // L2 bytes
   int* err = nullptr;
 };
 DevState g_dev[kMaxDevices];
@@ -145,6 +146,7 @@ int device_state(DevState** out) {
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TERN_ENODEV;
     if (prop.major != 10 || prop.minor != 3) return TERN_ENODEV;  // built for sm_103a only
     d.sms = prop.multiProcessorCount;
+    d.l2 = static_cast<size_t>(prop.l2CacheSize);
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return TERN_ECUDA;
     d.err = static_cast<int*>(p);
@@ -438,17 +440,10 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       rc = make_map_u8(&tmP2, p2, static_cast<uint64_t>(K), static_cast<uint64_t>(T),
                        static_cast<uint64_t>(K), 128, tok, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc != TERN_OK) return rc;
-      CUtensorMap tmY;
-      const bool y_tma = (N % 4) == 0 && tok == kS8TileT;
-      if (y_tma) {
-        rc = make_map_f32(&tmY, y, static_cast<uint64_t>(N), static_cast<uint64_t>(T),
-                          static_cast<uint64_t>(N) * 4, 32, kS8YBoxT);
-        if (rc != TERN_OK) return rc;
-      }
       float* partials = reinterpret_cast<float*>(scratch + 2 * piece +
                                                  align_up(sizeof(float) * T, 256));
-      rc = launch_s8(&tmW, &tmP1, &tmP2, y_tma ? &tmY : nullptr, scales, xs, y, T, K, N,
-                     static_cast<int*>(workspace), partials, d->sms, d->err, st) == cudaSuccess
+      rc = launch_s8(&tmW, &tmP1, &tmP2, scales, xs, y, T, K, N, static_cast<int*>(workspace),
+                     partials, d->sms, d->l2, d->err, st) == cudaSuccess
                ? TERN_OK
                : TERN_ECUDA;
       ++launches;

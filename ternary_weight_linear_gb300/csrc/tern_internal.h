@@ -90,11 +90,15 @@ inline TileSplit tile_split(int tiles, int G, int num_sms) {
 // (at most 160 chunk items, each kS8FoldWarps blocks of kS8YBoxT x 32 floats)
 constexpr size_t kS8PartialBytes =
     static_cast<size_t>(160) * kS8FoldWarps * kS8YBoxT * 32 * sizeof(float);
-size_t s8_smem_bytes();
 cudaError_t s8_set_attributes();
 // Token tile the s8 rung uses for T tokens (the pieces' tensor maps' box
 // height): kS8SmallTileT for T <= kS8SmallTileT, else kS8TileT.
 int s8_token_tile(int T);
+// Stage ring of the s8 kernel: 12 for the small token tile; for the 128-token
+// tile 4, or kS8DeepStages when the piece blocks (2 T K bytes, all read while
+// a wave of CTAs crosses one row block) take more than half of the L2.
+constexpr int kS8DeepStages = 6;
+int s8_stages(int T, int K, size_t l2_bytes);
 
 // bf16 rung: x reordered for the MMA (xp [T][K] bf16, optionally rotated
 // first), then tiles of 128 weight rows x 128 tokens on tcgen05 kind::f16.
@@ -107,14 +111,13 @@ cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CU
                         float* partials, int num_sms, int* err, cudaStream_t stream);
 cudaError_t bf16_set_attributes();
 // tmW: packed weights, box 32 B x kS8TileN rows, no swizzle.  tmP1 / tmP2:
-// the two fp8 activation pieces [T][K], box 128 B x kS8TileT rows, 128-byte
-// swizzle.  tmY: y as fp32 [T][N], box 32 x kS8YBoxT, or null (then y is stored
-// directly; needed when N % 4 != 0).  x_scale: [T] floats, readable up to T
-// rounded up to 4.
+// the two fp8 activation pieces [T][K], box 128 B x s8_token_tile(T) rows,
+// 128-byte swizzle.  y: fp32 [T][N], stored directly.  x_scale: [T] floats,
+// readable up to T rounded up to 4.
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
-                      const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
-                      float* y, int T, int K, int N, int* tickets, float* partials, int num_sms,
-                      int* err, cudaStream_t stream);
+                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
+                      int* tickets, float* partials, int num_sms, size_t l2_bytes, int* err,
+                      cudaStream_t stream);
 
 // Pack and quantise.
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,

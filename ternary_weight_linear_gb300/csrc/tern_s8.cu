@@ -16,13 +16,16 @@
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N).  Per
 // 128-wide group a stage holds the packed weights (TMA, 128 rows x 32 B) and
 // the two piece blocks (TMA, 128 tokens x 128 B each, 128-byte swizzle, the
-// canonical K-major SW128 layout of the MMA's B operand).  Warp roles:
+// canonical K-major SW128 layout of the MMA's B operand).  The stage ring in
+// shared memory is deeper than the ring of A slots in TMEM (which shares the
+// 512 columns with the D slots), so copies run further ahead than decodes.
+// Warp roles:
 //   warps 0-3   decode the group's weights into an A slot in TMEM
 //               (tcgen05.st, one row per thread);
 //   kFoldW warps fold: read the D slot (each warp 32 rows x kFC tokens), add
 //               8 s[n][g] * D into register accumulators, and at the end of
-//               the tile stage y = xs[t] * acc in shared memory and write it
-//               with a TMA store that overlaps the next tile;
+//               the tile store y = xs[t] * acc (each warp instruction writes
+//               32 consecutive floats of one token's row);
 //   one warp    producer (TMA) and the tile's x_scale block;
 //   two warps   issue (one thread each, alternate groups) 8 MMAs per group
 //               (4 per piece, K = 32 each) into a D slot (128 columns),
@@ -57,35 +60,38 @@ constexpr int kThreadsS = (kMmaW + kMmaWarps) * 32;
 // kMmaWarps <= kNDS.
 static_assert(kMmaWarps <= kNDS, "issuers may outrun the accumulator ring's parity check");
 
-// Layout for a token tile of TOK tokens (MMA N): 128, or 32 for T <= 32.  A
-// 32-token tile does a quarter of the MMA and fold work per weight byte, so
-// the call is bound by the weight bytes in flight: it gets a ring of 12
-// stages (each stage has an A slot of 32 TMEM columns) where the 128-token
-// tile has 4.
-template <int TOK>
+// Layout for a token tile of TOK tokens (MMA N): 128, or 32 for T <= 32,
+// and a stage ring of NST stages (36 KB of copies per 128-token stage, 12 KB
+// per 32-token one).  A 32-token tile does a quarter of the MMA and fold work
+// per weight byte, so the call is bound by the bytes in flight: it gets 12
+// stages.  The 128-token tile runs 4, or 6 when the piece blocks are too
+// large to stay in L2 (each wave of CTAs reads all of them, so they then miss
+// more often).  A slots (32 TMEM columns each) take what the D slots leave.
+template <int TOK, int NST>
 struct SL {
-  static constexpr int kStages = TOK == 32 ? 12 : 4;
+  static constexpr int kStages = NST;
+  static constexpr int kASlots = TOK == 32 ? 12 : 4;
+  // Parity waits: an issuer's previous use of a stage or A slot was its own
+  // group (the groups alternate between the issuers).  A slot a of group u
+  // is free once the stage of group u - kASlots is empty (its MMAs done),
+  // which needs kASlots <= kStages.
+  static_assert(kStages % kMmaWarps == 0 && kASlots % kMmaWarps == 0, "issuer parity");
+  static_assert(kASlots <= kStages, "A slot reuse");
   static constexpr int kFC = TOK * 4 / kFoldW;  // tokens (D columns) per fold warp
   static_assert(kFoldW % 4 == 0 && kFC % 16 == 0, "fold split");
-  // y through TMA stores of one box per fold warp (the y map's box is
-  // kS8YBoxT tokens); the 32-token tile stores y directly
-  static constexpr bool kYTma = TOK == kS8TileT;
-  static_assert(!kYTma || kFC == kS8YBoxT, "the y map's box");
   static constexpr int kPB = TOK * 128;   // one piece block of a group
   static constexpr int kWB = kRowsS * 32;  // packed weights of a group (4 KB)
   static constexpr int kP1Off = 0;         // 1024-aligned (128-byte swizzle atoms)
   static constexpr int kP2Off = kP1Off + kStages * kPB;
   static constexpr int kWOff = kP2Off + kStages * kPB;
-  static constexpr int kYB = kFC * 32 * 4;  // one fold warp's output block (kFC tokens x 32 rows)
-  static constexpr int kYOff = kWOff + kStages * kWB;
-  static constexpr int kXsOff = kYOff + (kYTma ? kFoldW * kYB : 0);  // x_scale of 2 tiles
+  static constexpr int kXsOff = kWOff + kStages * kWB;  // x_scale of 2 tiles
   static constexpr int kBarOff = kXsOff + 2 * TOK * 4;
-  static constexpr int kNumBars = 3 * kStages + 2 * kNDS + 4 + kMmaWarps;
+  static constexpr int kNumBars = 2 * kStages + kASlots + 2 * kNDS + 4 + kMmaWarps;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kACol = 0;
-  static constexpr uint32_t kDCol = kStages * 32;
+  static constexpr uint32_t kDCol = kASlots * 32;
   static_assert(kP2Off % 1024 == 0 && kWOff % 1024 == 0 && kXsOff % 16 == 0, "alignment");
   static_assert(kDCol + kNDS * TOK <= 512, "TMEM budget");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
@@ -99,24 +105,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-template <int TOK>
+template <int TOK, int NST>
 __global__ void __launch_bounds__(kThreadsS, 1)
     s8tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmP1,
-                const __grid_constant__ CUtensorMap tmP2, const __grid_constant__ CUtensorMap tmY,
-                const uint16_t* __restrict__ scales, const float* __restrict__ x_scale,
-                float* __restrict__ y, int T, int K, int N, int y_tma, int nfull, int chunks,
+                const __grid_constant__ CUtensorMap tmP2, const uint16_t* __restrict__ scales,
+                const float* __restrict__ x_scale, float* __restrict__ y, int T, int K, int N,
+                int nfull, int chunks,
                 int* __restrict__ tickets, float* __restrict__ partials, int* err) {
-  using L = SL<TOK>;
+  using L = SL<TOK, NST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  // empty[s]: the stage's weights are decoded and its A slot and pieces are
-  // read by the MMAs (the A ring is the stage ring, so a stage refilled by the
-  // producer also has a free A slot by the time its copy lands)
+  // empty[s]: the stage's weights are decoded and its group's MMAs are
+  // complete (so its pieces and the group's A slot have been read)
   uint64_t* empty = full + L::kStages;
   uint64_t* afull = empty + L::kStages;  // A slot written
-  uint64_t* mdone = afull + L::kStages;  // MMAs writing the D slot done
+  uint64_t* mdone = afull + L::kASlots;  // MMAs writing the D slot done
   uint64_t* dfree = mdone + kNDS;      // D slot read back
   uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
   uint64_t* xsfree = xsfull + 2;       // [2] ... and used
@@ -168,8 +173,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecW + 1);
-      mbar_init(&afull[s], kDecW);
     }
+    for (int a = 0; a < L::kASlots; ++a) mbar_init(&afull[a], kDecW);
     for (int d = 0; d < kNDS; ++d) {
       mbar_init(&mdone[d], 1);
       mbar_init(&dfree[d], kFoldW);
@@ -183,7 +188,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmP1);
     prefetch_tensormap(&tmP2);
-    if (y_tma) prefetch_tensormap(&tmY);
   }
   if (warp == kMmaW) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -235,13 +239,18 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // ------------------------------------------------------------ decode
     const int r = warp * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    int s = 0;
+    int s = 0, a = 0;
     uint32_t ph = 0;
     for (int u = 0; u < units; ++u) {
-      // the copy into stage s was issued after the MMAs that last read A
-      // slot s completed (the producer waited on empty[s]), so its landing
-      // also frees the slot
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, err))) break;
+      // A slot a was last read by group v = u - kASlots, whose stage's empty
+      // barrier completes with those MMAs (implied by full[s] when the rings
+      // have one length: the copy into stage s waited on it)
+      bool ok = mbar_wait(&full[s], ph, err);
+      if (L::kASlots < L::kStages && ok && u >= L::kASlots) {
+        const int v = u - L::kASlots;
+        ok = mbar_wait(&empty[v % L::kStages], (v / L::kStages) & 1, err);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint8_t* wrow = smem + L::kWOff + s * L::kWB + r * 32;
       const uint4 c0 = lds_v4(wrow);
@@ -255,18 +264,19 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         av[4 * j + 2] = decode_e4m3<2>(w[j]);
         av[4 * j + 3] = decode_e4m3<3>(w[j]);
       }
-      tmem_st32(tbase + lane_off + L::kACol + s * 32, av);
+      tmem_st32(tbase + lane_off + L::kACol + a * 32, av);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&afull[s]);
+        mbar_arrive(&afull[a]);
         mbar_arrive(&empty[s]);
       }
       if (++s == L::kStages) {
         s = 0;
         ph ^= 1;
       }
+      if (++a == L::kASlots) a = 0;
     }
   } else if (warp >= kMmaW) {
     // ------------------------------------------------------------ MMA issuers
@@ -278,16 +288,17 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const uint64_t desc2 = smem_desc_sw128(smem_addr(smem + L::kP2Off));
       int u = warp - kMmaW;
       for (; u < units; u += kMmaWarps) {
-        const int s = u % L::kStages, d = u % kNDS;
-        const uint32_t ph = (u / L::kStages) & 1, dph = (u / kNDS) & 1;
-        if (!mbar_wait(&afull[s], ph, err)) break;
+        const int s = u % L::kStages, a = u % L::kASlots, d = u % kNDS;
+        const uint32_t ph = (u / L::kStages) & 1, aph = (u / L::kASlots) & 1;
+        const uint32_t dph = (u / kNDS) & 1;
+        if (!mbar_wait(&afull[a], aph, err)) break;
         // the pieces landed (implied by afull; waited on here as well so the
         // tensor core's reads are ordered after the copy for this thread)
         if (!mbar_wait(&full[s], ph, err)) break;
         if (u >= kNDS && !mbar_wait(&dfree[d], dph ^ 1, err)) break;
         tc_fence_after();
         const uint32_t dcol = tbase + L::kDCol + d * TOK;
-        const uint32_t acol = tbase + L::kACol + s * 32;
+        const uint32_t acol = tbase + L::kACol + a * 32;
         // descriptor start addresses advance in 16-byte units: a stage is
         // kPB bytes, a K = 32 step 32 bytes inside the swizzle atom
         const uint64_t b1 = desc1 + static_cast<uint64_t>((s * L::kPB) >> 4);
@@ -404,25 +415,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       if (!store) {
 #pragma unroll
         for (int j = 0; j < L::kFC; ++j) acc[j] = 0.f;
-      } else if (L::kYTma && y_tma) {
-        // stage the warp's L::kFC x 32 block and store it asynchronously: the
-        // next tile's groups overlap the write-back
-        float* stg = reinterpret_cast<float*>(smem + L::kYOff + (warp - kDecW) * L::kYB);
-        if (lane == 0) bulk_wait_group_read0();  // the warp's previous block was read out
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < L::kFC; ++j) {
-          stg[j * 32 + lane] = xst[j] * acc[j];
-          acc[j] = 0.f;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        // a box that starts inside the tensor (the rest is clipped)
-        if (lane == 0 && rb * kRowsS + fq * 32 < N && t0 < T) {
-          tma_store_2d(&tmY, stg, rb * kRowsS + fq * 32, t0);
-          bulk_commit_group();
-        }
       } else {
+        // plain stores: a staged block and a TMA store per warp measured
+        // slower, and the stage ring gets the shared memory instead
 #pragma unroll
         for (int j = 0; j < L::kFC; ++j) {
           const int t = t0 + j;
@@ -433,7 +428,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&xsfree[xb]);
     }
-    if (lane == 0) bulk_wait_group0();  // output blocks written before the CTA exits
   }
 
   tc_fence_before();
@@ -444,39 +438,44 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 
 }  // namespace
 
-size_t s8_smem_bytes() { return SL<kS8TileT>::kAlloc; }
+// The s8 kernel's instances: (token tile, stages).
+#define TERN_S8_INSTANCES(X) X(kS8SmallTileT, 12) X(kS8TileT, 4) X(kS8TileT, kS8DeepStages)
 
 cudaError_t s8_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(s8tc_kernel<kS8TileT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SL<kS8TileT>::kAlloc);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(s8tc_kernel<kS8SmallTileT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SL<kS8SmallTileT>::kAlloc);
+  cudaError_t e = cudaSuccess;
+#define TERN_S8_ATTR(TOK, NST)                                                             \
+  if (e == cudaSuccess)                                                                    \
+    e = cudaFuncSetAttribute(s8tc_kernel<TOK, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             SL<TOK, NST>::kAlloc);
+  TERN_S8_INSTANCES(TERN_S8_ATTR)
+#undef TERN_S8_ATTR
+  return e;
 }
 
 int s8_token_tile(int T) { return T <= kS8SmallTileT ? kS8SmallTileT : kS8TileT; }
 
+int s8_stages(int T, int K, size_t l2_bytes) {
+  if (s8_token_tile(T) == kS8SmallTileT) return 12;
+  return 2 * static_cast<size_t>(T) * K > l2_bytes / 2 ? kS8DeepStages : 4;
+}
+
 cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUtensorMap* tmP2,
-                      const CUtensorMap* tmY, const uint16_t* scales, const float* x_scale,
-                      float* y, int T, int K, int N, int* tickets, float* partials, int num_sms,
-                      int* err, cudaStream_t stream) {
-  const int tok = s8_token_tile(T);
+                      const uint16_t* scales, const float* x_scale, float* y, int T, int K, int N,
+                      int* tickets, float* partials, int num_sms, size_t l2_bytes, int* err,
+                      cudaStream_t stream) {
+  const int tok = s8_token_tile(T), nst = s8_stages(T, K, l2_bytes);
   const int tiles = ((N + kRowsS - 1) / kRowsS) * ((T + tok - 1) / tok);
   const TileSplit sp = tile_split(tiles, K / 128, num_sms);
-  // without a y tensor map (N % 4 != 0: rows not 16-byte strided; or the
-  // 32-token tile) the fold warps store y directly; the map argument is then
-  // an unused copy
-  if (tok == kS8SmallTileT)
-    s8tc_kernel<kS8SmallTileT><<<sp.P, kThreadsS, SL<kS8SmallTileT>::kAlloc, stream>>>(
-        *tmW, *tmP1, *tmP2, *tmW, scales, x_scale, y, T, K, N, 0, sp.nfull, sp.chunks, tickets,
-        partials, err);
-  else
-    s8tc_kernel<kS8TileT><<<sp.P, kThreadsS, SL<kS8TileT>::kAlloc, stream>>>(
-        *tmW, *tmP1, *tmP2, tmY ? *tmY : *tmW, scales, x_scale, y, T, K, N, tmY ? 1 : 0,
-        sp.nfull, sp.chunks, tickets, partials, err);
-  return cudaGetLastError();
+#define TERN_S8_LAUNCH(TOK, NST)                                                            \
+  if (tok == TOK && nst == NST) {                                                           \
+    s8tc_kernel<TOK, NST><<<sp.P, kThreadsS, SL<TOK, NST>::kAlloc, stream>>>(               \
+        *tmW, *tmP1, *tmP2, scales, x_scale, y, T, K, N, sp.nfull, sp.chunks, tickets,       \
+        partials, err);                                                                     \
+    return cudaGetLastError();                                                              \
+  }
+  TERN_S8_INSTANCES(TERN_S8_LAUNCH)
+#undef TERN_S8_LAUNCH
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace tern

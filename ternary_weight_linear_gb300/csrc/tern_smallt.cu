@@ -446,11 +446,19 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16
                                                                uint8_t* __restrict__ out, int K,
                                                                int tok0, int Tt, int KS) {
   grid_dependents_launch();
-  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = kGS * KS;
   const int tasks = TC<TT>::kH * groups;
   const int stride = gridDim.x * kPrepWarps;
+  // Warm L2 with this warp's groups of x while the previous grid finishes (a
+  // prefetch only moves lines into L2, harmless while x may still be written).
+  if (lane < 32) {
+    const int task = blockIdx.x * kPrepWarps + warp + lane * stride;
+    const int t = task / groups, kbase = (task % groups) * 128;
+    if (task < tasks && t < Tt && kbase < K)
+      bulk_prefetch_l2(x + static_cast<size_t>(tok0 + t) * K + kbase, 256u);
+  }
+  grid_dependency_wait();  // x (and this buffer's last reader) come from earlier work
   // two tasks' loads in flight before their arithmetic
   for (int t0 = blockIdx.x * kPrepWarps + warp; t0 < tasks; t0 += 2 * stride) {
     uint2 raw[2];

@@ -231,6 +231,19 @@ def test_shapes_s8(tl, K, N, T):
     _check_case(tl, synth.case("shape", T, K=K, N=N, seed=K + N + T))
 
 
+def test_s8_deep_ring_ragged(tl):
+    # The s8 kernel's deeper stage ring, taken when the activation pieces
+    # (2 T K bytes) exceed half the L2: a ragged token tile (2100 = 16 x 128 +
+    # 52), an odd group count (K = 16512, 129 groups) and a partial row block
+    # (N = 333), on sampled outputs.
+    import torch
+    props = torch.cuda.get_device_properties(0)
+    T, K, N = 2100, 16512, 333
+    assert 2 * T * K > props.L2_cache_size // 2
+    assert _check_case(tl, synth.case("deep", T, K=K, N=N, seed=11, outliers=True), full=False,
+                       samples=8192) == "s8"
+
+
 @pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 521, 200), (2048, 300, 129)])
 def test_shapes_bf16_rung(tl, K, N, T):
     # the exact bf16 prefill rung on ragged shapes (N % 4 != 0: y stored directly)
