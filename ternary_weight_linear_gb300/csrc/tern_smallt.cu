@@ -450,9 +450,10 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 16) xprep_kernel(const uint16
   const int groups = kGS * KS;
   const int tasks = TC<TT>::kH * groups;
   const int stride = gridDim.x * kPrepWarps;
-  // Warm L2 with this warp's groups of x while the previous grid finishes (a
-  // prefetch only moves lines into L2, harmless while x may still be written).
-  if (lane < 32) {
+  // Warm L2 with the groups of x this warp reads first (lane i: its i-th
+  // task) while the previous grid finishes; a prefetch only moves lines into
+  // L2, so it is harmless while x may still be being written.
+  {
     const int task = blockIdx.x * kPrepWarps + warp + lane * stride;
     const int t = task / groups, kbase = (task % groups) * 128;
     if (task < tasks && t < Tt && kbase < K)
