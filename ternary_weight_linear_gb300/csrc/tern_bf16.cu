@@ -67,7 +67,7 @@ struct BL {
   static constexpr int kYB = kFCB * 32 * 4;  // one fold warp's output block
   static constexpr int kYOff = kWOff + kStagesB * kWB;
   static constexpr int kBarOff = kYOff + kFoldWB * kYB;
-  static constexpr int kNumBars = 3 * kStagesB + 2 * kNDB + kMmaWarpsB;
+  static constexpr int kNumBars = 3 * kStagesB + kNDB + kMmaWarpsB;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -121,12 +121,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + BL::kBarOff);
-  // empty[s]: the stage's weights are decoded and its A slot and x boxes are
-  // read by the MMAs
+  // empty[s]: the stage's weights are decoded and its group's MMAs are
+  // complete (its A slot and x boxes have been read, and its D slot holds the
+  // group's sums)
   uint64_t* empty = full + kStagesB;
   uint64_t* afull = empty + kStagesB;  // A slot written
-  uint64_t* mdone = afull + kStagesB;  // MMAs writing the D slot done
-  uint64_t* dfree = mdone + kNDB;      // D slot read back
+  uint64_t* dfree = afull + kStagesB;  // D slot read back
   uint64_t* mfin = dfree + kNDB;       // [issuer] all of that issuer's MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BL::kTmemSlot);
 
@@ -175,10 +175,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_init(&empty[s], kDecWB + 1);
       mbar_init(&afull[s], kDecWB);
     }
-    for (int d = 0; d < kNDB; ++d) {
-      mbar_init(&mdone[d], 1);
-      mbar_init(&dfree[d], kFoldWB);
-    }
+    for (int d = 0; d < kNDB; ++d) mbar_init(&dfree[d], kFoldWB);
     for (int w = 0; w < kMmaWarpsB; ++w) mbar_init(&mfin[w], 1);
     fence_mbar_init();
     prefetch_tensormap(&tmW);
@@ -277,10 +274,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (; u < units; u += kMmaWarpsB) {
         const int s = u % kStagesB, d = u % kNDB;
         const uint32_t ph = (u / kStagesB) & 1, dph = (u / kNDB) & 1;
+        // The decoders arrive on afull only after waiting on the stage's
+        // copy, so acquiring afull orders the x boxes' bytes before these
+        // MMAs too (release/acquire chains are transitive).
         if (!mbar_wait(&afull[s], ph, err)) break;
-        // the x boxes landed (implied by afull; waited on here as well so the
-        // tensor core's reads are ordered after the copy for this thread)
-        if (!mbar_wait(&full[s], ph, err)) break;
         if (u >= kNDB && !mbar_wait(&dfree[d], dph ^ 1, err)) break;
         tc_fence_after();
         const uint32_t dcol = tbase + BL::kDCol + d * kTokB;
@@ -293,8 +290,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         for (int kk = 0; kk < 4; ++kk) mma_f16_ts(dcol, acol + kk * 8, b0 + 2 * kk, idesc, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_f16_ts(dcol, acol + 32 + kk * 8, b1 + 2 * kk, idesc, true);
-        mma_commit(&empty[s]);
-        mma_commit(&mdone[d]);
+        mma_commit(&empty[s]);  // one commit per group: the fold waits on it too
       }
       mma_commit(&mfin[warp - kMmaWB]);
       mbar_wait(&mfin[warp - kMmaWB], 0, err);
@@ -309,8 +305,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     float acc[kFCB];
 #pragma unroll
     for (int j = 0; j < kFCB; ++j) acc[j] = 0.f;
-    int d = 0;
-    uint32_t dph = 0;
+    // group u's sums are in D slot u % kNDB once empty[u % kStagesB] has
+    // completed.  Parity: that barrier's next phase needs the MMAs of group
+    // u + kStagesB, which wait for this warp's fold of group
+    // u + kStagesB - kNDB (later than u).
+    static_assert(kStagesB > kNDB, "the fold's parity wait on the stage ring");
+    int d = 0, s = 0;
+    uint32_t ph = 0;
     bool ok = true;
     for (int m = 0; m < nitems && ok; ++m) {
       const Item itm = item_of(m);
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (int g = itm.g0; g < itm.g1; ++g) {
         const float sg = snext;
         if (g + 1 < itm.g1) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], dph, err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ph, err))) {
           ok = false;
           break;
         }
@@ -341,9 +342,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           for (int j = 0; j < 32; ++j)
             acc[32 * c + j] = fmaf(sg, __uint_as_float(dv[j]), acc[32 * c + j]);
         }
-        if (++d == kNDB) {
-          d = 0;
-          dph ^= 1;
+        if (++d == kNDB) d = 0;
+        if (++s == kStagesB) {
+          s = 0;
+          ph ^= 1;
         }
       }
       if (!ok) break;

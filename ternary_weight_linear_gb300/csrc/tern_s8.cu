@@ -77,6 +77,7 @@ struct SL {
   // which needs kASlots <= kStages.
   static_assert(kStages % kMmaWarps == 0 && kASlots % kMmaWarps == 0, "issuer parity");
   static_assert(kASlots <= kStages, "A slot reuse");
+  static_assert(kStages > kNDS, "the fold's parity wait on the stage ring");
   static constexpr int kFC = TOK * 4 / kFoldW;  // tokens (D columns) per fold warp
   static_assert(kFoldW % 4 == 0 && kFC % 16 == 0, "fold split");
   static constexpr int kPB = TOK * 128;   // one piece block of a group
@@ -86,7 +87,7 @@ struct SL {
   static constexpr int kWOff = kP2Off + kStages * kPB;
   static constexpr int kXsOff = kWOff + kStages * kWB;  // x_scale of 2 tiles
   static constexpr int kBarOff = kXsOff + 2 * TOK * 4;
-  static constexpr int kNumBars = 2 * kStages + kASlots + 2 * kNDS + 4 + kMmaWarps;
+  static constexpr int kNumBars = 2 * kStages + kASlots + kNDS + 4 + kMmaWarps;
   static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -118,11 +119,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   // empty[s]: the stage's weights are decoded and its group's MMAs are
-  // complete (so its pieces and the group's A slot have been read)
+  // complete (so its pieces and the group's A slot have been read, and its D
+  // slot holds the group's sums)
   uint64_t* empty = full + L::kStages;
   uint64_t* afull = empty + L::kStages;  // A slot written
-  uint64_t* mdone = afull + L::kASlots;  // MMAs writing the D slot done
-  uint64_t* dfree = mdone + kNDS;      // D slot read back
+  uint64_t* dfree = afull + L::kASlots;  // D slot read back
   uint64_t* xsfull = dfree + kNDS;     // [2] tile's x_scale landed
   uint64_t* xsfree = xsfull + 2;       // [2] ... and used
   uint64_t* mfin = xsfree + 2;         // [issuer] all of that issuer's MMAs complete
@@ -175,10 +176,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       mbar_init(&empty[s], kDecW + 1);
     }
     for (int a = 0; a < L::kASlots; ++a) mbar_init(&afull[a], kDecW);
-    for (int d = 0; d < kNDS; ++d) {
-      mbar_init(&mdone[d], 1);
-      mbar_init(&dfree[d], kFoldW);
-    }
+    for (int d = 0; d < kNDS; ++d) mbar_init(&dfree[d], kFoldW);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&xsfull[b], 1);
       mbar_init(&xsfree[b], kFoldW);
@@ -281,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   } else if (warp >= kMmaW) {
     // ------------------------------------------------------------ MMA issuers
     // one thread per issuer warp, groups u = w, w + kMmaWarps, ...; no warp
-    // votes, two commits per group
+    // votes, one commit per group
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kRowsS, TOK);
       const uint64_t desc1 = smem_desc_sw128(smem_addr(smem + L::kP1Off));
@@ -289,12 +287,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       int u = warp - kMmaW;
       for (; u < units; u += kMmaWarps) {
         const int s = u % L::kStages, a = u % L::kASlots, d = u % kNDS;
-        const uint32_t ph = (u / L::kStages) & 1, aph = (u / L::kASlots) & 1;
-        const uint32_t dph = (u / kNDS) & 1;
+        const uint32_t aph = (u / L::kASlots) & 1, dph = (u / kNDS) & 1;
+        // The decoders arrive on afull only after waiting on the stage's
+        // copy, so acquiring afull orders the pieces' bytes before these
+        // MMAs too (release/acquire chains are transitive).
         if (!mbar_wait(&afull[a], aph, err)) break;
-        // the pieces landed (implied by afull; waited on here as well so the
-        // tensor core's reads are ordered after the copy for this thread)
-        if (!mbar_wait(&full[s], ph, err)) break;
         if (u >= kNDS && !mbar_wait(&dfree[d], dph ^ 1, err)) break;
         tc_fence_after();
         const uint32_t dcol = tbase + L::kDCol + d * TOK;
@@ -308,12 +305,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           mma_f8f6f4_ts(dcol, acol + kk * 8, b1 + 2 * kk, idesc, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_f8f6f4_ts(dcol, acol + kk * 8, b2 + 2 * kk, idesc, true);
-        mma_commit(&empty[s]);
-        mma_commit(&mdone[d]);
+        mma_commit(&empty[s]);  // one commit per group: the fold waits on it too
       }
       // This issuer's MMAs are complete before the CTA tears down.  (Its own
-      // barrier: a D slot's barrier may have moved on by two phases when
-      // another issuer's later group reused the slot.)
+      // barrier: a stage's barrier may have moved on by two phases when the
+      // other issuer's later group reused the stage.)
       mma_commit(&mfin[warp - kMmaW]);
       mbar_wait(&mfin[warp - kMmaW], 0, err);
     }
@@ -327,8 +323,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     float acc[L::kFC];
 #pragma unroll
     for (int j = 0; j < L::kFC; ++j) acc[j] = 0.f;
-    int d = 0;
-    uint32_t dph = 0;
+    // group u's sums are in D slot u % kNDS once empty[u % kStages] has
+    // completed.  Parity: that barrier's next phase needs the MMAs of group
+    // u + kStages, which wait for this warp's fold of group u + kStages - kNDS
+    // (later than u, as kStages > kNDS).
+    int d = 0, s = 0;
+    uint32_t ph = 0;
     bool ok = true;
     for (int m = 0; m < nitems && ok; ++m) {
       const Item itm = item_of(m);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       for (int g = itm.g0; g < itm.g1; ++g) {
         const float sg = 8.0f * snext;  // D holds acc / 8
         if (g + 1 < itm.g1) snext = n < N ? __half2float(__ushort_as_half(srow[g + 1])) : 0.f;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mdone[d], dph, err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ph, err))) {
           ok = false;
           break;
         }
@@ -365,9 +365,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           for (int j = 0; j < kCh; ++j)
             acc[kCh * c + j] = fmaf(sg, __uint_as_float(dv[j]), acc[kCh * c + j]);
         }
-        if (++d == kNDS) {
-          d = 0;
-          dph ^= 1;
+        if (++d == kNDS) d = 0;
+        if (++s == L::kStages) {
+          s = 0;
+          ph ^= 1;
         }
       }
       if (!ok) break;
