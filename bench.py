@@ -501,12 +501,17 @@ def run_ours(args, rank, world, local):
     # activation split into two exact pieces), so its ceiling in int8 ops is
     # half the e4m3 tensor rate, i.e. the bf16 rate: e4m3 runs at twice bf16
     # (nominal ratio), and the measured bf16 peak is the denominator.
+    # DRAM bytes of one pass (both launches) from the committed ncu summaries
+    s8_src = os.path.join(ROOT, "ternary_weight_linear_gb300", "csrc", "tern_s8.cu")
+    s8_parts = [profile_traffic(s8_src, f) for f in ("s8tc_kernel_gu_t2048.md",
+                                                     "s8tc_kernel_dn_t2048.md")]
+    s8_traffic = sum(s8_parts) if all(v is not None for v in s8_parts) else None
     s8 = {"metric": "int8 TOPS at T=2048 (s8 rung, gate+up + down)", "value": round(s8_tops, 1),
           "unit": "TOPS", "us_per_pass": round(s8_us, 1),
           "roofline": {"bound": "tensor", "achieved": round(s8_tops, 1),
                        "peak": peaks.get("bf16_tflops", 1900.0), "peak_kind": peak_kind + " bf16",
                        "unit": "TOPS", "frac": round(s8_tops / peaks.get("bf16_tflops", 1900.0), 4),
-                       "traffic": None}}
+                       "traffic": s8_traffic, "traffic_unit": "bytes per pass (gate+up + down)"}}
 
     # ---- whole-stack family (64 resident layers) at T = 1, 4, 2048
     stack = run_stack(tl, torch, gen, dev, peaks, stream) if not args.no_stack else None
