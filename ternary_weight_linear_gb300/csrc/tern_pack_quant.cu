@@ -54,6 +54,39 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ W,
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Per-token code of v: rint(v / scale) clamped to [-127, 127], the quotient
+// rounded as one IEEE single-precision division (nearest-even, as rint).
+// Without a division per element: with inv = 1 / scale rounded, q0 = v * inv
+// differs from v / scale by less than 128 * (2^-23 + 2^-48) < 1.53e-5 (|v| <=
+// absmax, so |v / scale| < 128; two roundings of relative error 2^-24 each),
+// and the rounded quotient from v / scale by at most half an ulp below 128,
+// 2^-18; so the two are less than kQMargin = 2^-15 apart.  When q0 lies
+// farther than kQMargin from every half-integer, both fall strictly inside
+// the same rounding interval and rint(q0) is the code; otherwise the element
+// takes the division.  fast: scale and 1 / scale normal (absmax >= 127 *
+// 2^-126), where those relative bounds hold; else every element divides.
+constexpr float kQMargin = 3.0517578125e-05f;  // 2^-15
+__device__ __forceinline__ float quant_code(float v, float scale, float inv, bool fast) {
+  float r;
+  if (fast) {
+    const float q0 = v * inv;
+    r = rintf(q0);
+    if (!(fabsf(q0 - r) < 0.5f - kQMargin)) r = rintf(v / scale);
+  } else {
+    r = rintf(v / scale);
+  }
+  return fminf(fmaxf(r, -127.f), 127.f);
+}
+// max of two floats that propagates NaN (IEEE maximum, not maximumNumber)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ bool quant_fast(float scale) {
+  return scale >= 1.1754943508222875e-38f && scale < 8.507059173023462e+37f;  // [2^-126, 2^126)
+}
+
 // One CTA per token.  Pass 1: absmax.  Pass 2: codes.
 constexpr int kQThreads = 256;
 __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __restrict__ x,
@@ -80,6 +113,8 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
   for (int i = 1; i < kQThreads / 32; ++i) a = fmaxf(a, red[i]);
   const float scale = a / 127.0f;  // IEEE single-precision division
   if (threadIdx.x == 0) xs[t] = scale;
+  const float inv = 1.0f / scale;
+  const bool fast = quant_fast(scale);
   for (int c = threadIdx.x; c < chunks; c += kQThreads) {
     uint32_t out[2] = {0u, 0u};
     if (a > 0.f) {
@@ -87,10 +122,8 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float r0 = rintf(bf16_lo(w[j]) / scale);
-        float r1 = rintf(bf16_hi(w[j]) / scale);
-        r0 = fminf(fmaxf(r0, -127.f), 127.f);
-        r1 = fminf(fmaxf(r1, -127.f), 127.f);
+        const float r0 = quant_code(bf16_lo(w[j]), scale, inv, fast);
+        const float r1 = quant_code(bf16_hi(w[j]), scale, inv, fast);
         const uint32_t b0 = static_cast<uint32_t>(static_cast<int>(r0)) & 0xFFu;
         const uint32_t b1 = static_cast<uint32_t>(static_cast<int>(r1)) & 0xFFu;
         out[j >> 1] |= (b0 | (b1 << 8)) << (16 * (j & 1));
@@ -105,19 +138,43 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
 // p2 = q - p1 (multiples of 16 up to 128, and integers in [-8, 7]: all exact
 // in e4m3), written as p1[T][K] and p2[T][K] in the decoder's k order: within
 // every 16-wide block of k, byte slot 4i + b holds k = 4b + i.
-// rotate: the token's row is first Hadamard-rotated blockwise (each warp a
-// 1024-wide block at a time, hadamard_block_1024, scaled by 1/32 and rounded
-// once to bf16, nearest-even) into dynamic shared memory (2 K bytes), and
-// quantised from there.
+// The row is read twice (absmax, then codes), so it is staged in dynamic
+// shared memory (2 K bytes) when it fits: stage, with one bulk copy per
+// kQCopy bytes in flight at once (a CTA's loads would otherwise keep too few
+// bytes in flight per SM to cover the latency); rotate: the token's row is
+// first Hadamard-rotated blockwise (each warp a 1024-wide block at a time,
+// hadamard_block_1024, scaled by 1/32 and rounded once to bf16,
+// nearest-even) into shared memory, and quantised from there.  Otherwise both
+// passes read global memory.
+constexpr uint32_t kQCopy = 16384;
 __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t* __restrict__ x,
                                                                  uint8_t* __restrict__ p1,
                                                                  uint8_t* __restrict__ p2,
                                                                  float* __restrict__ xs, int K,
-                                                                 int rotate) {
+                                                                 int rotate, int stage, int* err) {
   extern __shared__ __align__(16) uint16_t xrow[];
+  __shared__ uint64_t row_bar;
   const int t = blockIdx.x;
   const uint16_t* row = x + static_cast<size_t>(t) * K;
-  if (rotate) {
+  if (stage) {
+    const uint32_t bytes = 2u * static_cast<uint32_t>(K);  // K % 16 == 0: 16-byte multiples
+    if (threadIdx.x == 0) {
+      mbar_init(&row_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&row_bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += kQCopy)
+        bulk_load(reinterpret_cast<uint8_t*>(xrow) + off,
+                  reinterpret_cast<const uint8_t*>(row) + off,
+                  bytes - off < kQCopy ? bytes - off : kQCopy, &row_bar);
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+    const bool ok = mbar_wait(&row_bar, 0, err);
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0 && !ok) mbar_wait(&row_bar, 0, err);  // no copy outlives the CTA
+      return;
+    }
+    row = xrow;
+  } else if (rotate) {
     const int lane = threadIdx.x & 31;
     for (int b = threadIdx.x >> 5; b < K / kRotBlock; b += kQThreads / 32) {
       float v[32];
@@ -163,27 +220,57 @@ __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t*
   for (int i = 1; i < kQThreads / 32; ++i) a = fmaxf(a, red[i]);
   const float scale = a / 127.0f;  // IEEE single-precision division
   if (threadIdx.x == 0) xs[t] = scale;
+  const float inv = 1.0f / scale;
+  const bool fast = quant_fast(scale);
   for (int blk = threadIdx.x; blk < (K >> 4); blk += kQThreads) {
     const uint4 v0 = load16(16 * blk);
     const uint4 v1 = load16(16 * blk + 8);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+    // The 16 codes from the product (see quant_code): dmax is the largest
+    // distance of a product from its nearest integer (NaN if any is NaN).
+    // On the fast path |q0| < 127.0001, so the codes need no clamp.  A block
+    // with any product within kQMargin of a half-integer, a row off the fast
+    // path and an all-zero row take the division for all 16 (one branch per
+    // block; a block needs it with probability about 1e-3).
+    float r[16];
+    float dmax = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      int q = 0;
-      if (a > 0.f) {
-        const float v = (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
-        const float r = fminf(fmaxf(rintf(v / scale), -127.f), 127.f);
-        q = static_cast<int>(r);
-      }
-      const int h = (q + 8) >> 4;  // floor((q + 8) / 16), in [-8, 8]
-      const uint32_t e1 = __nv_cvt_float_to_fp8(static_cast<float>(16 * h), __NV_SATFINITE,
-                                                __NV_E4M3);
-      const uint32_t e2 = __nv_cvt_float_to_fp8(static_cast<float>(q - 16 * h), __NV_SATFINITE,
-                                                __NV_E4M3);
-      const int slot = 4 * (k & 3) + (k >> 2);  // k = 4b + i -> slot 4i + b
-      o1[slot >> 2] |= e1 << (8 * (slot & 3));
-      o2[slot >> 2] |= e2 << (8 * (slot & 3));
+      const float q0 = ((k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1])) * inv;
+      r[k] = rintf(q0);
+      dmax = fmax_nan(dmax, fabsf(q0 - r[k]));
+    }
+    if (!(fast && dmax < 0.5f - kQMargin)) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        r[k] = a > 0.f ? quant_code((k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]), scale,
+                                    inv, false)
+                       : 0.f;
+    }
+    // pieces of the codes as exact floats: h = floor((q + 8) / 16) in
+    // [-8, 8], p1 = 16 h, p2 = q - p1 (every step exact in fp32)
+    float f1[16], f2[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float h = floorf(fmaf(r[k], 0.0625f, 0.5f));
+      f1[k] = 16.0f * h;
+      f2[k] = fmaf(-16.0f, h, r[k]);
+    }
+    // word i of a piece block holds k = i, i + 4, i + 8, i + 12 in bytes 0..3
+    // (slot 4i + b holds k = 4b + i), converted two at a time
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o1[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i], f1[i + 4]),
+                                                             __NV_SATFINITE, __NV_E4M3)) |
+              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i + 8], f1[i + 12]),
+                                                              __NV_SATFINITE, __NV_E4M3))
+               << 16);
+      o2[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i], f2[i + 4]),
+                                                             __NV_SATFINITE, __NV_E4M3)) |
+              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i + 8], f2[i + 12]),
+                                                              __NV_SATFINITE, __NV_E4M3))
+               << 16);
     }
     const size_t off = static_cast<size_t>(t) * K + 16 * blk;
     *reinterpret_cast<uint4*>(p1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
@@ -359,9 +446,11 @@ cudaError_t quant_set_attributes() {
 }
 
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
-                                int K, int rotate, cudaStream_t stream) {
-  const size_t smem = rotate ? 2 * static_cast<size_t>(K) : 0;
-  quant_pieces_kernel<<<T, kQThreads, smem, stream>>>(x, p1, p2, xs, K, rotate);
+                                int K, int rotate, int* err, cudaStream_t stream) {
+  // rotated rows are always staged (K <= kRotateMaxK); plain rows when they fit
+  const int stage = !rotate && K <= kRotateMaxK;
+  const size_t smem = (rotate || stage) ? 2 * static_cast<size_t>(K) : 0;
+  quant_pieces_kernel<<<T, kQThreads, smem, stream>>>(x, p1, p2, xs, K, rotate, stage, err);
   return cudaGetLastError();
 }
 

@@ -170,6 +170,62 @@ def test_quant_s8_golden_ties_and_zero_row(tl):
     assert float(xs[0].item()) == 1.0
 
 
+def _every_bf16_up_to(absmax_values, K, seed):
+    """bf16 bits [len(absmax_values), K]: row t holds every finite bf16
+    magnitude <= a_t (a_t itself first), random signs, zeros after."""
+    rng = np.random.default_rng(seed)
+    codes = np.arange(0, 0x7F80, dtype=np.uint32)          # every finite bf16 >= 0
+    mags = (codes << 16).view(np.float32)
+    rows = np.zeros((len(absmax_values), K), dtype=np.uint16)
+    for t, a in enumerate(absmax_values):
+        a_bits = np.uint16(np.array([a], dtype=np.float32).view(np.uint32)[0] >> 16)
+        a_bf = float((np.uint32(a_bits) << 16).view(np.float32))
+        sel = codes[(mags <= a_bf) & (codes != a_bits)].astype(np.uint16)
+        assert 1 + len(sel) <= K
+        sign = rng.integers(0, 2, size=len(sel)).astype(np.uint16) << 15
+        rows[t, 0] = a_bits
+        rows[t, 1:1 + len(sel)] = sel | sign
+    return rows
+
+
+# absmax values whose scale a / 127 is normal (the product-and-check path)
+# or below 2^-126 (every element divides), including a bf16 subnormal
+_EVERY_A = [127.0, 100.0, 3.3, 1e-3, 6.0e4, 3.0e38, 2e-36, 1e-36, 1e-39]
+
+
+def test_quant_s8_every_bf16_value(tl):
+    # every finite bf16 magnitude up to each absmax, both signs: the codes
+    # equal rint(x / scale) with the quotient rounded as an IEEE division
+    import torch
+    K = 32768
+    xb = _every_bf16_up_to(_EVERY_A, K, seed=3)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    q, xs = tl.tern_quant_act_s8(x)
+    q_ref, xs_ref = oracle.quant_s8(xb, len(_EVERY_A), K)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_s8_pieces_every_bf16_value(tl):
+    # The same rows through the s8 rung, whose own quantiser splits the codes
+    # into two fp8 pieces: with unit scales the integer sums are exact (|acc|
+    # < 2^24), so y = fl(x_scale * acc) bit for bit.
+    K, N = 32768, 128
+    xb = _every_bf16_up_to(_EVERY_A, K, seed=4)
+    T = len(_EVERY_A)
+    W = synth.ternary_weights(N, K, 0.4, seed=7)
+    s = np.ones((N, K // 128), dtype=np.float16)
+    Wd, sd, xd = _dev_case(W, s, xb)
+    Wp = tl.tern_pack(Wd)
+    with forced_rung(tl, "s8"):
+        y = tl.tern_linear(Wp, sd, xd).cpu().numpy()
+    q_ref, xs_ref = oracle.quant_s8(xb, T, K)
+    acc = q_ref.astype(np.int64) @ W.astype(np.int64).T
+    assert np.abs(acc).max() < 2 ** 24
+    expect = xs_ref.astype(np.float32)[:, None] * acc.astype(np.float32)
+    assert np.array_equal(y.view(np.uint32), expect.view(np.uint32))
+
+
 # ---------------------------------------------------------------- every rung, every band
 
 @pytest.mark.parametrize("rung", RUNGS)
