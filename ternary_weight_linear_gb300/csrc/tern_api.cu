@@ -427,7 +427,7 @@ int tern_linear(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t*
       uint8_t* p1 = scratch;
       uint8_t* p2 = scratch + piece;
       float* xs = reinterpret_cast<float*>(scratch + 2 * piece);
-      if (launch_quant_pieces(x, p1, p2, xs, T, K, rotate, d->err, st) != cudaSuccess)
+      if (launch_quant_pieces(x, p1, p2, xs, T, K, rotate, d->sms, d->err, st) != cudaSuccess)
         return TERN_ECUDA;
       ++launches;
       CUtensorMap tmW, tmP1, tmP2;

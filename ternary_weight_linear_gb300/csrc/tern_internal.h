@@ -128,7 +128,7 @@ cudaError_t launch_quant_s8(const uint16_t* x, int8_t* q, float* xs, int T, int 
 // rotate: quantise the blockwise Hadamard rotation of x (K % 1024 == 0,
 // K <= kRotateMaxK: the rotated row is staged in shared memory).
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
-                                int K, int rotate, int* err, cudaStream_t stream);
+                                int K, int rotate, int num_sms, int* err, cudaStream_t stream);
 cudaError_t quant_set_attributes();
 
 // Base-3 packed weights (26 bytes per 128-weight group) -> 2-bit codes.

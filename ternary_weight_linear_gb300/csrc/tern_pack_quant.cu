@@ -77,6 +77,31 @@ __device__ __forceinline__ float quant_code(float v, float scale, float inv, boo
   }
   return fminf(fmaxf(r, -127.f), 127.f);
 }
+// Pairs of fp32 values in one 64-bit register for the packed fp32x2
+// arithmetic (each half rounded as its scalar instruction would be).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 // max of two floats that propagates NaN (IEEE maximum, not maximumNumber)
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float d;
@@ -134,47 +159,136 @@ __global__ void __launch_bounds__(kQThreads) quant_s8_kernel(const uint16_t* __r
 }
 
 // s8 rung input: the codes q of quant_s8_kernel (same arithmetic), split
-// exactly into two fp8 e4m3 pieces p1 = 16 floor((q + 8) / 16) and
-// p2 = q - p1 (multiples of 16 up to 128, and integers in [-8, 7]: all exact
+// exactly into two fp8 e4m3 pieces p1 = 16 rint(q / 16) (ties to even) and
+// p2 = q - p1 (multiples of 16 up to 128, and integers in [-8, 8]: all exact
 // in e4m3), written as p1[T][K] and p2[T][K] in the decoder's k order: within
 // every 16-wide block of k, byte slot 4i + b holds k = 4b + i.
-// The row is read twice (absmax, then codes), so it is staged in dynamic
-// shared memory (2 K bytes) when it fits: stage, with one bulk copy per
-// kQCopy bytes in flight at once (a CTA's loads would otherwise keep too few
-// bytes in flight per SM to cover the latency); rotate: the token's row is
-// first Hadamard-rotated blockwise (each warp a 1024-wide block at a time,
-// hadamard_block_1024, scaled by 1/32 and rounded once to bf16,
-// nearest-even) into shared memory, and quantised from there.  Otherwise both
-// passes read global memory.
+// Codes and pieces of token t's row (global or shared memory): absmax, then
+// the pieces of every 16-wide block.  red: kQThreads / 32 floats of shared
+// memory.  Ends without a barrier.
+__device__ __forceinline__ void quant_row_pieces(const uint16_t* row, int t, int K,
+                                                 uint8_t* __restrict__ p1,
+                                                 uint8_t* __restrict__ p2,
+                                                 float* __restrict__ xs, float* red) {
+  // (plain 16-byte loads: row is global or shared memory)
+  auto load16 = [&](int e) { return *reinterpret_cast<const uint4*>(row + e); };
+  const int chunks = K >> 3;
+  float a = 0.f;
+  for (int c = threadIdx.x; c < chunks; c += kQThreads) {
+    const uint4 v = load16(8 * c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  a = red[0];
+#pragma unroll
+  for (int i = 1; i < kQThreads / 32; ++i) a = fmaxf(a, red[i]);
+  const float scale = a / 127.0f;  // IEEE single-precision division
+  if (threadIdx.x == 0) xs[t] = scale;
+  const float inv = 1.0f / scale;
+  const bool fast = quant_fast(scale);
+  for (int blk = threadIdx.x; blk < (K >> 4); blk += kQThreads) {
+    const uint4 v0 = load16(16 * blk);
+    const uint4 v1 = load16(16 * blk + 8);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    // The 16 codes from the product (see quant_code): dmax is the largest
+    // distance of a product from its nearest integer (NaN if any is NaN).
+    // On the fast path |q0| < 127.0001, so the codes need no clamp.  A block
+    // with any product within kQMargin of a half-integer, a row off the fast
+    // path and an all-zero row take the division for all 16 (one branch per
+    // block; a block needs it with probability about 1e-3).
+    float r[16];
+    float dmax = 0.f;
+    const uint64_t inv2 = pack_f32x2(inv, inv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // elements 2j, 2j + 1 as one fp32 pair
+      const uint64_t q2 = mul_f32x2(pack_f32x2(bf16_lo(w[j]), bf16_hi(w[j])), inv2);
+      float q0a, q0b;
+      unpack_f32x2(q2, q0a, q0b);
+      r[2 * j] = rintf(q0a);
+      r[2 * j + 1] = rintf(q0b);
+      float da, db;
+      unpack_f32x2(sub_f32x2(q2, pack_f32x2(r[2 * j], r[2 * j + 1])), da, db);
+      dmax = fmax_nan(dmax, fabsf(da));
+      dmax = fmax_nan(dmax, fabsf(db));
+    }
+    if (!(fast && dmax < 0.5f - kQMargin)) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        r[k] = a > 0.f ? quant_code((k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]), scale,
+                                    inv, false)
+                       : 0.f;
+    }
+    // pieces of the codes as exact floats, two at a time: p1 = 16 rint(q /
+    // 16) (q / 16 + 1.5 * 2^23 rounds to an integer, ties to even), p2 = q -
+    // p1 in [-8, 8]; every step is exact in fp32
+    float f1[16], f2[16];
+    const uint64_t c16th = pack_f32x2(0.0625f, 0.0625f), cbig = pack_f32x2(12582912.f, 12582912.f);
+    const uint64_t c16 = pack_f32x2(16.f, 16.f), cneg = pack_f32x2(-201326592.f, -201326592.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint64_t r2 = pack_f32x2(r[2 * j], r[2 * j + 1]);
+      const uint64_t p12 = fma_f32x2(fma_f32x2(r2, c16th, cbig), c16, cneg);
+      unpack_f32x2(p12, f1[2 * j], f1[2 * j + 1]);
+      unpack_f32x2(sub_f32x2(r2, p12), f2[2 * j], f2[2 * j + 1]);
+    }
+    // word i of a piece block holds k = i, i + 4, i + 8, i + 12 in bytes 0..3
+    // (slot 4i + b holds k = 4b + i), converted two at a time
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o1[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i], f1[i + 4]),
+                                                             __NV_SATFINITE, __NV_E4M3)) |
+              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i + 8], f1[i + 12]),
+                                                              __NV_SATFINITE, __NV_E4M3))
+               << 16);
+      o2[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i], f2[i + 4]),
+                                                             __NV_SATFINITE, __NV_E4M3)) |
+              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i + 8], f2[i + 12]),
+                                                              __NV_SATFINITE, __NV_E4M3))
+               << 16);
+    }
+    const size_t off = static_cast<size_t>(t) * K + 16 * blk;
+    *reinterpret_cast<uint4*>(p1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    *reinterpret_cast<uint4*>(p2 + off) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+}
+
+
+// The row is read twice (absmax, then codes).  Three ways to hold it:
+//   staged (K <= kRotateMaxK): persistent CTAs walk the tokens; each copies
+//     its next token's row into one of two shared-memory buffers (bulk
+//     copies of up to kQCopy bytes) while it quantises the current one (one
+//     buffer when two do not fit: the copy then precedes each token);
+//   rotate: one CTA per token Hadamard-rotates the row blockwise (each warp a
+//     1024-wide block at a time, hadamard_block_1024, scaled by 1/32 and
+//     rounded once to bf16, nearest-even) into shared memory;
+//   otherwise one CTA per token reads global memory twice.
 constexpr uint32_t kQCopy = 16384;
+constexpr size_t kQSmemPerSm = 228 * 1024;  // shared memory of an SM
+constexpr int kQCtasPerSm = 4;              // the kernel's registers allow four CTAs
+enum : int { kQGlobal = 0, kQRotate = 1, kQStaged = 2 };
 __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t* __restrict__ x,
                                                                  uint8_t* __restrict__ p1,
                                                                  uint8_t* __restrict__ p2,
-                                                                 float* __restrict__ xs, int K,
-                                                                 int rotate, int stage, int* err) {
+                                                                 float* __restrict__ xs, int T,
+                                                                 int K, int mode, int nbuf,
+                                                                 int* err) {
   extern __shared__ __align__(16) uint16_t xrow[];
-  __shared__ uint64_t row_bar;
-  const int t = blockIdx.x;
-  const uint16_t* row = x + static_cast<size_t>(t) * K;
-  if (stage) {
-    const uint32_t bytes = 2u * static_cast<uint32_t>(K);  // K % 16 == 0: 16-byte multiples
-    if (threadIdx.x == 0) {
-      mbar_init(&row_bar, 1);
-      fence_mbar_init();
-      mbar_arrive_expect_tx(&row_bar, bytes);
-      for (uint32_t off = 0; off < bytes; off += kQCopy)
-        bulk_load(reinterpret_cast<uint8_t*>(xrow) + off,
-                  reinterpret_cast<const uint8_t*>(row) + off,
-                  bytes - off < kQCopy ? bytes - off : kQCopy, &row_bar);
-    }
-    __syncthreads();  // the barrier is initialised before anyone waits on it
-    const bool ok = mbar_wait(&row_bar, 0, err);
-    if (!__syncthreads_and(ok)) {
-      if (threadIdx.x == 0 && !ok) mbar_wait(&row_bar, 0, err);  // no copy outlives the CTA
-      return;
-    }
-    row = xrow;
-  } else if (rotate) {
+  __shared__ uint64_t row_bar[2];
+  __shared__ float red[kQThreads / 32];
+  if (mode == kQGlobal) {
+    const int t = blockIdx.x;
+    quant_row_pieces(x + static_cast<size_t>(t) * K, t, K, p1, p2, xs, red);
+    return;
+  }
+  if (mode == kQRotate) {
+    const int t = blockIdx.x;
+    const uint16_t* row = x + static_cast<size_t>(t) * K;
     const int lane = threadIdx.x & 31;
     for (int b = threadIdx.x >> 5; b < K / kRotBlock; b += kQThreads / 32) {
       float v[32];
@@ -198,83 +312,50 @@ __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t*
       }
     }
     __syncthreads();
-    row = xrow;
+    quant_row_pieces(xrow, t, K, p1, p2, xs, red);
+    return;
   }
-  // (plain 16-byte loads: row is global or, rotated, shared memory)
-  auto load16 = [&](int e) { return *reinterpret_cast<const uint4*>(row + e); };
-  const int chunks = K >> 3;
-  float a = 0.f;
-  for (int c = threadIdx.x; c < chunks; c += kQThreads) {
-    const uint4 v = load16(8 * c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  // staged
+  const uint32_t bytes = 2u * static_cast<uint32_t>(K);  // K % 16 == 0: 16-byte multiples
+  auto issue = [&](int tt, int b) {  // one thread: token tt's row into buffer b
+    mbar_arrive_expect_tx(&row_bar[b], bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(x + static_cast<size_t>(tt) * K);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(xrow + static_cast<size_t>(b) * K);
+    for (uint32_t off = 0; off < bytes; off += kQCopy)
+      bulk_load(dst + off, src + off, bytes - off < kQCopy ? bytes - off : kQCopy, &row_bar[b]);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&row_bar[0], 1);
+    mbar_init(&row_bar[1], 1);
+    fence_mbar_init();
+    if (static_cast<int>(blockIdx.x) < T) issue(blockIdx.x, 0);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  __shared__ float red[kQThreads / 32];
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
-  __syncthreads();
-  a = red[0];
-#pragma unroll
-  for (int i = 1; i < kQThreads / 32; ++i) a = fmaxf(a, red[i]);
-  const float scale = a / 127.0f;  // IEEE single-precision division
-  if (threadIdx.x == 0) xs[t] = scale;
-  const float inv = 1.0f / scale;
-  const bool fast = quant_fast(scale);
-  for (int blk = threadIdx.x; blk < (K >> 4); blk += kQThreads) {
-    const uint4 v0 = load16(16 * blk);
-    const uint4 v1 = load16(16 * blk + 8);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    // The 16 codes from the product (see quant_code): dmax is the largest
-    // distance of a product from its nearest integer (NaN if any is NaN).
-    // On the fast path |q0| < 127.0001, so the codes need no clamp.  A block
-    // with any product within kQMargin of a half-integer, a row off the fast
-    // path and an all-zero row take the division for all 16 (one branch per
-    // block; a block needs it with probability about 1e-3).
-    float r[16];
-    float dmax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float q0 = ((k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1])) * inv;
-      r[k] = rintf(q0);
-      dmax = fmax_nan(dmax, fabsf(q0 - r[k]));
+  __syncthreads();  // the barriers are initialised before anyone waits on them
+  int i = 0;
+  for (int t = blockIdx.x; t < T; t += gridDim.x, ++i) {
+    const int b = nbuf == 2 ? (i & 1) : 0;
+    const uint32_t par = nbuf == 2 ? ((i >> 1) & 1) : (i & 1);
+    const int tn = t + gridDim.x;
+    // buffer b ^ 1 was last read in the previous iteration, which ended with
+    // a barrier
+    if (nbuf == 2 && threadIdx.x == 0 && tn < T) {
+      fence_proxy_async_smem();
+      issue(tn, b ^ 1);
     }
-    if (!(fast && dmax < 0.5f - kQMargin)) {
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        r[k] = a > 0.f ? quant_code((k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]), scale,
-                                    inv, false)
-                       : 0.f;
+    const bool ok = mbar_wait(&row_bar[b], par, err);
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0) {  // no copy outlives the CTA
+        mbar_wait(&row_bar[b], par, err);
+        if (nbuf == 2 && tn < T) mbar_wait(&row_bar[b ^ 1], ((i + 1) >> 1) & 1, err);
+      }
+      return;
     }
-    // pieces of the codes as exact floats: h = floor((q + 8) / 16) in
-    // [-8, 8], p1 = 16 h, p2 = q - p1 (every step exact in fp32)
-    float f1[16], f2[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float h = floorf(fmaf(r[k], 0.0625f, 0.5f));
-      f1[k] = 16.0f * h;
-      f2[k] = fmaf(-16.0f, h, r[k]);
+    quant_row_pieces(xrow + static_cast<size_t>(b) * K, t, K, p1, p2, xs, red);
+    __syncthreads();  // buffer b and red are free again
+    if (nbuf == 1 && threadIdx.x == 0 && tn < T) {
+      fence_proxy_async_smem();
+      issue(tn, 0);
     }
-    // word i of a piece block holds k = i, i + 4, i + 8, i + 12 in bytes 0..3
-    // (slot 4i + b holds k = 4b + i), converted two at a time
-    uint32_t o1[4], o2[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o1[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i], f1[i + 4]),
-                                                             __NV_SATFINITE, __NV_E4M3)) |
-              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f1[i + 8], f1[i + 12]),
-                                                              __NV_SATFINITE, __NV_E4M3))
-               << 16);
-      o2[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i], f2[i + 4]),
-                                                             __NV_SATFINITE, __NV_E4M3)) |
-              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(f2[i + 8], f2[i + 12]),
-                                                              __NV_SATFINITE, __NV_E4M3))
-               << 16);
-    }
-    const size_t off = static_cast<size_t>(t) * K + 16 * blk;
-    *reinterpret_cast<uint4*>(p1 + off) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    *reinterpret_cast<uint4*>(p2 + off) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
   }
 }
 
@@ -446,11 +527,24 @@ cudaError_t quant_set_attributes() {
 }
 
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
-                                int K, int rotate, int* err, cudaStream_t stream) {
-  // rotated rows are always staged (K <= kRotateMaxK); plain rows when they fit
-  const int stage = !rotate && K <= kRotateMaxK;
-  const size_t smem = (rotate || stage) ? 2 * static_cast<size_t>(K) : 0;
-  quant_pieces_kernel<<<T, kQThreads, smem, stream>>>(x, p1, p2, xs, K, rotate, stage, err);
+                                int K, int rotate, int num_sms, int* err, cudaStream_t stream) {
+  if (rotate) {  // K <= kRotateMaxK: the rotated row fits
+    quant_pieces_kernel<<<T, kQThreads, 2 * static_cast<size_t>(K), stream>>>(
+        x, p1, p2, xs, T, K, kQRotate, 1, err);
+  } else if (K <= kRotateMaxK) {
+    // two row buffers when they fit the kernel's shared-memory allowance;
+    // as many CTAs as fit per SM (at most kQCtasPerSm: registers)
+    const int nbuf = 4 * static_cast<size_t>(K) <= 2 * static_cast<size_t>(kRotateMaxK) ? 2 : 1;
+    const size_t smem = 2 * static_cast<size_t>(K) * nbuf;
+    int per_sm = static_cast<int>(kQSmemPerSm / (smem + 1024));
+    if (per_sm > kQCtasPerSm) per_sm = kQCtasPerSm;
+    if (per_sm < 1) per_sm = 1;
+    const int grid = T < per_sm * num_sms ? T : per_sm * num_sms;
+    quant_pieces_kernel<<<grid, kQThreads, smem, stream>>>(x, p1, p2, xs, T, K, kQStaged, nbuf,
+                                                           err);
+  } else {
+    quant_pieces_kernel<<<T, kQThreads, 0, stream>>>(x, p1, p2, xs, T, K, kQGlobal, 1, err);
+  }
   return cudaGetLastError();
 }
 

@@ -7,7 +7,7 @@
 // integers travel as exact fp8 e4m3 values:
 //   * w / 8 in {-1/8, 0, 1/8} (the packed code decodes to it with a shift and
 //     an AND, as in the small-T rungs);
-//   * q = p1 + p2 with p1 = 16 floor((q + 8) / 16) and p2 = q - p1, both
+//   * q = p1 + p2 with p1 = 16 rint(q / 16) and p2 = q - p1, both
 //     exact in e4m3 (prepared by the pieces quantiser);
 // and the two pieces are fed as two halves of the contraction into the same
 // fp32 accumulator, which then holds exactly acc / 8 (|acc| <= 127 * 128, far

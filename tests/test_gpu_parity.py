@@ -300,6 +300,14 @@ def test_s8_deep_ring_ragged(tl):
                        samples=8192) == "s8"
 
 
+@pytest.mark.parametrize("K,N,T", [(1024, 64, 3000), (40960, 64, 40), (65664, 16, 20)])
+def test_s8_quantiser_row_modes(tl, K, N, T):
+    # The s8 rung's activation quantiser keeps a token's row in shared memory:
+    # two buffers per CTA with many tokens per CTA (K = 1024, T = 3000), one
+    # buffer (K = 40960), or none, reading global memory (K = 65664).
+    assert _check_case(tl, synth.case("qmode", T, K=K, N=N, seed=K + T, outliers=True), "s8") == "s8"
+
+
 @pytest.mark.parametrize("K,N,T", [(128, 1, 17), (256, 129, 33), (1152, 521, 200), (2048, 300, 129)])
 def test_shapes_bf16_rung(tl, K, N, T):
     # the exact bf16 prefill rung on ragged shapes (N % 4 != 0: y stored directly)
