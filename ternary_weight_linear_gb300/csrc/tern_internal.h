@@ -119,6 +119,23 @@ cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUt
                       int* tickets, float* partials, int num_sms, size_t l2_bytes, int* err,
                       cudaStream_t stream);
 
+// Launch configuration of a programmatic dependent launch (the kernel may
+// start while the previous kernel in the stream finishes; it waits for that
+// kernel's results with griddepcontrol.wait).  attr: one attribute slot.
+inline cudaLaunchConfig_t pdl_launch_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block,
+                                            size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // Pack and quantise.
 cudaError_t launch_pack(const int8_t* W, uint32_t* Wp, int K, int N, int* bad, int num_sms,
                         cudaStream_t stream);

@@ -281,6 +281,8 @@ __global__ void __launch_bounds__(kQThreads) quant_pieces_kernel(const uint16_t*
   extern __shared__ __align__(16) uint16_t xrow[];
   __shared__ uint64_t row_bar[2];
   __shared__ float red[kQThreads / 32];
+  grid_dependents_launch();
+  grid_dependency_wait();  // x and the output buffers come from earlier work
   if (mode == kQGlobal) {
     const int t = blockIdx.x;
     quant_row_pieces(x + static_cast<size_t>(t) * K, t, K, p1, p2, xs, red);
@@ -528,9 +530,12 @@ cudaError_t quant_set_attributes() {
 
 cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, float* xs, int T,
                                 int K, int rotate, int num_sms, int* err, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
   if (rotate) {  // K <= kRotateMaxK: the rotated row fits
-    quant_pieces_kernel<<<T, kQThreads, 2 * static_cast<size_t>(K), stream>>>(
-        x, p1, p2, xs, T, K, kQRotate, 1, err);
+    const cudaLaunchConfig_t cfg =
+        pdl_launch_config(attr, dim3(T), dim3(kQThreads), 2 * static_cast<size_t>(K), stream);
+    return cudaLaunchKernelEx(&cfg, quant_pieces_kernel, x, p1, p2, xs, T, K,
+                              static_cast<int>(kQRotate), 1, err);
   } else if (K <= kRotateMaxK) {
     // two row buffers when they fit the kernel's shared-memory allowance;
     // as many CTAs as fit per SM (at most kQCtasPerSm: registers)
@@ -540,12 +545,13 @@ cudaError_t launch_quant_pieces(const uint16_t* x, uint8_t* p1, uint8_t* p2, flo
     if (per_sm > kQCtasPerSm) per_sm = kQCtasPerSm;
     if (per_sm < 1) per_sm = 1;
     const int grid = T < per_sm * num_sms ? T : per_sm * num_sms;
-    quant_pieces_kernel<<<grid, kQThreads, smem, stream>>>(x, p1, p2, xs, T, K, kQStaged, nbuf,
-                                                           err);
-  } else {
-    quant_pieces_kernel<<<T, kQThreads, 0, stream>>>(x, p1, p2, xs, T, K, kQGlobal, 1, err);
+    const cudaLaunchConfig_t cfg = pdl_launch_config(attr, dim3(grid), dim3(kQThreads), smem, stream);
+    return cudaLaunchKernelEx(&cfg, quant_pieces_kernel, x, p1, p2, xs, T, K,
+                              static_cast<int>(kQStaged), nbuf, err);
   }
-  return cudaGetLastError();
+  const cudaLaunchConfig_t cfg = pdl_launch_config(attr, dim3(T), dim3(kQThreads), 0, stream);
+  return cudaLaunchKernelEx(&cfg, quant_pieces_kernel, x, p1, p2, xs, T, K,
+                            static_cast<int>(kQGlobal), 1, err);
 }
 
 }  // namespace tern

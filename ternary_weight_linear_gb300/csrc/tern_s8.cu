@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 int nfull, int chunks,
                 int* __restrict__ tickets, float* __restrict__ partials, int* err) {
   using L = SL<TOK, NST>;
+  grid_dependents_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -192,6 +193,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the set-up above overlaps the previous kernel; the pieces, x_scale, y and
+  // the workspace belong to it until it has finished
+  grid_dependency_wait();
 
   if (warp == kProdW) {
     // ------------------------------------------------------------ producer
@@ -467,12 +471,14 @@ cudaError_t launch_s8(const CUtensorMap* tmW, const CUtensorMap* tmP1, const CUt
   const int tok = s8_token_tile(T), nst = s8_stages(T, K, l2_bytes);
   const int tiles = ((N + kRowsS - 1) / kRowsS) * ((T + tok - 1) / tok);
   const TileSplit sp = tile_split(tiles, K / 128, num_sms);
+  cudaLaunchAttribute attr[1];
 #define TERN_S8_LAUNCH(TOK, NST)                                                            \
   if (tok == TOK && nst == NST) {                                                           \
-    s8tc_kernel<TOK, NST><<<sp.P, kThreadsS, SL<TOK, NST>::kAlloc, stream>>>(               \
-        *tmW, *tmP1, *tmP2, scales, x_scale, y, T, K, N, sp.nfull, sp.chunks, tickets,       \
-        partials, err);                                                                     \
-    return cudaGetLastError();                                                              \
+    const cudaLaunchConfig_t cfg =                                                          \
+        pdl_launch_config(attr, dim3(sp.P), dim3(kThreadsS), SL<TOK, NST>::kAlloc, stream); \
+    return cudaLaunchKernelEx(&cfg, s8tc_kernel<TOK, NST>, *tmW, *tmP1, *tmP2, scales,      \
+                              x_scale, y, T, K, N, sp.nfull, sp.chunks, tickets, partials,  \
+                              err);                                                         \
   }
   TERN_S8_INSTANCES(TERN_S8_LAUNCH)
 #undef TERN_S8_LAUNCH
