@@ -5,7 +5,13 @@ torch's own float8 conversions.
 
 - The 2-bit code turns into the e4m3 encoding of w / 8 with one mask.
 - s8 rung: every int8 code q in [-127, 127] is the exact sum of two e4m3
-  values 16 * floor((q + 8) / 16) and the remainder in [-8, 7].
+  values 16 * floor((q + 8) / 16) and the remainder in [-8, 7] (the int8
+  decode variant's split), and of 16 * rint(q / 16) and the remainder in
+  [-8, 8] (the s8 quantiser's split, through its fp32 magic-number steps).
+- s8 quantiser: the code rint(x * (1/scale)) equals rint(x / scale) (the
+  quotient rounded once) wherever the product lies at least 2^-15 from a
+  half-integer, for every finite bf16 x up to the row's absmax, and the
+  product is never farther than 1.91e-5 from the rounded quotient.
 - bf16 rungs: a bf16 value scaled into (-2^15, 2^15) splits as h1 = e5m2(v),
   h2 = e5m2(v - h1), h3 = e5m2(v - h1 - h2) with h1 + h2 + h3 == v whenever
   |v| >= 2^-7, every nonzero piece a normal e5m2 value and every fp32
@@ -77,6 +83,56 @@ def test_int8_codes_split_into_two_exact_e4m3_pieces():
     assert np.array_equal(_e4m3(p1), p1.astype(np.float64))
     assert np.array_equal(_e4m3(p2), p2.astype(np.float64))
     assert np.array_equal(p1 + p2, q)
+
+
+def test_int8_codes_split_by_rint_in_fp32():
+    # the s8 quantiser's steps on fp32 values: t = q / 16 + 1.5 * 2^23 (one
+    # rounding: q / 16 is exact), p1 = 16 t - 16 * 1.5 * 2^23 (exact), p2 = q - p1
+    q = np.arange(-127, 128).astype(np.float32)
+    t = q * np.float32(0.0625) + np.float32(12582912.0)
+    p1 = t * np.float32(16.0) - np.float32(201326592.0)
+    p2 = q - p1
+    qi = np.arange(-127, 128)
+    h = np.rint(qi / 16.0)                      # ties to even
+    assert np.array_equal(p1.astype(np.int64), 16 * h.astype(np.int64))
+    assert p1.min() == -128 and p1.max() == 128 and np.all(p1 % 16 == 0)
+    assert p2.min() == -8 and p2.max() == 8
+    assert np.array_equal(_e4m3(p1), p1.astype(np.float64))
+    assert np.array_equal(_e4m3(p2), p2.astype(np.float64))
+    assert np.array_equal((p1 + p2).astype(np.int64), qi)
+
+
+def _bf16_magnitudes_up_to(a):
+    codes = np.arange(0, 0x7F80, dtype=np.uint32)
+    mags = (codes << 16).view(np.float32)
+    return mags[mags <= a]
+
+
+def test_quant_product_and_check_matches_the_division():
+    # scales on the product path (scale = absmax / 127 normal), absmax values
+    # in bf16 from 2^-118 up to the largest finite bf16
+    rng = np.random.default_rng(8)
+    codes = np.unique(np.concatenate([rng.integers(0x0480, 0x7F80, size=40),
+                                      [0x3F80, 0x42FE, 0x7F7F, 0x0480]])).astype(np.uint32)
+    margin = np.float32(2.0 ** -15)
+    for c in codes:
+        a = (np.uint32(c) << 16).view(np.float32)
+        scale = np.float32(a) / np.float32(127.0)
+        assert scale >= np.float32(2.0 ** -126)           # the kernel's fast-path test
+        inv = np.float32(1.0) / scale
+        v = _bf16_magnitudes_up_to(a)
+        v = np.concatenate([v, -v])
+        quot = v / scale                                  # rounded once (IEEE)
+        q0 = v * inv                                      # rounded product
+        prod = v.astype(np.float64) * np.float64(inv)     # exact product (FMA-contracted form)
+        assert np.abs(q0.astype(np.float64) - quot).max() < 1.91e-5
+        assert np.abs(prod - quot).max() < 1.91e-5
+        for qq in (q0.astype(np.float64), prod):
+            r = np.rint(q0)
+            safe = np.abs(qq - r) < 0.5 - margin
+            assert np.array_equal(r[safe], np.rint(quot)[safe])
+            # and the product path never leaves [-127, 127]
+            assert np.abs(r).max() <= 127
 
 
 def test_rne_e5m2_agrees_with_torch():
