@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                   const __grid_constant__ CUtensorMap tmY, const uint16_t* __restrict__ scales,
                   float* __restrict__ y, int T, int K, int N, int y_tma, int nfull, int chunks,
                   int* __restrict__ tickets, float* __restrict__ partials, int* err) {
+  grid_dependents_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -187,6 +188,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the set-up above overlaps the previous kernel; the reordered x, y and the
+  // workspace belong to it until it has finished
+  grid_dependency_wait();
 
   if (warp == kProdWB) {
     // ------------------------------------------------------------ producer
@@ -426,6 +430,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 __global__ void __launch_bounds__(256) interleave_kernel(const uint16_t* __restrict__ x,
                                                          uint16_t* __restrict__ xp,
                                                          long long blocks) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // x and the output buffer come from earlier work
   for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < blocks;
        b += static_cast<long long>(gridDim.x) * blockDim.x) {
     const uint4 lo = ldg_nc_v4(x + 16 * b);      // k 0..7
@@ -453,6 +459,8 @@ __global__ void __launch_bounds__(256) interleave_kernel(const uint16_t* __restr
 __global__ void __launch_bounds__(256) interleave_rot_kernel(const uint16_t* __restrict__ x,
                                                              uint16_t* __restrict__ xp,
                                                              long long pairs) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // x and the output buffer come from earlier work
   const int lane = threadIdx.x & 31;
   for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
        w < pairs; w += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
@@ -502,14 +510,18 @@ cudaError_t launch_interleave(const uint16_t* x, uint16_t* xp, int T, int K, int
     const long long pairs = static_cast<long long>(T) * (K / kRotBlock);
     long long blocks = (pairs + 7) / 8;
     if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
-    interleave_rot_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xp, pairs);
-  } else {
-    const long long n16 = static_cast<long long>(T) * (K / 16);
-    long long blocks = (n16 + 255) / 256;
-    if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
-    interleave_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xp, n16);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        pdl_launch_config(attr, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream);
+    return cudaLaunchKernelEx(&cfg, interleave_rot_kernel, x, xp, pairs);
   }
-  return cudaGetLastError();
+  const long long n16 = static_cast<long long>(T) * (K / 16);
+  long long blocks = (n16 + 255) / 256;
+  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_launch_config(attr, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream);
+  return cudaLaunchKernelEx(&cfg, interleave_kernel, x, xp, n16);
 }
 
 cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmY,
@@ -517,10 +529,11 @@ cudaError_t launch_bf16(const CUtensorMap* tmW, const CUtensorMap* tmX, const CU
                         float* partials, int num_sms, int* err, cudaStream_t stream) {
   const int tiles = ((N + kRowsB - 1) / kRowsB) * ((T + kTokB - 1) / kTokB);
   const TileSplit sp = tile_split(tiles, K / 128, num_sms);
-  bf16tc_kernel<<<sp.P, kThreadsB, BL::kAlloc, stream>>>(*tmW, *tmX, tmY ? *tmY : *tmW, scales, y,
-                                                          T, K, N, tmY ? 1 : 0, sp.nfull, sp.chunks,
-                                                          tickets, partials, err);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_launch_config(attr, dim3(sp.P), dim3(kThreadsB), BL::kAlloc, stream);
+  return cudaLaunchKernelEx(&cfg, bf16tc_kernel, *tmW, *tmX, tmY ? *tmY : *tmW, scales, y, T, K,
+                            N, tmY ? 1 : 0, sp.nfull, sp.chunks, tickets, partials, err);
 }
 
 }  // namespace tern
